@@ -1,0 +1,578 @@
+// C ABI of the Dual-Flow decode library: validation, workspace, orchestration of the step,
+// CUDA-graph capture and replay. Every arithmetic step runs in the kernels of this library.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+using namespace df;
+
+namespace df {
+
+// ------------------------------------------------------------------ tensor maps
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+int get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? DF_OK : DF_ERR_CUDA;
+}
+}  // namespace
+
+int encode_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_rows) {
+  if (get_encoder() != DF_OK) return DF_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (row_stride_bytes & 15u)) return DF_ERR_ARG;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DF_OK : DF_ERR_CUDA;
+}
+
+int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                       uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+  if (get_encoder() != DF_OK) return DF_ERR_CUDA;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || (stride1_bytes & 15u) || (stride2_bytes & 15u)) return DF_ERR_ARG;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DF_OK : DF_ERR_CUDA;
+}
+
+}  // namespace df
+
+// ------------------------------------------------------------------ helpers
+namespace {
+
+size_t elem_size(const dualflow_config& c) { return c.dtype == DF_DTYPE_BF16 ? 2 : 4; }
+
+int validate_config(const dualflow_config* c) {
+  if (!c) return DF_ERR_ARG;
+  if (c->dtype != DF_DTYPE_F32 && c->dtype != DF_DTYPE_BF16) return DF_ERR_DTYPE;
+  if (c->n_layers < 0 || c->d_model <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0 || c->head_dim <= 0 ||
+      c->ffn_hidden < 0 || c->vocab < 0 || c->max_batch <= 0 || c->max_ctx <= 0 || c->n_experts < 0)
+    return DF_ERR_ARG;
+  if (c->n_q_heads % c->n_kv_heads != 0 || c->head_dim % 2 != 0) return DF_ERR_SHAPE;
+  if (!(c->rms_eps >= 0.f) || !(c->rope_base > 0.f)) return DF_ERR_ARG;
+  if (c->paged && (c->page_size <= 0 || c->max_pages <= 0)) return DF_ERR_ARG;
+  if (c->n_experts > 0 && (c->topk_primary <= 0 || c->topk_aux <= 0 || c->topk_primary > c->n_experts ||
+                           c->topk_aux > c->n_experts))
+    return DF_ERR_SHAPE;
+  if (c->dtype == DF_DTYPE_BF16) {
+    const int G = c->n_q_heads / c->n_kv_heads;
+    if (c->head_dim != kHeadDim || 2 * G > kMaxGroupRows) return DF_ERR_UNSUPPORTED;
+    if (c->d_model % 64 || c->ffn_hidden % 64 || (c->n_q_heads * c->head_dim) % 64) return DF_ERR_UNSUPPORTED;
+    if (2 * c->max_batch > kGemmMaxAct) return DF_ERR_UNSUPPORTED;
+    if (c->paged && c->page_size != 16 && c->page_size != 32 && c->page_size != 64) return DF_ERR_UNSUPPORTED;
+    if (c->n_experts > 0) return DF_ERR_UNSUPPORTED;
+  } else {
+    if (c->head_dim / 2 > 1024 || c->max_ctx > 40000) return DF_ERR_UNSUPPORTED;
+    if (c->n_experts > 0) return DF_ERR_UNSUPPORTED;
+  }
+  return DF_OK;
+}
+
+template <typename T>
+int dalloc(T** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  return cudaMalloc(reinterpret_cast<void**>(p), bytes) == cudaSuccess ? DF_OK : DF_ERR_OOM;
+}
+
+cudaStream_t S(dualflow_stream s) { return reinterpret_cast<cudaStream_t>(s); }
+
+#define DF_TRY(x)              \
+  do {                         \
+    int _rc = (x);             \
+    if (_rc != DF_OK) return _rc; \
+  } while (0)
+
+int pages_per_seq(const dualflow_config& c) { return c.paged ? (c.max_ctx + c.page_size - 1) / c.page_size : 0; }
+
+GemmArgs gemm_args(const dualflow_ctx* ctx) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  const dualflow_config& c = ctx->cfg;
+  g.n_q_heads = c.n_q_heads;
+  g.n_kv_heads = c.n_kv_heads;
+  g.rope = ctx->rope;
+  g.paged = c.paged;
+  g.page_size = c.paged ? c.page_size : 1;
+  g.max_ctx = c.max_ctx;
+  g.max_pages = c.max_pages;
+  g.pages_per_seq = pages_per_seq(c);
+  return g;
+}
+
+AttnArgs attn_args(const dualflow_ctx* ctx, const dualflow_kv* kv, int layer, int batch, int extra, int aux_on) {
+  AttnArgs a;
+  memset(&a, 0, sizeof(a));
+  const dualflow_config& c = ctx->cfg;
+  a.q = ctx->q;
+  a.o = ctx->o;
+  a.k_cache = kv->k[layer];
+  a.v_cache = kv->v[layer];
+  a.seq_len = kv->seq_len;
+  a.page_table = kv->page_table;
+  a.batch = batch;
+  a.n_q_heads = c.n_q_heads;
+  a.n_kv_heads = c.n_kv_heads;
+  a.paged = c.paged;
+  a.page_size = c.paged ? c.page_size : 1;
+  a.max_ctx = c.max_ctx;
+  a.max_pages = c.max_pages;
+  a.pages_per_seq = pages_per_seq(c);
+  a.extra = extra;
+  a.aux_on = aux_on;
+  return a;
+}
+
+int check_kv(const dualflow_ctx* ctx, const dualflow_kv* kv, int layer) {
+  if (!kv || !kv->k || !kv->v || !kv->seq_len) return DF_ERR_ARG;
+  if (layer < 0 || layer >= kv->n_layers) return DF_ERR_ARG;
+  if (!kv->k[layer] || !kv->v[layer]) return DF_ERR_ARG;
+  if (ctx->cfg.paged && !kv->page_table) return DF_ERR_ARG;
+  return DF_OK;
+}
+
+int check_weights(const dualflow_ctx* ctx, const dualflow_weights* w) {
+  const dualflow_config& c = ctx->cfg;
+  if (!w || w->n_layers != c.n_layers) return DF_ERR_ARG;
+  if (!w->E1 || !w->E2 || !w->W_lm || !w->g_final) return DF_ERR_ARG;
+  if (!w->g_attn || !w->g_mlp || !w->Wqkv || !w->Wo || !w->a || !w->b || !w->c) return DF_ERR_ARG;
+  if (c.n_experts == 0 && (!w->Wgu || !w->Wd)) return DF_ERR_ARG;
+  for (int l = 0; l < c.n_layers; ++l) {
+    if (!w->g_attn[l] || !w->g_mlp[l] || !w->Wqkv[l] || !w->Wo[l] || !w->a[l] || !w->b[l] || !w->c[l])
+      return DF_ERR_ARG;
+    if (c.n_experts == 0 && (!w->Wgu[l] || !w->Wd[l])) return DF_ERR_ARG;
+  }
+  return DF_OK;
+}
+
+// ------------------------------------------------------------------ the MLP block
+int run_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int batch, int aux_on, cudaStream_t s) {
+  const dualflow_config& c = ctx->cfg;
+  const int mp = batch, ma = aux_on ? batch : 0;
+  DF_TRY(launch_rmsnorm(ctx, h, w->g_mlp[l], ctx->x, batch, aux_on, s));
+  if (c.dtype == DF_DTYPE_BF16) {
+    GemmArgs g = gemm_args(ctx);
+    g.x = ctx->x;
+    g.W = w->Wgu[l];
+    g.n_out = c.ffn_hidden;
+    g.k = c.d_model;
+    g.m_p = mp;
+    g.m_a = ma;
+    g.epi = EPI_SWIGLU;
+    g.y = ctx->u;
+    g.ldy = c.ffn_hidden;
+    g.vec = w->b[l];
+    DF_TRY(launch_gemm_tc(ctx, g, s));
+    g = gemm_args(ctx);
+    g.x = ctx->u;
+    g.W = w->Wd[l];
+    g.n_out = c.d_model;
+    g.k = c.ffn_hidden;
+    g.m_p = mp;
+    g.m_a = ma;
+    g.epi = EPI_COUPLE_ADD;
+    g.y = h;
+    g.ldy = c.d_model;
+    g.vec = w->c[l];
+    return launch_gemm_tc(ctx, g, s);
+  }
+  const int M = mp + ma, F = c.ffn_hidden;
+  DF_TRY(launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wgu[l], 2 * F, c.d_model, ctx->raw, 0, s));
+  DF_TRY(launch_swiglu_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->b[l], (float*)ctx->u, s));
+  DF_TRY(launch_linear_f32(ctx, (const float*)ctx->u, M, (const float*)w->Wd[l], c.d_model, F, ctx->raw, 0, s));
+  return launch_couple_add_f32(ctx, ctx->raw, batch, aux_on, c.d_model, (const float*)w->c[l], h, s);
+}
+
+// ------------------------------------------------------------------ the whole step
+int run_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens, int batch,
+             float* logits, int aux_on, cudaStream_t s) {
+  const dualflow_config& c = ctx->cfg;
+  const int mp = batch, ma = aux_on ? batch : 0, M = mp + ma;
+  const bool bf16 = c.dtype == DF_DTYPE_BF16;
+  const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
+  DF_TRY(launch_embed_rmsnorm(ctx, w->E1, w->E2, tokens, c.n_layers > 0 ? w->g_attn[0] : w->g_final, batch, aux_on, s));
+  for (int l = 0; l < c.n_layers; ++l) {
+    if (l > 0) DF_TRY(launch_rmsnorm(ctx, ctx->h, w->g_attn[l], ctx->x, batch, aux_on, s));
+    if (bf16) {
+      GemmArgs g = gemm_args(ctx);
+      g.x = ctx->x;
+      g.W = w->Wqkv[l];
+      g.n_out = qkv_n;
+      g.k = c.d_model;
+      g.m_p = mp;
+      g.m_a = ma;
+      g.epi = EPI_QKV;
+      g.vec = w->a[l];
+      g.q_out = ctx->q;
+      g.seq_len = kv->seq_len;
+      g.k_cache = kv->k[l];
+      g.v_cache = kv->v[l];
+      g.page_table = kv->page_table;
+      DF_TRY(launch_gemm_tc(ctx, g, s));
+      DF_TRY(launch_attention_bf16(ctx, attn_args(ctx, kv, l, batch, 1, aux_on), s));
+      g = gemm_args(ctx);
+      g.x = ctx->o;
+      g.W = w->Wo[l];
+      g.n_out = c.d_model;
+      g.k = qd;
+      g.m_p = mp;
+      g.m_a = ma;
+      g.epi = EPI_ADD_F32;
+      g.y = ctx->h;
+      g.ldy = c.d_model;
+      DF_TRY(launch_gemm_tc(ctx, g, s));
+    } else {
+      DF_TRY(launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wqkv[l], qkv_n, c.d_model, ctx->raw, 0, s));
+      DF_TRY(launch_qkv_post_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->a[l], kv->k[l], kv->v[l],
+                                 kv->page_table, kv->seq_len, (float*)ctx->q, s));
+      DF_TRY(launch_attention_f32(ctx, (const float*)ctx->q, (float*)ctx->o, kv->k[l], kv->v[l], kv->page_table,
+                                  kv->seq_len, batch, 1, aux_on, s));
+      DF_TRY(launch_linear_f32(ctx, (const float*)ctx->o, M, (const float*)w->Wo[l], c.d_model, qd, ctx->h, 1, s));
+    }
+    DF_TRY(run_mlp(ctx, ctx->h, w, l, batch, aux_on, s));
+  }
+  DF_TRY(launch_rmsnorm(ctx, ctx->h, w->g_final, ctx->x, batch, aux_on, s));
+  if (bf16) {
+    GemmArgs g = gemm_args(ctx);
+    g.x = ctx->x;
+    g.W = w->W_lm;
+    g.n_out = c.vocab;
+    g.k = c.d_model;
+    g.m_p = mp;
+    g.m_a = ma;
+    g.epi = EPI_STORE_F32;
+    g.y = logits;
+    g.ldy = c.vocab;
+    return launch_gemm_tc(ctx, g, s);
+  }
+  return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->W_lm, c.vocab, c.d_model, logits, 0, s);
+}
+
+void graph_key(std::vector<uint64_t>& k, const dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+               const int32_t* tokens, int batch, const float* logits, int aux_on, cudaStream_t s) {
+  const int L = ctx->cfg.n_layers;
+  auto P = [&](const void* p) { k.push_back(reinterpret_cast<uint64_t>(p)); };
+  P(s);
+  P(tokens);
+  P(logits);
+  k.push_back((uint64_t)batch);
+  k.push_back((uint64_t)aux_on);
+  P(w->E1), P(w->E2), P(w->W_lm), P(w->g_final);
+  P(kv->seq_len), P(kv->page_table);
+  for (int l = 0; l < L; ++l) {
+    P(w->g_attn[l]), P(w->g_mlp[l]), P(w->Wqkv[l]), P(w->Wo[l]), P(w->a[l]), P(w->b[l]), P(w->c[l]);
+    P(w->Wgu ? w->Wgu[l] : nullptr), P(w->Wd ? w->Wd[l] : nullptr);
+    P(w->Wr ? w->Wr[l] : nullptr), P(w->We_gu ? w->We_gu[l] : nullptr), P(w->We_d ? w->We_d[l] : nullptr);
+    P(kv->k[l]), P(kv->v[l]);
+  }
+}
+
+void drop_graphs(dualflow_ctx* ctx) {
+  for (auto& g : ctx->graphs)
+    if (g.exec) cudaGraphExecDestroy(g.exec);
+  ctx->graphs.clear();
+}
+
+}  // namespace
+
+// ================================================================== C ABI
+extern "C" {
+
+const char* dualflow_status_string(int st) {
+  switch (st) {
+    case DF_OK: return "ok";
+    case DF_ERR_ARG: return "invalid argument";
+    case DF_ERR_SHAPE: return "shape inconsistent with the config";
+    case DF_ERR_DTYPE: return "unknown storage dtype";
+    case DF_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case DF_ERR_CUDA: return "CUDA runtime error";
+    case DF_ERR_OOM: return "device allocation failed";
+    case DF_ERR_DEVICE_BOUNDS: return "device-side bounds check failed (page id, token or cache slot)";
+    case DF_ERR_TIMEOUT: return "bounded device wait expired";
+    default: return "unknown status";
+  }
+}
+
+int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
+  if (!out) return DF_ERR_ARG;
+  *out = nullptr;
+  int rc = validate_config(cfg);
+  if (rc != DF_OK) return rc;
+  dualflow_ctx* ctx = new dualflow_ctx();
+  ctx->cfg = *cfg;
+  const dualflow_config& c = ctx->cfg;
+  auto fail = [&](int code) {
+    dualflow_free(ctx);
+    return code;
+  };
+  if (cudaGetDevice(&ctx->device) != cudaSuccess) return fail(DF_ERR_CUDA);
+  if (cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess)
+    return fail(DF_ERR_CUDA);
+  const size_t es = elem_size(c);
+  const int MB = 2 * c.max_batch;
+  const int half = c.head_dim / 2;
+  const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
+  // RoPE table in fp64 on the host, stored fp32: (cos, sin)(pos * base^(-2i/D)), pos = 0..max_ctx
+  {
+    std::vector<float2> tab((size_t)(c.max_ctx + 1) * half);
+    for (int p = 0; p <= c.max_ctx; ++p)
+      for (int i = 0; i < half; ++i) {
+        const double ang = (double)p * pow((double)c.rope_base, -2.0 * i / c.head_dim);
+        tab[(size_t)p * half + i] = make_float2((float)cos(ang), (float)sin(ang));
+      }
+    if (dalloc(&ctx->rope, tab.size() * sizeof(float2)) != DF_OK) return fail(DF_ERR_OOM);
+    if (cudaMemcpy(ctx->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(DF_ERR_CUDA);
+  }
+  if (dalloc(&ctx->status, sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
+  cudaMemset(ctx->status, 0, sizeof(int32_t));
+  // decode attention: persistent grid of 2 CTAs per SM; partial slots = pairs + CTAs
+  ctx->attn_ctas = 2 * ctx->num_sms;
+  const int pairs = c.max_batch * c.n_kv_heads;
+  ctx->attn_slots = pairs + ctx->attn_ctas;
+  if (dalloc(&ctx->attn_part, (size_t)ctx->attn_slots * kAttnPartFloats * sizeof(float)) != DF_OK)
+    return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->attn_cnt, (size_t)pairs * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
+  cudaMemset(ctx->attn_cnt, 0, (size_t)pairs * sizeof(int32_t));
+  // split-K partials: the largest need among the step's and the attention call's projections
+  if (c.dtype == DF_DTYPE_BF16) {
+    const int n_pad = ((MB + 15) / 16) * 16;
+    struct Shape { int n, k, epi; };
+    const Shape shapes[] = {{qkv_n, c.d_model, EPI_QKV}, {c.d_model, qd, EPI_ADD_F32},
+                            {c.ffn_hidden, c.d_model, EPI_SWIGLU}, {c.d_model, c.ffn_hidden, EPI_COUPLE_ADD},
+                            {c.vocab, c.d_model, EPI_STORE_F32}, {qd, c.d_model, EPI_Q2}};
+    size_t need = 0;
+    int tiles = 1;
+    for (const Shape& sh : shapes) {
+      if (sh.n <= 0 || sh.k <= 0) continue;
+      const int t = sh.epi == EPI_SWIGLU ? sh.n / 64 : (sh.n + kGemmTileN - 1) / kGemmTileN;
+      const int sp = gemm_splits(ctx, sh.n, sh.k, sh.epi);
+      if (sp > 1) need = std::max(need, (size_t)sp * t * n_pad * kGemmTileN);
+      tiles = std::max(tiles, t);
+    }
+    ctx->gemm_part_floats = need;
+    ctx->gemm_cnt_n = tiles;
+    if (dalloc(&ctx->gemm_part, need * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+    if (dalloc(&ctx->gemm_cnt, (size_t)tiles * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
+    cudaMemset(ctx->gemm_cnt, 0, (size_t)tiles * sizeof(int32_t));
+  }
+  const size_t xw = std::max({c.d_model, c.ffn_hidden, qd});
+  const size_t raw_n = std::max({qkv_n, 2 * c.ffn_hidden, c.d_model, c.vocab, qd});
+  if (dalloc(&ctx->h, (size_t)MB * c.d_model * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->x, (size_t)MB * xw * es) != DF_OK) return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->q, (size_t)MB * qd * es) != DF_OK) return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->o, (size_t)MB * qd * es) != DF_OK) return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->u, (size_t)MB * std::max(c.ffn_hidden, 1) * es) != DF_OK) return fail(DF_ERR_OOM);
+  if (c.dtype == DF_DTYPE_F32 && dalloc(&ctx->raw, (size_t)MB * raw_n * sizeof(float)) != DF_OK)
+    return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->tokens_dev, (size_t)c.max_batch * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->logits_dev, (size_t)MB * std::max(c.vocab, 1) * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+  if (cudaDeviceSynchronize() != cudaSuccess) return fail(DF_ERR_CUDA);
+  *out = ctx;
+  return DF_OK;
+}
+
+int dualflow_free(dualflow_ctx* ctx) {
+  if (!ctx) return DF_OK;
+  cudaDeviceSynchronize();
+  drop_graphs(ctx);
+  void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->gemm_part, ctx->gemm_cnt, ctx->h,
+                  ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  delete ctx;
+  return DF_OK;
+}
+
+int dualflow_decode_attention(dualflow_ctx* ctx, const void* q1, const void* h2, const void* Wq, const void* a,
+                              const dualflow_kv* kv, int32_t layer, int32_t batch, void* o, int32_t aux_on,
+                              dualflow_stream stream) {
+  if (!ctx || !q1 || !o) return DF_ERR_ARG;
+  if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
+  if (aux_on && (!h2 || !Wq || !a)) return DF_ERR_ARG;
+  if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
+  DF_TRY(check_kv(ctx, kv, layer));
+  const dualflow_config& c = ctx->cfg;
+  cudaStream_t s = S(stream);
+  if (c.dtype == DF_DTYPE_BF16) {
+    if (aux_on) {
+      GemmArgs g = gemm_args(ctx);
+      g.x = h2;
+      g.W = Wq;
+      g.n_out = c.n_q_heads * c.head_dim;
+      g.k = c.d_model;
+      g.m_p = 0;
+      g.m_a = batch;
+      g.epi = EPI_Q2;
+      g.vec = a;
+      g.q_out = ctx->q;
+      g.q1_in = q1;
+      g.seq_len = kv->seq_len;
+      DF_TRY(launch_gemm_tc(ctx, g, s));
+    } else {
+      DF_TRY(launch_rope_q1(ctx, q1, ctx->q, kv->seq_len, batch, s));
+    }
+    AttnArgs at = attn_args(ctx, kv, layer, batch, 0, aux_on);
+    at.o = o;
+    return launch_attention_bf16(ctx, at, s);
+  }
+  if (aux_on)
+    DF_TRY(launch_linear_f32(ctx, (const float*)h2, batch, (const float*)Wq, c.n_q_heads * c.head_dim, c.d_model,
+                             ctx->raw, 0, s));
+  DF_TRY(launch_q2_post_f32(ctx, ctx->raw, (const float*)q1, batch, aux_on, (const float*)a, kv->seq_len,
+                            (float*)ctx->q, s));
+  return launch_attention_f32(ctx, (const float*)ctx->q, (float*)o, kv->k[layer], kv->v[layer], kv->page_table,
+                              kv->seq_len, batch, 0, aux_on, s);
+}
+
+int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_primary, int32_t m_aux, const void* W,
+                            int32_t n, int32_t k, void* y, int32_t epilogue, const void* epi_arg,
+                            dualflow_stream stream) {
+  if (!ctx || !x || !W || !y) return DF_ERR_ARG;
+  if (m_primary < 0 || m_aux < 0 || m_primary + m_aux <= 0 || n <= 0 || k <= 0) return DF_ERR_ARG;
+  if (epilogue < DF_EPI_STORE_F32 || epilogue > DF_EPI_COUPLE_ADD) return DF_ERR_ARG;
+  if (epilogue == DF_EPI_COUPLE_ADD && (!epi_arg || (m_aux != 0 && m_aux != m_primary))) return DF_ERR_ARG;
+  const dualflow_config& c = ctx->cfg;
+  cudaStream_t s = S(stream);
+  if (c.dtype == DF_DTYPE_BF16) {
+    if (k % 64 != 0 || m_primary + m_aux > kGemmMaxAct) return DF_ERR_SHAPE;
+    GemmArgs g = gemm_args(ctx);
+    g.x = x;
+    g.W = W;
+    g.n_out = n;
+    g.k = k;
+    g.m_p = m_primary;
+    g.m_a = m_aux;
+    g.y = y;
+    g.ldy = n;
+    g.vec = epi_arg;
+    g.epi = epilogue == DF_EPI_STORE_F32 ? EPI_STORE_F32
+            : epilogue == DF_EPI_STORE_BF16 ? EPI_STORE_BF16
+            : epilogue == DF_EPI_ADD_F32 ? EPI_ADD_F32
+                                          : EPI_COUPLE_ADD;
+    const size_t n_pad = ((size_t)(m_primary + m_aux) + 15) / 16 * 16;
+    const int sp = gemm_splits(ctx, n, k, g.epi);
+    const int tiles = (n + kGemmTileN - 1) / kGemmTileN;
+    if (sp > 1 && ((size_t)sp * tiles * n_pad * kGemmTileN > ctx->gemm_part_floats || tiles > ctx->gemm_cnt_n))
+      return DF_ERR_SHAPE;
+    return launch_gemm_tc(ctx, g, s);
+  }
+  const int M = m_primary + m_aux;
+  if ((size_t)M * n > (size_t)2 * c.max_batch * std::max({(c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim,
+                                                            2 * c.ffn_hidden, c.d_model, c.vocab}))
+    return DF_ERR_SHAPE;
+  if (epilogue == DF_EPI_STORE_F32 || epilogue == DF_EPI_STORE_BF16)
+    return launch_linear_f32(ctx, (const float*)x, M, (const float*)W, n, k, (float*)y, 0, s);
+  if (epilogue == DF_EPI_ADD_F32) return launch_linear_f32(ctx, (const float*)x, M, (const float*)W, n, k, (float*)y, 1, s);
+  DF_TRY(launch_linear_f32(ctx, (const float*)x, M, (const float*)W, n, k, ctx->raw, 0, s));
+  return launch_couple_add_f32(ctx, ctx->raw, m_primary, m_aux > 0, n, (const float*)epi_arg, (float*)y, s);
+}
+
+int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int32_t layer, int32_t batch,
+                         int32_t aux_on, int32_t* expert_ids_out, dualflow_stream stream) {
+  (void)expert_ids_out;
+  if (!ctx || !h || !w) return DF_ERR_ARG;
+  if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
+  if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
+  if (layer < 0 || layer >= ctx->cfg.n_layers) return DF_ERR_ARG;
+  DF_TRY(check_weights(ctx, w));
+  return run_mlp(ctx, h, w, layer, batch, aux_on, S(stream));
+}
+
+int dualflow_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
+                  int32_t batch, float* logits, int32_t aux_on, dualflow_stream stream) {
+  if (!ctx || !tokens || !logits) return DF_ERR_ARG;
+  if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
+  if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
+  DF_TRY(check_weights(ctx, w));
+  if (!kv || kv->n_layers != ctx->cfg.n_layers) return DF_ERR_ARG;
+  for (int l = 0; l < ctx->cfg.n_layers; ++l) DF_TRY(check_kv(ctx, kv, l));
+  cudaStream_t s = S(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (s != nullptr && cudaStreamIsCapturing(s, &cap) != cudaSuccess) return DF_ERR_CUDA;
+  if (!ctx->graphs_enabled || s == nullptr || cap != cudaStreamCaptureStatusNone)
+    return run_step(ctx, w, kv, tokens, batch, logits, aux_on, s);
+  std::vector<uint64_t> key;
+  graph_key(key, ctx, w, kv, tokens, batch, logits, aux_on, s);
+  for (auto& g : ctx->graphs)
+    if (g.key == key) return cudaGraphLaunch(g.exec, s) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  cudaGraph_t graph = nullptr;
+  if (cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal) != cudaSuccess) return DF_ERR_CUDA;
+  const int rc = run_step(ctx, w, kv, tokens, batch, logits, aux_on, s);
+  const cudaError_t ec = cudaStreamEndCapture(s, &graph);
+  if (rc != DF_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rc;
+  }
+  if (ec != cudaSuccess) return DF_ERR_CUDA;
+  GraphEntry e;
+  e.key = std::move(key);
+  const cudaError_t ei = cudaGraphInstantiate(&e.exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) return DF_ERR_CUDA;
+  if (ctx->graphs.size() >= 16) {
+    cudaGraphExecDestroy(ctx->graphs.front().exec);
+    ctx->graphs.erase(ctx->graphs.begin());
+  }
+  ctx->graphs.push_back(std::move(e));
+  return cudaGraphLaunch(ctx->graphs.back().exec, s) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int dualflow_step_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens_host,
+                       int32_t batch, float* logits_host, int32_t aux_on, dualflow_stream stream) {
+  if (!ctx || !tokens_host || !logits_host) return DF_ERR_ARG;
+  if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
+  cudaStream_t s = S(stream);
+  if (cudaMemcpyAsync(ctx->tokens_dev, tokens_host, (size_t)batch * sizeof(int32_t), cudaMemcpyHostToDevice, s) !=
+      cudaSuccess)
+    return DF_ERR_CUDA;
+  DF_TRY(dualflow_step(ctx, w, kv, ctx->tokens_dev, batch, ctx->logits_dev, aux_on, stream));
+  const size_t rows = aux_on ? 2 : 1;
+  if (cudaMemcpyAsync(logits_host, ctx->logits_dev, rows * batch * ctx->cfg.vocab * sizeof(float),
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DF_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int dualflow_set_graphs(dualflow_ctx* ctx, int32_t enabled) {
+  if (!ctx || (enabled != 0 && enabled != 1)) return DF_ERR_ARG;
+  ctx->graphs_enabled = enabled;
+  if (!enabled) drop_graphs(ctx);
+  return DF_OK;
+}
+
+int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream) {
+  if (!ctx) return DF_ERR_ARG;
+  cudaStream_t s = S(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DF_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, ctx->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DF_ERR_CUDA;
+  if (v != 0 && cudaMemset(ctx->status, 0, sizeof(v)) != cudaSuccess) return DF_ERR_CUDA;
+  return v;
+}
+
+}  // extern "C"

@@ -1,0 +1,470 @@
+// Asymmetric shared-KV decode attention, bf16 storage / fp32 accumulation, sm_103a.
+//
+// "Atencao de KV Compartilhada Assimetrica" (gist.science technical summary, "Mecanismos Chave"):
+// the auxiliary query attends the primary flow's K1/V1, so one load of each K1/V1 tile can serve
+// both flows. For every (sequence b, KV head g) the kernel scores the 2*G query rows of group g --
+// the G primary heads and the G coupled auxiliary heads -- against the same tile:
+//   S^T (16 keys x 8 rows) = K_tile (16 x 128) . Q^T   and   O^T (128 x 8) += V^T . P^T
+// with mma.sync m16n8k16 (keys as M, the 8 query rows as N: no padding). Tiles of 64 keys are
+// staged in shared memory by TMA (128-byte swizzle) through a 3-stage mbarrier pipeline fed by a
+// producer warp; four consumer warps take 16 keys each and keep their own online-softmax state
+// (running max via warp shuffles), merged at the end of a segment.
+//
+// Work split (flash-decoding): all (b, g, tile) triples are laid end to end and cut into equal
+// contiguous ranges, one per CTA, so ragged lengths balance across the GPU. A pair cut across
+// several CTAs writes per-CTA partials (O, max, sum); the last CTA to arrive (atomic counter, no
+// waiting) merges them in CTA order, so the result does not depend on arrival order.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace df {
+namespace {
+
+constexpr int kStagesA = 3;
+constexpr int kConsumers = 4;
+constexpr int kAttnThreads = (kConsumers + 1) * 32;
+constexpr int kHalf = kAttnTileKeys * 128;   // 64 keys x 64 dims x 2 B = 8 KB (one swizzled box)
+constexpr int kTileBytes = 2 * kHalf;         // K (or V) tile: 16 KB
+constexpr int kStageBytes = 2 * kTileBytes;   // K + V: 32 KB
+constexpr int kMergeFloats = 36 * 32;         // per warp: m0, m1, l0, l1, o[32] for 32 lanes
+
+struct AttnParams {
+  AttnArgs a;
+  float* part;
+  int32_t* cnt;
+  int32_t* status;
+  float scale_log2;  // log2(e) / sqrt(D)
+};
+
+__device__ __forceinline__ void set_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
+
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* err, int32_t* status) {
+  if (*err) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*err) return false;
+    if (globaltimer() - t0 > kWaitLimitNs) {
+      *err = 1;
+      set_status(status, DF_ERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Walks the (b, g, tile) sequence in order.
+struct Walker {
+  int b, g, j, tiles_b;
+};
+
+__device__ __forceinline__ int tiles_of(const int* sched, int b, int Hkv) { return (sched[b + 1] - sched[b]) / Hkv; }
+
+__device__ __forceinline__ void walker_seek(Walker& w, const int* sched, int B, int Hkv, int t) {
+  int b = 0;
+  while (b < B - 1 && sched[b + 1] <= t) ++b;
+  w.b = b;
+  w.tiles_b = tiles_of(sched, b, Hkv);
+  const int rem = t - sched[b];
+  w.g = w.tiles_b ? rem / w.tiles_b : 0;
+  w.j = w.tiles_b ? rem % w.tiles_b : 0;
+}
+
+__device__ __forceinline__ void walker_next(Walker& w, const int* sched, int B, int Hkv) {
+  if (++w.j < w.tiles_b) return;
+  w.j = 0;
+  if (++w.g < Hkv) return;
+  w.g = 0;
+  do {
+    ++w.b;
+    w.tiles_b = (w.b < B) ? tiles_of(sched, w.b, Hkv) : 1;
+  } while (w.tiles_b == 0);
+}
+
+// owner CTA of global tile t when T tiles are cut into C equal contiguous ranges
+__device__ __forceinline__ int owner_of(long long t, long long T, int C) { return (int)(((t + 1) * C - 1) / T); }
+
+__device__ __forceinline__ uint32_t swz(int key, int chunk) { return (uint32_t)(key * 128 + ((chunk ^ (key & 7)) << 4)); }
+
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_kernel(const __grid_constant__ CUtensorMap map_k,
+                                                                     const __grid_constant__ CUtensorMap map_v,
+                                                                     const AttnParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const AttnArgs& a = P.a;
+  const int B = a.batch, Hkv = a.n_kv_heads, Hq = a.n_q_heads, G = Hq / Hkv;
+  float* mbuf = reinterpret_cast<float*>(smem + kStagesA * kStageBytes);      // 2 x kMergeFloats
+  uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + 2 * kMergeFloats);
+  uint64_t* empty = full + kStagesA;
+  volatile int* err = reinterpret_cast<volatile int*>(empty + kStagesA);
+  int* sched = const_cast<int*>(err) + 4;  // [B + 1] exclusive prefix of tiles
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumers);
+    }
+    *err = 0;
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      sched[b] = acc;
+      const int L = a.seq_len[b] + a.extra;
+      int tb = (L + kAttnTileKeys - 1) / kAttnTileKeys;
+      if (L < 0 || L > a.max_ctx) {  // out-of-range length: skip the sequence, report it
+        set_status(P.status, DF_ERR_DEVICE_BOUNDS);
+        tb = 0;
+      }
+      acc += tb * Hkv;
+    }
+    sched[B] = acc;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const long long T = sched[B];
+  // Cut the T tiles over C = min(grid, T) CTAs so that every participating CTA owns at least one
+  // tile (the partial-merge counts rely on it); CTAs beyond C only zero empty sequences.
+  const int C = (int)(T < (long long)gridDim.x ? T : (long long)gridDim.x);
+  const long long t0 = (c < C) ? T * c / C : 0, t1 = (c < C) ? T * (c + 1) / C : 0;
+
+  if (warp == kConsumers) {
+    // ------------------------------ TMA producer ------------------------------
+    if (lane == 0 && t1 > t0) {
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      const uint64_t pol = policy_evict_first();
+      Walker w;
+      walker_seek(w, sched, B, Hkv, (int)t0);
+      for (long long t = t0, i = 0; t < t1; ++t, ++i) {
+        const int s = (int)(i % kStagesA);
+        const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
+        if (!wait_or_fail(&empty[s], ph ^ 1u, err, P.status)) break;
+        uint8_t* Kst = smem + s * kStageBytes;
+        uint8_t* Vst = Kst + kTileBytes;
+        const int key0 = w.j * kAttnTileKeys;
+        const int Leff = a.seq_len[w.b] + a.extra;
+        if (!a.paged) {
+          const int row = w.b * Hkv + w.g;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+          tma_load_3d_hint(Kst, &map_k, &full[s], 0, key0, row, pol);
+          tma_load_3d_hint(Kst + kHalf, &map_k, &full[s], 64, key0, row, pol);
+          tma_load_3d_hint(Vst, &map_v, &full[s], 0, key0, row, pol);
+          tma_load_3d_hint(Vst + kHalf, &map_v, &full[s], 64, key0, row, pol);
+        } else {
+          const int ps = a.page_size, npg = kAttnTileKeys / ps;
+          int pid[kAttnTileKeys / 16];
+          uint32_t bytes = 0;
+          for (int jj = 0; jj < npg; ++jj) {
+            const int lp = key0 / ps + jj;
+            pid[jj] = -1;
+            if (lp * ps < Leff && lp < a.pages_per_seq) {
+              const int v = a.page_table[(size_t)w.b * a.pages_per_seq + lp];
+              if (v >= 0 && v < a.max_pages) {
+                pid[jj] = v;
+                bytes += 4u * (uint32_t)ps * 128u;
+              } else {
+                set_status(P.status, DF_ERR_DEVICE_BOUNDS);
+              }
+            }
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+          for (int jj = 0; jj < npg; ++jj) {
+            if (pid[jj] < 0) continue;
+            const int row = pid[jj] * Hkv + w.g;
+            const int off = jj * ps * 128;
+            tma_load_3d_hint(Kst + off, &map_k, &full[s], 0, 0, row, pol);
+            tma_load_3d_hint(Kst + kHalf + off, &map_k, &full[s], 64, 0, row, pol);
+            tma_load_3d_hint(Vst + off, &map_v, &full[s], 0, 0, row, pol);
+            tma_load_3d_hint(Vst + kHalf + off, &map_v, &full[s], 64, 0, row, pol);
+          }
+        }
+        walker_next(w, sched, B, Hkv);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------ consumers ------------------------------
+  // sequences with nothing to attend: o = 0
+  for (int b = c; b < B; b += gridDim.x) {
+    if (sched[b + 1] != sched[b]) continue;
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.o);
+    const int nf = a.aux_on ? 2 : 1;
+    for (int f = 0; f < nf; ++f)
+      for (int i = threadIdx.x; i < Hq * kHeadDim; i += kConsumers * 32)
+        o[((size_t)f * B + b) * Hq * kHeadDim + i] = __float2bfloat16_rn(0.f);
+  }
+  if (t1 <= t0) return;
+
+  const int kw = 16 * warp;
+  const int qn = lane >> 2;          // query row this lane feeds into the B fragment
+  const int q0 = 2 * (lane & 3);     // the two query rows this lane accumulates
+  const float NEG_INF = -INFINITY;
+  const uint32_t sbase = smem_u32(smem);
+
+  float m[2] = {NEG_INF, NEG_INF}, l[2] = {0.f, 0.f};
+  float o[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  uint32_t qb[8][2];
+
+  Walker w;
+  walker_seek(w, sched, B, Hkv, (int)t0);
+  bool new_seg = true;
+  for (long long t = t0, i = 0; t < t1; ++t, ++i) {
+    const int Leff = a.seq_len[w.b] + a.extra;
+    if (new_seg) {
+      // load this group's 2G query rows (primary heads, then auxiliary heads) as B fragments
+      const int f = qn / G, hh = qn % G;
+      const bool valid = (qn < 2 * G) && (f == 0 || a.aux_on);
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q);
+      const size_t base = (((size_t)f * B + w.b) * Hq + w.g * G + hh) * kHeadDim;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[kk][0] = valid ? q32[(base + 16 * kk + q0) >> 1] : 0u;
+        qb[kk][1] = valid ? q32[(base + 16 * kk + 8 + q0) >> 1] : 0u;
+      }
+      new_seg = false;
+    }
+    const int s = (int)(i % kStagesA);
+    const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
+    const bool ok = wait_or_fail(&full[s], ph, err, P.status);
+    const int key0 = w.j * kAttnTileKeys;
+    const int valid = Leff - key0;
+    const uint32_t Kb = sbase + s * kStageBytes, Vb = Kb + kTileBytes;
+    if (ok) {
+      bool zeroed = false;
+      if (valid < kw + 16) {
+        // rows past the sequence end: zero V so that p = 0 cannot meet a non-finite value
+        uint8_t* Vp = smem + s * kStageBytes + kTileBytes;
+        for (int e = lane; e < 16 * 16; e += 32) {
+          const int r = kw + (e >> 4), half = (e >> 3) & 1, ch = e & 7;
+          if (r >= valid) *reinterpret_cast<uint4*>(Vp + half * kHalf + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+        zeroed = true;
+      }
+      // S^T = K . Q^T for my 16 keys
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      {
+        const int mi = lane >> 3;
+        const int key = kw + (lane & 7) + ((mi & 1) << 3);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int chunk = ((kk & 3) << 1) + (mi >> 1);
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(Kb + (kk >> 2) * kHalf + swz(key, chunk), a0, a1, a2, a3);
+          mma_bf16_16816(sc, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+        }
+      }
+      // mask and online softmax (log2 domain)
+      const int r0 = kw + qn, r1 = r0 + 8;
+      float s0 = (r0 < valid) ? sc[0] * P.scale_log2 : NEG_INF;
+      float s1 = (r0 < valid) ? sc[1] * P.scale_log2 : NEG_INF;
+      float s2 = (r1 < valid) ? sc[2] * P.scale_log2 : NEG_INF;
+      float s3 = (r1 < valid) ? sc[3] * P.scale_log2 : NEG_INF;
+      float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
+      const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+      const float base0 = (mn0 == NEG_INF) ? 0.f : mn0, base1 = (mn1 == NEG_INF) ? 0.f : mn1;
+      const float cr0 = exp2f(m[0] - base0), cr1 = exp2f(m[1] - base1);
+      const float p0 = exp2f(s0 - base0), p1 = exp2f(s1 - base1), p2 = exp2f(s2 - base0), p3 = exp2f(s3 - base1);
+      l[0] = l[0] * cr0 + p0 + p2;
+      l[1] = l[1] * cr1 + p1 + p3;
+      m[0] = mn0;
+      m[1] = mn1;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        o[mt][0] *= cr0;
+        o[mt][1] *= cr1;
+        o[mt][2] *= cr0;
+        o[mt][3] *= cr1;
+      }
+      // P^T (keys x rows) -> B fragments via an in-register 8x8 transpose
+      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+      // O^T += V^T . P^T
+      {
+        const int mi = lane >> 3;
+        const int key = kw + (lane & 7) + ((mi >> 1) << 3);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int chunk = ((mt & 3) << 1) + (mi & 1);
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4_trans(Vb + (mt >> 2) * kHalf + swz(key, chunk), a0, a1, a2, a3);
+          mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+        }
+      }
+      if (zeroed) fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+
+    // ---- end of this CTA's segment of pair (b, g): merge warps, write result or partial ----
+    const bool seg_end = (w.j == w.tiles_b - 1) || (t == t1 - 1);
+    if (seg_end) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+        l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
+      }
+      auto put = [&](float* buf) {
+        buf[0 * 32 + lane] = m[0];
+        buf[1 * 32 + lane] = m[1];
+        buf[2 * 32 + lane] = l[0];
+        buf[3 * 32 + lane] = l[1];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) buf[(4 + mt * 4 + r) * 32 + lane] = o[mt][r];
+      };
+      auto merge = [&](const float* buf) {
+#pragma unroll
+        for (int qq = 0; qq < 2; ++qq) {
+          const float mb = buf[qq * 32 + lane], lb = buf[(2 + qq) * 32 + lane];
+          const float M = fmaxf(m[qq], mb);
+          const float sa = (M == NEG_INF) ? 0.f : exp2f(m[qq] - M);
+          const float sb = (M == NEG_INF) ? 0.f : exp2f(mb - M);
+          l[qq] = l[qq] * sa + lb * sb;
+          m[qq] = M;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][qq] = o[mt][qq] * sa + buf[(4 + mt * 4 + qq) * 32 + lane] * sb;
+            o[mt][qq + 2] = o[mt][qq + 2] * sa + buf[(4 + mt * 4 + qq + 2) * 32 + lane] * sb;
+          }
+        }
+      };
+      named_bar_sync(1, kConsumers * 32);
+      if (warp >= 2) put(mbuf + (warp - 2) * kMergeFloats);
+      named_bar_sync(1, kConsumers * 32);
+      if (warp < 2) merge(mbuf + warp * kMergeFloats);
+      named_bar_sync(1, kConsumers * 32);
+      if (warp == 1) put(mbuf);
+      named_bar_sync(1, kConsumers * 32);
+      if (warp == 0 && !*err) {
+        const int p = w.b * Hkv + w.g;
+        const long long pstart = sched[w.b] + (long long)w.g * w.tiles_b;
+        const int first = owner_of(pstart, T, C), last = owner_of(pstart + w.tiles_b - 1, T, C);
+        merge(mbuf);
+        __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(a.o);
+        auto store = [&](float (&acc)[8][4], const float (&den)[2]) {
+#pragma unroll
+          for (int qq = 0; qq < 2; ++qq) {
+            const int q = q0 + qq, f = q / G, hh = q % G;
+            if (q >= 2 * G || (f == 1 && !a.aux_on)) continue;
+            const float inv = 1.0f / den[qq];
+            const size_t base = (((size_t)f * B + w.b) * Hq + w.g * G + hh) * kHeadDim;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              ob[base + 16 * mt + qn] = __float2bfloat16_rn(acc[mt][qq] * inv);
+              ob[base + 16 * mt + qn + 8] = __float2bfloat16_rn(acc[mt][qq + 2] * inv);
+            }
+          }
+        };
+        if (first == last) {
+          store(o, l);
+        } else {
+          float* slot = P.part + (size_t)(p + c) * kAttnPartFloats;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+              slot[(q0 + qq) * kHeadDim + 16 * mt + qn] = o[mt][qq];
+              slot[(q0 + qq) * kHeadDim + 16 * mt + qn + 8] = o[mt][qq + 2];
+            }
+          if (qn == 0) {
+            slot[8 * kHeadDim + q0] = m[0];
+            slot[8 * kHeadDim + q0 + 1] = m[1];
+            slot[8 * kHeadDim + 8 + q0] = l[0];
+            slot[8 * kHeadDim + 8 + q0 + 1] = l[1];
+          }
+          __threadfence();
+          __syncwarp();
+          int prev = 0;
+          if (lane == 0) prev = atomicAdd(&P.cnt[p], 1);
+          prev = __shfl_sync(0xffffffffu, prev, 0);
+          if (prev == last - first) {
+            __threadfence();
+            float M[2] = {NEG_INF, NEG_INF};
+            for (int cc = first; cc <= last; ++cc) {
+              const float* sl = P.part + (size_t)(p + cc) * kAttnPartFloats;
+              M[0] = fmaxf(M[0], __ldcg(sl + 8 * kHeadDim + q0));
+              M[1] = fmaxf(M[1], __ldcg(sl + 8 * kHeadDim + q0 + 1));
+            }
+            float acc[8][4], den[2] = {0.f, 0.f};
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+            for (int cc = first; cc <= last; ++cc) {
+              const float* sl = P.part + (size_t)(p + cc) * kAttnPartFloats;
+#pragma unroll
+              for (int qq = 0; qq < 2; ++qq) {
+                const float ms = __ldcg(sl + 8 * kHeadDim + q0 + qq);
+                const float sc2 = (M[qq] == NEG_INF) ? 0.f : exp2f(ms - M[qq]);
+                den[qq] += __ldcg(sl + 8 * kHeadDim + 8 + q0 + qq) * sc2;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                  acc[mt][qq] += __ldcg(sl + (q0 + qq) * kHeadDim + 16 * mt + qn) * sc2;
+                  acc[mt][qq + 2] += __ldcg(sl + (q0 + qq) * kHeadDim + 16 * mt + qn + 8) * sc2;
+                }
+              }
+            }
+            store(acc, den);
+            if (lane == 0) P.cnt[p] = 0;
+          }
+        }
+      }
+      // reset the running state for the next pair
+      m[0] = m[1] = NEG_INF;
+      l[0] = l[1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+      new_seg = true;
+    }
+    walker_next(w, sched, B, Hkv);
+  }
+}
+
+}  // namespace
+
+int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s) {
+  const dualflow_config& cfg = ctx->cfg;
+  if (a.batch <= 0) return DF_OK;
+  CUtensorMap mk, mv;
+  int rc;
+  if (!a.paged) {
+    const uint64_t rows = (uint64_t)cfg.max_batch * cfg.n_kv_heads;
+    rc = encode_map_3d_bf16(&mk, a.k_cache, kHeadDim, (uint64_t)cfg.max_ctx, rows, kHeadDim * 2,
+                            (uint64_t)cfg.max_ctx * kHeadDim * 2, 64, kAttnTileKeys, 1);
+    if (rc == DF_OK)
+      rc = encode_map_3d_bf16(&mv, a.v_cache, kHeadDim, (uint64_t)cfg.max_ctx, rows, kHeadDim * 2,
+                              (uint64_t)cfg.max_ctx * kHeadDim * 2, 64, kAttnTileKeys, 1);
+  } else {
+    const uint64_t rows = (uint64_t)cfg.max_pages * cfg.n_kv_heads;
+    rc = encode_map_3d_bf16(&mk, a.k_cache, kHeadDim, (uint64_t)cfg.page_size, rows, kHeadDim * 2,
+                            (uint64_t)cfg.page_size * kHeadDim * 2, 64, (uint32_t)cfg.page_size, 1);
+    if (rc == DF_OK)
+      rc = encode_map_3d_bf16(&mv, a.v_cache, kHeadDim, (uint64_t)cfg.page_size, rows, kHeadDim * 2,
+                              (uint64_t)cfg.page_size * kHeadDim * 2, 64, (uint32_t)cfg.page_size, 1);
+  }
+  if (rc != DF_OK) return rc;
+  AttnParams p;
+  p.a = a;
+  p.part = ctx->attn_part;
+  p.cnt = ctx->attn_cnt;
+  p.status = ctx->status;
+  p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+  const size_t smem = 1024 + (size_t)kStagesA * kStageBytes + 2 * kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
+                      (size_t)(a.batch + 1) * 4;
+  cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return DF_ERR_CUDA;
+  attn_bf16_kernel<<<ctx->attn_ctas, kAttnThreads, smem, s>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+}  // namespace df

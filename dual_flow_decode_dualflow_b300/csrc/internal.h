@@ -1,0 +1,143 @@
+// Internal declarations shared by the library's translation units: the context, the argument
+// blocks of every kernel family and their host launchers.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/dualflow.h"
+
+namespace df {
+
+// ---- bf16 kernel constraints --------------------------------------------------------------
+constexpr int kHeadDim = 128;       // bf16 attention and QKV epilogue assume D = 128
+constexpr int kMaxGroupRows = 8;    // 2 flows x G query heads per KV head share one mma n-tile
+constexpr int kAttnTileKeys = 64;   // keys per pipeline stage of the decode-attention kernel
+constexpr int kGemmTileN = 128;     // weight rows (output features) per tcgen05 tile
+constexpr int kGemmTileK = 64;      // reduction elements per pipeline stage (128-byte rows)
+constexpr int kGemmMaxAct = 256;    // activation rows (both flows) per tcgen05 tile
+
+// Partial result of one attention segment: 8 query rows x (D values + running max + sum).
+constexpr int kAttnPartFloats = kMaxGroupRows * (kHeadDim + 2);
+
+// ---- epilogues of the tcgen05 stacked linear ------------------------------------------------
+enum GemmEpi : int {
+  EPI_STORE_F32 = 0,  // y fp32
+  EPI_STORE_BF16 = 1, // y bf16
+  EPI_ADD_F32 = 2,    // y fp32 +=
+  EPI_COUPLE_ADD = 3, // z2 += c (*) z1; y fp32 += z
+  EPI_QKV = 4,        // query coupling a, RoPE, q store, primary K/V append
+  EPI_Q2 = 5,         // attention-only: q2 = acc + a (*) q1, RoPE of q1 and q2
+  EPI_SWIGLU = 6,     // u = silu(gate) (*) up, u2 += b (*) u1, bf16 store
+};
+
+struct GemmArgs {
+  // operands
+  const void* x;   // [m_p + m_a, k] bf16 (activations, both flows stacked)
+  const void* W;   // [n_rows, k] bf16
+  int n_out;       // output features (for EPI_SWIGLU: hidden units F, W has 2F rows)
+  int k;
+  int m_p, m_a;    // primary / auxiliary activation rows
+  int epi;
+  // epilogue operands
+  void* y;             // STORE/ADD/COUPLE: [m, n_out] ; SWIGLU: u [m, F] bf16
+  int ldy;             // leading dimension of y in elements
+  const void* vec;     // COUPLE: c ; QKV/Q2: a ; SWIGLU: b   (bf16 [n_out])
+  // QKV / Q2
+  void* q_out;             // [2, B, Hq, D] bf16
+  const void* q1_in;       // Q2: q1 [B, Hq, D] bf16
+  int n_q_heads, n_kv_heads;
+  const int32_t* seq_len;  // [B] device
+  const float2* rope;      // [max_ctx + 1][D/2] (cos, sin)
+  void* k_cache;
+  void* v_cache;
+  const int32_t* page_table;
+  int paged, page_size, max_ctx, max_pages, pages_per_seq;
+};
+
+struct AttnArgs {
+  const void* q;            // [2, B, Hq, D] bf16, post-RoPE
+  void* o;                  // [2, B, Hq, D] bf16
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* seq_len;   // [B] device
+  const int32_t* page_table;
+  int batch, n_q_heads, n_kv_heads;
+  int paged, page_size, max_ctx, max_pages, pages_per_seq;
+  int extra;                // 1 when the step appended slot seq_len[b] (attend 0..seq_len[b])
+  int aux_on;
+};
+
+struct GraphEntry {
+  std::vector<uint64_t> key;
+  cudaGraphExec_t exec = nullptr;
+};
+
+}  // namespace df
+
+struct dualflow_ctx {
+  dualflow_config cfg;
+  int device = 0;
+  int num_sms = 148;
+  int32_t* status = nullptr;       // device status word
+  float2* rope = nullptr;          // [max_ctx + 1][head_dim / 2]
+  // decode-attention split workspace
+  float* attn_part = nullptr;
+  int32_t* attn_cnt = nullptr;
+  int attn_ctas = 0;               // persistent grid size of the attention kernel
+  int attn_slots = 0;
+  // tcgen05 split-K workspace
+  float* gemm_part = nullptr;
+  size_t gemm_part_floats = 0;
+  int32_t* gemm_cnt = nullptr;
+  int gemm_cnt_n = 0;
+  // step activations
+  float* h = nullptr;              // [2, max_batch, d] fp32 residual
+  void* x = nullptr;               // [2 * max_batch, max(d, F)] storage dtype (normed input)
+  void* q = nullptr;               // [2, max_batch, Hq, D]
+  void* o = nullptr;               // [2, max_batch, Hq * D]
+  void* u = nullptr;               // [2 * max_batch, F]
+  float* raw = nullptr;            // fp32 path: [2 * max_batch, max_n] projection scratch
+  int32_t* tokens_dev = nullptr;   // dualflow_step_host staging
+  float* logits_dev = nullptr;
+  int graphs_enabled = 1;
+  std::vector<df::GraphEntry> graphs;
+};
+
+namespace df {
+
+// Tensor-map encoding through the driver entry point (no link-time libcuda dependency).
+int encode_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                       uint32_t box_inner, uint32_t box_rows);
+int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
+                       uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+
+// Launchers (return dualflow_status).
+int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s);
+int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi);
+int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s);
+
+int launch_embed_rmsnorm(dualflow_ctx* ctx, const void* E1, const void* E2, const int32_t* tokens, const void* g,
+                         int batch, int aux_on, cudaStream_t s);
+int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s);
+int launch_rope_q1(dualflow_ctx* ctx, const void* q1, void* q, const int32_t* seq_len, int batch, cudaStream_t s);
+
+// fp32 (CUDA-core) path
+int launch_linear_f32(dualflow_ctx* ctx, const float* x, int m, const float* W, int n, int k, float* y, int accumulate,
+                      cudaStream_t s);
+int launch_qkv_post_f32(dualflow_ctx* ctx, const float* raw, int batch, int aux_on, const float* a, void* k_cache,
+                        void* v_cache, const int32_t* page_table, const int32_t* seq_len, float* q, cudaStream_t s);
+int launch_q2_post_f32(dualflow_ctx* ctx, const float* raw, const float* q1, int batch, int aux_on, const float* a,
+                       const int32_t* seq_len, float* q, cudaStream_t s);
+int launch_attention_f32(dualflow_ctx* ctx, const float* q, float* o, const void* k_cache, const void* v_cache,
+                         const int32_t* page_table, const int32_t* seq_len, int batch, int extra, int aux_on,
+                         cudaStream_t s);
+int launch_swiglu_f32(dualflow_ctx* ctx, const float* raw, int batch, int aux_on, const float* b, float* u,
+                      cudaStream_t s);
+int launch_couple_add_f32(dualflow_ctx* ctx, const float* raw, int batch, int aux_on, int n, const float* c, float* h,
+                          cudaStream_t s);
+
+}  // namespace df

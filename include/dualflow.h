@@ -1,0 +1,213 @@
+/*
+ * dualflow.h -- C ABI of the B300 (sm_103a) Dual-Flow Transformer decode library.
+ *
+ * The method ("Resumo Tecnico: Dual-Flow Transformers", gist.science, sections "Arquitetura
+ * Central" and "Mecanismos Chave"): a primary flow and an auxiliary flow share every attention,
+ * MLP and output matrix and the single persistent KV cache, which only the primary flow writes;
+ * the auxiliary flow has its own token embedding, is coupled one way to the primary flow by the
+ * learned vectors a_l (query), b_l (MLP intermediate) and c_l (MLP output), and never feeds back.
+ * The pages give no coupling equations; this library fixes them as
+ *     q2 = Wq.x2 + a_l (*) q1      u2 += b_l (*) u1      y2 += c_l (*) y1
+ * Decode is memory-bound (same page, "Declaracao do Problema"), and grouping both flows lets one
+ * read of each weight tile and each K1/V1 tile serve both ("Custos de Inferencia vs. Treinamento").
+ *
+ * Conventions for every call
+ *  - Pointers named "device" are CUDA device addresses; all others are host addresses.
+ *  - The caller owns every tensor (weights, cache, inputs, outputs). A context owns only its
+ *    workspace, sized at dualflow_init from the config's max_* fields. Hot calls never allocate.
+ *  - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and returns a dualflow_status. Argument and shape errors are detected on the host
+ *    before any launch and leave every buffer untouched. Errors found on the device (an out-of-
+ *    range page id, token or cache slot; an expired bounded wait) are latched in a device status
+ *    word and reported by dualflow_sync_status.
+ *  - Activations of the two flows are stacked flow-major: row r = f * batch + b, f = 0 primary,
+ *    f = 1 auxiliary. With aux_on = 0 only the primary rows are computed and written, and the
+ *    primary results are bit-identical to those of a call with aux_on = 1.
+ *  - Storage dtype (config.dtype): DF_DTYPE_BF16 stores weights, embeddings, norm gains, coupling
+ *    vectors and the KV cache as bf16 (round to nearest even); the residual stream, logits and all
+ *    accumulations are fp32. DF_DTYPE_F32 stores everything as fp32 (no TF32 anywhere).
+ *  - Matrices are row-major [out_features, in_features]; y = x . W^T.
+ */
+#ifndef DUALFLOW_H
+#define DUALFLOW_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DF_API __attribute__((visibility("default")))
+#else
+#define DF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dualflow_ctx dualflow_ctx; /* opaque; owns workspace only */
+typedef void* dualflow_stream;            /* cudaStream_t */
+
+typedef enum {
+  DF_OK = 0,
+  DF_ERR_ARG = 1,            /* null pointer, negative or zero size, bad flag */
+  DF_ERR_SHAPE = 2,          /* sizes inconsistent with the config or beyond its max_* fields */
+  DF_ERR_DTYPE = 3,          /* unknown storage dtype */
+  DF_ERR_UNSUPPORTED = 4,    /* a valid config this build has no kernel for (see dualflow_init) */
+  DF_ERR_CUDA = 5,           /* a CUDA runtime call failed */
+  DF_ERR_OOM = 6,            /* workspace allocation failed at init */
+  DF_ERR_DEVICE_BOUNDS = 7,  /* device-side check failed: page id, token id or cache slot out of range */
+  DF_ERR_TIMEOUT = 8         /* a bounded device wait expired; the kernel returned early */
+} dualflow_status;
+
+enum { DF_DTYPE_F32 = 0, DF_DTYPE_BF16 = 1 };
+
+/* Model and capacity description. */
+typedef struct {
+  int32_t n_layers;
+  int32_t d_model;
+  int32_t n_q_heads;   /* Hq */
+  int32_t n_kv_heads;  /* Hkv; GQA group G = Hq / Hkv, query head h reads KV head h / G */
+  int32_t head_dim;    /* D */
+  int32_t ffn_hidden;  /* SwiGLU hidden F (dense) or per-expert hidden (MoE) */
+  int32_t vocab;
+  int32_t n_experts;   /* 0 = dense MLP */
+  int32_t topk_primary;
+  int32_t topk_aux;
+  int32_t dtype;       /* DF_DTYPE_* */
+  int32_t paged;       /* 0 = contiguous cache, 1 = paged cache */
+  int32_t page_size;   /* positions per page (paged only) */
+  int32_t max_batch;
+  int32_t max_ctx;     /* cache capacity in positions per sequence (also the contiguous stride) */
+  int32_t max_pages;   /* physical pages per layer (paged only) */
+  float rope_base;     /* RoPE rotate-half pairs (i, i + D/2), theta_i = base^(-2i/D) */
+  float rms_eps;       /* RMSNorm x = h / sqrt(mean(h^2) + eps) * g */
+} dualflow_config;
+
+/* Per-layer device pointers are passed as host arrays of n_layers device pointers.
+ *   E1, E2   [vocab, d]       token embeddings of the primary / auxiliary flow
+ *   W_lm     [vocab, d]       shared LM head;      g_final [d] shared final-norm gain
+ *   g_attn, g_mlp [d]         shared pre-attention / pre-MLP RMSNorm gains
+ *   Wqkv     [(Hq + 2 Hkv) D, d]   rows: Wq (Hq*D), then Wk (Hkv*D), then Wv (Hkv*D)
+ *   Wo       [d, Hq D]
+ *   Wgu      [2F, d]          rows: gate (F), then up (F)        (dense only)
+ *   Wd       [d, F]                                              (dense only)
+ *   Wr       [E, d]           shared router                      (MoE only)
+ *   We_gu    [E, 2F, d]       per expert: gate rows then up rows (MoE only)
+ *   We_d     [E, d, F]                                           (MoE only)
+ *   a [Hq D], b [F], c [d]    coupling vectors of each layer
+ */
+typedef struct {
+  const void* E1;
+  const void* E2;
+  const void* W_lm;
+  const void* g_final;
+  const void* const* g_attn;
+  const void* const* g_mlp;
+  const void* const* Wqkv;
+  const void* const* Wo;
+  const void* const* Wgu;
+  const void* const* Wd;
+  const void* const* Wr;
+  const void* const* We_gu;
+  const void* const* We_d;
+  const void* const* a;
+  const void* const* b;
+  const void* const* c;
+  int32_t n_layers;
+} dualflow_weights;
+
+/* The primary flow's persistent KV cache ("Arquitetura Central": only the primary writes it).
+ *   k[l], v[l]  device; contiguous: [max_batch, Hkv, max_ctx, D]
+ *                        paged:      [max_pages, Hkv, page_size, D]
+ *   page_table  device int32 [max_batch, ceil(max_ctx / page_size)]; entry j of row b is the
+ *               physical page holding positions [j*page_size, (j+1)*page_size); -1 = unused
+ *   seq_len     device int32 [batch]: positions cached BEFORE the call. A step writes the new
+ *               primary key/value at slot seq_len[b] and both flows attend positions
+ *               0..seq_len[b]; the caller advances seq_len afterwards. */
+typedef struct {
+  void* const* k;
+  void* const* v;
+  const int32_t* page_table;
+  const int32_t* seq_len;
+  int32_t n_layers;
+} dualflow_kv;
+
+/* Creates a context for `cfg` on the current CUDA device and allocates its workspace.
+ * Host-validates the config (DF_ERR_ARG / DF_ERR_SHAPE / DF_ERR_DTYPE before touching the GPU).
+ * bf16 kernels need head_dim == 128, Hq / Hkv <= 4, d_model, ffn_hidden and Hq*head_dim
+ * multiples of 64 (else DF_ERR_UNSUPPORTED). On failure *out is set to NULL. */
+DF_API int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out);
+
+/* Releases the context and its workspace. NULL-safe. Synchronizes the device first. */
+DF_API int dualflow_free(dualflow_ctx* ctx);
+
+/* Static description of a status code; never NULL. */
+DF_API const char* dualflow_status_string(int status);
+
+/* Attention-only dual-flow decode of one layer ("Atencao de KV Compartilhada Assimetrica"):
+ *   q2 = Wq . h2 + a (*) q1;  RoPE(q1), RoPE(q2) at position seq_len[b];
+ *   o_f = softmax(q_f K1^T / sqrt(D)) V1 over the cached positions 0..seq_len[b]-1 of layer `layer`.
+ * Nothing is appended. q1 [batch, Hq, D] (raw primary query projection), h2 [batch, d]
+ * (auxiliary flow's normed input), Wq [Hq D, d], a [Hq D]: device, storage dtype.
+ * o: device [2, batch, Hq, D], storage dtype (aux rows written only when aux_on).
+ * seq_len[b] == 0 yields o = 0 for that row. Every K1/V1 tile is read once for both flows. */
+DF_API int dualflow_decode_attention(dualflow_ctx* ctx, const void* q1, const void* h2, const void* Wq, const void* a,
+                              const dualflow_kv* kv, int32_t layer, int32_t batch, void* o, int32_t aux_on,
+                              dualflow_stream stream);
+
+/* Epilogues of dualflow_stacked_linear. */
+enum {
+  DF_EPI_STORE_F32 = 0,   /* y fp32 [M, n] = x W^T */
+  DF_EPI_STORE_BF16 = 1,  /* y storage-dtype [M, n] (bf16 rounding for bf16 contexts) */
+  DF_EPI_ADD_F32 = 2,     /* y fp32 [M, n] += x W^T (residual update) */
+  DF_EPI_COUPLE_ADD = 3   /* z = x W^T; z[aux rows] += c (*) z[primary rows]; y fp32 += z.
+                             epi_arg: device c [n], storage dtype; needs m_aux == m_primary */
+};
+
+/* Stacked-activation linear: rows 0..m_primary-1 of x are the primary flow, the next m_aux rows
+ * the auxiliary flow; one read of W serves all of them. x: device [m_primary + m_aux, k] storage
+ * dtype; W: device [n, k] storage dtype; y per `epilogue`. k must be a multiple of 64 and
+ * m_primary + m_aux <= 256 for bf16 contexts. */
+DF_API int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_primary, int32_t m_aux, const void* W,
+                            int32_t n, int32_t k, void* y, int32_t epilogue, const void* epi_arg,
+                            dualflow_stream stream);
+
+/* The MLP block of layer `layer` for both flows ("Acoplamento Leve"), in place on the fp32
+ * residual h: device [2, batch, d] (flow-major). x_f = RMSNorm(h_f, g_mlp); dense:
+ * u_f = silu(Wg x_f) (*) (Wu x_f), u2 += b (*) u1, y_f = Wd u_f; MoE ("Replay de Roteador"):
+ * the primary picks its top-k_primary experts from its router logits, the auxiliary flow uses the
+ * top-k_aux experts of the PRIMARY logits with softmax weights from its own logits, b couples an
+ * expert's intermediate when both flows use it; then y2 += c (*) y1 and h_f += y_f.
+ * expert_ids_out (MoE only, nullable): device int32 [2, batch, max(k_primary, k_aux)], experts of
+ * each row in descending router logit order (ties to the lower index), -1 padded. */
+DF_API int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int32_t layer, int32_t batch,
+                         int32_t aux_on, int32_t* expert_ids_out, dualflow_stream stream);
+
+/* One whole decode step of both flows: embeddings E1[tok], E2[tok] -> n_layers x {RMSNorm,
+ * QKV with query coupling, RoPE and primary-only KV append, shared-KV attention, O projection,
+ * coupled MLP} -> final RMSNorm -> shared LM head.
+ * tokens: device int32 [batch]; logits: device fp32 [2, batch, vocab] (aux rows written only
+ * when aux_on). Writes slot seq_len[b] of every layer's K1/V1 and nothing else of the cache.
+ * On a non-default stream the first call for a given set of arguments captures the step into a
+ * CUDA graph and later identical calls replay it (see dualflow_set_graphs). */
+DF_API int dualflow_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
+                  int32_t batch, float* logits, int32_t aux_on, dualflow_stream stream);
+
+/* dualflow_step with HOST token and logit buffers: copies tokens_host [batch] to the device,
+ * runs the step, copies logits [2, batch, vocab] back to logits_host and synchronizes `stream`.
+ * Pinned host memory gives asynchronous copies. */
+DF_API int dualflow_step_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+                       const int32_t* tokens_host, int32_t batch, float* logits_host, int32_t aux_on,
+                       dualflow_stream stream);
+
+/* Enables (1, default) or disables (0) CUDA-graph capture and replay in dualflow_step. */
+DF_API int dualflow_set_graphs(dualflow_ctx* ctx, int32_t enabled);
+
+/* Synchronizes `stream`, then returns and clears the device status word: DF_OK, or the first
+ * DF_ERR_DEVICE_BOUNDS / DF_ERR_TIMEOUT latched by a kernel since the last call. */
+DF_API int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DUALFLOW_H */

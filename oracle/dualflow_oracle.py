@@ -46,6 +46,8 @@ are silent, each one a choice of this implementation:
      (replay, widened) and its weights the softmax of its own logits r2 over that set.
      b couples an expert's intermediate only when the expert is in both flows' sets.
   R9 mixture head: alpha = 1/2 + 1/2 * sum_i p1_i^2 (collision probability mapped to [1/2, 1]).
+  R10 an attention-only call on a sequence with nothing cached (L_b = 0) returns o = 0 (softmax
+     over an empty set is undefined; the step itself always attends at least its own new entry).
 
 Precision: inputs arrive as the stored values widened to fp64. With mirror=True and a bf16
 workload the oracle rounds (to nearest bf16, ties to even) exactly where the GPU path stores
@@ -367,6 +369,9 @@ def attention_only_step(hp: HParams, q1: np.ndarray, h2: np.ndarray, Wq: np.ndar
         if aux_on:
             qs.append(Wq @ h2[b] + a * q1[b].reshape(-1))
         qs = [_store(rope(qf.reshape(Hq, D), L, hp.rope_base), hp, mirror) for qf in qs]
+        if L == 0:  # R10
+            out[: len(qs), i] = 0.0
+            continue
         Kc, Vc = cache.seq(b, L)
         for f in range(len(qs)):
             for h in range(Hq):

@@ -1,0 +1,76 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol, and rejects bad
+configurations on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dual_flow_decode_dualflow_b300 as dfl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dualflow.h")
+
+
+def declared_functions():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"DF_API\s+(?:const\s+)?\w+\*?\s+(dualflow_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("dualflow_init", "dualflow_decode_attention", "dualflow_stacked_linear", "dualflow_coupled_mlp",
+              "dualflow_step", "dualflow_free"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = dfl.load_library()
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(dfl.C_FUNCTIONS) >= set(declared_functions())
+
+
+def test_status_strings():
+    for code in range(9):
+        s = dfl.dualflow_status_string(code)
+        assert s and s != "unknown status"
+    assert dfl.dualflow_status_string(99) == "unknown status"
+
+
+def _good(**kw):
+    base = dict(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=1, head_dim=128, ffn_hidden=512, vocab=1000,
+                dtype=dfl.DF_DTYPE_BF16, max_batch=4, max_ctx=256)
+    base.update(kw)
+    return dfl.make_config(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=7), dfl.DF_ERR_DTYPE),
+    (dict(d_model=0), dfl.DF_ERR_ARG),
+    (dict(max_batch=-1), dfl.DF_ERR_ARG),
+    (dict(n_q_heads=6, n_kv_heads=4), dfl.DF_ERR_SHAPE),
+    (dict(head_dim=64), dfl.DF_ERR_UNSUPPORTED),
+    (dict(n_q_heads=16, n_kv_heads=1), dfl.DF_ERR_UNSUPPORTED),
+    (dict(d_model=200), dfl.DF_ERR_UNSUPPORTED),
+    (dict(max_batch=200), dfl.DF_ERR_UNSUPPORTED),
+    (dict(paged=1, page_size=16, max_pages=0), dfl.DF_ERR_ARG),
+    (dict(paged=1, page_size=8, max_pages=10), dfl.DF_ERR_UNSUPPORTED),
+    (dict(n_experts=4, topk_primary=5, topk_aux=1), dfl.DF_ERR_SHAPE),
+    (dict(rms_eps=-1.0), dfl.DF_ERR_ARG),
+])
+def test_init_rejects_bad_config_on_host(kw, code):
+    rc, h = dfl.dualflow_init_status(_good(**kw))
+    assert rc == code and h is None
+
+
+def test_null_arguments_rejected():
+    lib = dfl.load_library()
+    assert lib.dualflow_init(None, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_free(None) == dfl.DF_OK
+    assert lib.dualflow_step(None, None, None, None, 1, None, 1, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_decode_attention(None, None, None, None, None, None, 0, 1, None, 1, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_stacked_linear(None, None, 1, 0, None, 1, 64, None, 0, None, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_coupled_mlp(None, None, None, 0, 1, 1, None, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_set_graphs(None, 1) == dfl.DF_ERR_ARG
+    assert lib.dualflow_sync_status(None, None) == dfl.DF_ERR_ARG
