@@ -1,0 +1,394 @@
+#!/usr/bin/env python
+"""Dual-flow decode benchmark on B300: tokens/s of the whole decode step and achieved HBM bandwidth.
+
+Workload: the 24-layer dense dual-flow model (d_model 2048, 16/4 heads of 128, SwiGLU 8192, vocab
+32000), batch 32, every sequence with 4096 cached positions, bf16 storage / fp32 accumulation,
+synthetic seeded inputs generated in place. One step = one decode step of both flows for the
+whole batch (embeddings -> 24 x {RMSNorm, QKV + query coupling + RoPE + KV append, shared-KV
+attention, O projection, RMSNorm, gate/up + SwiGLU + b coupling, down + c coupling} -> final
+RMSNorm -> LM head), replayed as one CUDA graph through dualflow_step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs its own replica (independent sequences: no data-path collective);
+value = total tokens of all ranks / max-over-ranks step time. --impl reference times the CPU
+fp64 oracle on a bounded sample of the same workload and scales it to the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dual-flow decode tokens/s at 1 B300; achieved HBM GB/s vs ~8 TB/s roofline"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6400.0
+
+
+def load_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def workload():
+    from dfsynth import workloads as W
+    return W.DENSE_24L_B32_L4096
+
+
+def step_bytes(w) -> dict:
+    """Algorithmic HBM bytes of one step: every weight once, every cached K1/V1 element once, the
+    appended entries, the gathered embedding rows and the fp32 logits."""
+    from dfsynth import workloads as W
+    es = 2 if w.dtype == "bf16" else 4
+    weights = sum(s.numel for s in W.global_specs(w) if s.name in ("W_lm", "g_final")) * es
+    for l in range(w.n_layers):
+        weights += sum(s.numel for s in W.layer_specs(w, l) if not s.name.endswith((".K", ".V"))) * es
+    lens = w.seq_lens()
+    kv_per_pos = w.n_kv_heads * w.head_dim * es * 2  # K and V
+    kv_read = int(lens.sum()) * kv_per_pos * w.n_layers
+    kv_write = w.batch * kv_per_pos * w.n_layers
+    emb = 2 * w.batch * w.d_model * es
+    logits = 2 * w.batch * w.vocab * 4
+    # one attention launch reads positions 0..L_b (the appended one included), q, and writes o
+    qo = 2 * w.batch * w.n_q_heads * w.head_dim * es
+    attn = int((lens + 1).sum()) * kv_per_pos + 2 * qo
+    return dict(total=weights + kv_read + kv_write + emb + logits, weights=weights, kv_read=kv_read,
+                kv_write=kv_write, attention_per_launch=attn)
+
+
+def attention_traffic() -> float | None:
+    """DRAM bytes per attention launch from the committed ncu summary, if the kernel is unchanged."""
+    prof = os.path.join(ROOT, "profiles", "attention_dense_24l_b32_l4096.md")
+    src = os.path.join(ROOT, "dual_flow_decode_dualflow_b300", "csrc", "attn_bf16.cu")
+    try:
+        txt = open(prof).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    rec = dict(line.split(":", 1) for line in txt.splitlines() if line.startswith(("source_sha256:", "traffic_bytes_per_launch:")))
+    if rec.get("source_sha256", "").strip() != sha:
+        return None
+    try:
+        return float(rec["traffic_bytes_per_launch"].strip())
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def mark(self, start: bool):
+        if start:
+            self.t_start = time.time()
+        else:
+            self.t_end = time.time()
+
+    def __enter__(self):
+        self.t_start = self.t_end = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200", "-i",
+                 str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, mxv = float(f[2]), float(f[3])
+            except ValueError:
+                continue
+            if self.t_start is not None and not (self.t_start - 0.05 <= ts <= (self.t_end or ts) + 0.05):
+                continue
+            sm.append(clk)
+            mx = mxv
+            for n, v in zip(names, f[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+class OracleSample:
+    """The CPU oracle on a bounded sample of the workload: the first `n_layers` layers and the
+    sequences in `rows`, inputs drawn and widened beforehand. time_step() times one oracle decode
+    step on a subset of those rows; full_step() scales it to the whole workload's step."""
+
+    def __init__(self, w, rows, n_layers):
+        import oracle as O
+        from tests import gpu_harness as H
+        self.O, self.w, self.rows, self.n_layers = O, w, list(rows), n_layers
+        ws = w.replace(n_layers=n_layers)
+        self.layers = [H.LazyLayers(ws)[l] for l in range(n_layers)]
+        self.caches = []
+        for l in range(n_layers):
+            kc, vc = H.LazySeqCache(ws, f"L{l}.K"), H.LazySeqCache(ws, f"L{l}.V")
+            self.caches.append(O.DenseCache({b: kc[b] for b in self.rows}, {b: vc[b] for b in self.rows}))
+        self.glob = {"E1": H.LazyRows(ws, "E1"), "E2": H.LazyRows(ws, "E2"), "W_lm": H.host_f64(ws, "W_lm"),
+                     "g_final": H.host_f64(ws, "g_final")}
+        self.tokens, self.lens, self.hp = ws.tokens(), ws.seq_lens(), H.hparams(ws)
+
+    def time_step(self, rows) -> float:
+        t0 = time.perf_counter()
+        self.O.decode_step(self.hp, self.glob, self.layers, self.caches, self.tokens, self.lens, aux_on=True,
+                           mirror=True, rows=rows)
+        return time.perf_counter() - t0
+
+    def full_step(self, seconds: float, n_rows: int) -> float:
+        # the LM head costs about one layer: scale (sample layers + head) to (all layers + head)
+        return seconds * (self.w.batch / n_rows) * (self.w.n_layers + 1) / (self.n_layers + 1)
+
+    def describe(self, n_rows: int) -> str:
+        return (f"oracle (numpy fp64) decode step of both flows on {n_rows} of {self.w.batch} sequences x "
+                f"{self.n_layers} of {self.w.n_layers} layers + LM head (inputs drawn beforehand), scaled to the "
+                f"full step by sequences and by (layers + 1)")
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return int(max(n)) if n else 1
+    except Exception:
+        return 1
+
+
+def run_reference(args, w) -> dict:
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample per step (one sequence,
+    rotating through the batch, over the first layer and the LM head)."""
+    rows = list(range(min(8, w.batch)))
+    samp = OracleSample(w, rows, 1)
+    per = []
+    for i in range(args.warmup + args.steps):
+        t = samp.time_step([rows[i % len(rows)]])
+        if i >= args.warmup:
+            per.append(samp.full_step(t, 1))
+    desc = samp.describe(1)
+    s = statistics.median(per)
+    value = w.batch / s
+    cores = blas_threads()
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx_len, "layers": w.n_layers},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
+    import torch
+
+    import dual_flow_decode_dualflow_b300 as dfl
+    from tests import gpu_harness as H
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = torch.distributed if world > 1 else None
+    run = H.DeviceRun(w, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def timed(aux_on: int, steps: int, warmup: int, sampler=None):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                run.step(aux_on=aux_on, stream=stream)
+        stream.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ctx = sampler if sampler is not None else _Null()
+        with ctx:
+            if sampler is not None:
+                sampler.mark(True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(steps):
+                    run.step(aux_on=aux_on, stream=stream)
+                e1.record(stream)
+            e1.synchronize()
+            if sampler is not None:
+                sampler.mark(False)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ms = e0.elapsed_time(e1) / steps
+        if dist:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    ms = timed(1, args.steps, args.warmup, sampler)
+    st = dfl.dualflow_sync_status(run.ctx)
+    if st != 0:
+        raise RuntimeError(f"device status after the timed steps: {dfl.dualflow_status_string(st)}")
+    _, launches = dfl.dualflow_profile_read(run.ctx)
+    if args.quick:
+        run.close()
+        if rank == 0:
+            return {"metric": METRIC, "value": world * w.batch / (ms * 1e-3), "unit": "tokens/s",
+                    "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "n_gpus": world,
+                    "config": {"workload": w.name, "layers": w.n_layers}, "note": "quick run (no extras)"}
+        return None
+    ms_primary = timed(0, max(args.steps // 2, 3), 3)
+
+    # per-kernel times inside the step (event pairs captured into the step's graph)
+    dfl.dualflow_set_profiling(run.ctx, 1)
+    fam_ms = [0.0] * dfl.DF_PROF_FAMILIES
+    fam_n = [0] * dfl.DF_PROF_FAMILIES
+    nprof = max(min(args.steps, 50), 3)
+    with torch.cuda.stream(stream):
+        for i in range(3 + nprof):
+            run.step(aux_on=1, stream=stream)
+            t, n = dfl.dualflow_profile_read(run.ctx)
+            if i >= 3:
+                fam_ms = [a + b for a, b in zip(fam_ms, t)]
+                fam_n = [a + b for a, b in zip(fam_n, n)]
+    dfl.dualflow_set_profiling(run.ctx, 0)
+
+    # end to end through the host-buffer C-ABI call: tokens H2D, step, logits D2H, every step
+    tok = torch.from_numpy(run.tokens_np.copy()).pin_memory()
+    out = torch.empty((2, w.batch, w.vocab), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
+    if dist:
+        dist.barrier()
+    e2e_steps = max(args.steps // 2, 3)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    run.close()
+    if rank != 0:
+        return None
+
+    peak, peak_kind = load_peaks()
+    nb = step_bytes(w)
+    step_gbs = nb["total"] / (ms * 1e-3) / 1e9
+    att_ms = fam_ms[dfl.PROF_NAMES.index("attention")] / max(fam_n[dfl.PROF_NAMES.index("attention")], 1)
+    att_gbs = nb["attention_per_launch"] / (att_ms * 1e-3) / 1e9
+    prof_total = sum(fam_ms) / nprof
+    samp = OracleSample(w, [0, 1, 2, 3], 6)
+    cpu_s = samp.full_step(samp.time_step([0, 1, 2, 3]), 4)
+    cpu_desc = samp.describe(4)
+    launches_per_step = int(sum(launches))
+    res = {
+        "metric": METRIC, "value": world * w.batch / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
+        "data": "synthetic: seeded counter-hash generator, random-init weights of the workload's shapes",
+        "config": {"workload": w.name, "layers": w.n_layers, "d_model": w.d_model, "q_heads": w.n_q_heads,
+                   "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "ffn_hidden": w.ffn_hidden,
+                   "vocab": w.vocab, "batch_per_gpu": w.batch, "ctx": w.ctx_len,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {nb['total'] / 1e9:.2f} GB per step vs 126 MB L2, no flush"},
+        "hbm": {"step_bytes": nb["total"], "achieved_gbs": step_gbs, "frac_of_8000": step_gbs / NOMINAL_HBM_GBS,
+                f"frac_of_{peak_kind}": step_gbs / peak},
+        "primary_only": {"ms_per_step": ms_primary, "dual_over_primary": ms / ms_primary},
+        "roofline": {"kernel": "attn_bf16_kernel (shared-KV decode attention)", "bound": "hbm",
+                     "achieved": att_gbs, "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "bytes_per_launch": nb["attention_per_launch"],
+                     "avg_launch_ms": att_ms, "traffic": attention_traffic()},
+        "kernel_ms_per_step": {n: fam_ms[i] / nprof for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
+        "kernel_share": {n: fam_ms[i] / nprof / prof_total for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
+        "cpu_baseline": {"value": w.batch / cpu_s, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": cpu_desc},
+        "e2e": {"value": world * w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(tok.numel() * 4),
+                "d2h_bytes_per_step": int(out.numel() * 4),
+                "api": "dualflow_step_host (pinned host tokens in, host logits out, stream sync per step)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
+        "clocks": sampler.summary(),
+    }
+    return res
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling captures only: run the workload with this many layers")
+    ap.add_argument("--quick", action="store_true", help="profiling captures only: time the step, skip the rest")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = workload()
+    if args.layers:
+        w = w.replace(n_layers=args.layers)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, w)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, w, rank, world, local_rank)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -22,7 +22,9 @@ DF_EPI_STORE_F32, DF_EPI_STORE_BF16, DF_EPI_ADD_F32, DF_EPI_COUPLE_ADD = 0, 1, 2
 
 C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dualflow_decode_attention",
                "dualflow_stacked_linear", "dualflow_coupled_mlp", "dualflow_step", "dualflow_step_host",
-               "dualflow_set_graphs", "dualflow_sync_status")
+               "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status")
+DF_PROF_FAMILIES = 8
+PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
 
 class dualflow_config(ctypes.Structure):
@@ -75,6 +77,8 @@ def load_library(path: str = LIB_PATH):
         "dualflow_step": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, vp, i32, vp], i32),
         "dualflow_step_host": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, vp, i32, vp], i32),
         "dualflow_set_graphs": ([vp, i32], i32),
+        "dualflow_set_profiling": ([vp, i32], i32),
+        "dualflow_profile_read": ([vp, POINTER(c_float), POINTER(i32), i32], i32),
         "dualflow_sync_status": ([vp, vp], i32),
     }
     for name, (args, res) in sig.items():
@@ -169,6 +173,18 @@ def dualflow_step_host(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens_hos
 
 def dualflow_set_graphs(ctx, enabled: int) -> None:
     _check("dualflow_set_graphs", load_library().dualflow_set_graphs(ctx, enabled))
+
+
+def dualflow_set_profiling(ctx, enabled: int) -> None:
+    _check("dualflow_set_profiling", load_library().dualflow_set_profiling(ctx, enabled))
+
+
+def dualflow_profile_read(ctx) -> tuple[list[float], list[int]]:
+    """(ms per kernel family, launches per kernel family) of the last dualflow_step."""
+    ms = (c_float * DF_PROF_FAMILIES)()
+    n = (c_int32 * DF_PROF_FAMILIES)()
+    _check("dualflow_profile_read", load_library().dualflow_profile_read(ctx, ms, n, DF_PROF_FAMILIES))
+    return list(ms), list(n)
 
 
 def dualflow_sync_status(ctx, stream=None) -> int:

@@ -87,7 +87,7 @@ int validate_config(const dualflow_config* c) {
     if (c->paged && c->page_size != 16 && c->page_size != 32 && c->page_size != 64) return DF_ERR_UNSUPPORTED;
     if (c->n_experts > 0) return DF_ERR_UNSUPPORTED;
   } else {
-    if (c->head_dim / 2 > 1024 || c->max_ctx > 40000) return DF_ERR_UNSUPPORTED;
+    if (c->head_dim / 2 > 1024 || c->max_ctx > 40000 || c->d_model % 4) return DF_ERR_UNSUPPORTED;
     if (c->n_experts > 0) return DF_ERR_UNSUPPORTED;
   }
   return DF_OK;
@@ -169,11 +169,40 @@ int check_weights(const dualflow_ctx* ctx, const dualflow_weights* w) {
   return DF_OK;
 }
 
+// ------------------------------------------------------------------ launch bookkeeping
+// Counts every kernel the step launches by family and, when profiling is on, brackets it with a
+// CUDA event pair on the launching stream. The records are external event nodes when the step is
+// being captured, so the replayed graph records them (a plain record during capture would only
+// become an internal dependency, with no timestamp).
+struct Launcher {
+  dualflow_ctx* ctx;
+  cudaStream_t s;
+  template <class F>
+  int operator()(int fam, F&& f) {
+    ctx->step_launches[fam]++;
+    ProfRec* r = nullptr;
+    if (ctx->profiling && ctx->prof_n < (int)ctx->prof.size()) {
+      r = &ctx->prof[ctx->prof_n++];
+      r->fam = fam;
+      if (cudaEventRecordWithFlags(r->a, s, cudaEventRecordExternal) != cudaSuccess) return DF_ERR_CUDA;
+    }
+    const int rc = f();
+    if (r && cudaEventRecordWithFlags(r->b, s, cudaEventRecordExternal) != cudaSuccess) return DF_ERR_CUDA;
+    return rc;
+  }
+};
+
+void reset_counts(dualflow_ctx* ctx) {
+  for (int& n : ctx->step_launches) n = 0;
+  ctx->prof_n = 0;
+}
+
 // ------------------------------------------------------------------ the MLP block
 int run_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int batch, int aux_on, cudaStream_t s) {
   const dualflow_config& c = ctx->cfg;
   const int mp = batch, ma = aux_on ? batch : 0;
-  DF_TRY(launch_rmsnorm(ctx, h, w->g_mlp[l], ctx->x, batch, aux_on, s));
+  Launcher L{ctx, s};
+  DF_TRY(L(DF_PROF_NORM, [&] { return launch_rmsnorm(ctx, h, w->g_mlp[l], ctx->x, batch, aux_on, s); }));
   if (c.dtype == DF_DTYPE_BF16) {
     GemmArgs g = gemm_args(ctx);
     g.x = ctx->x;
@@ -186,25 +215,32 @@ int run_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int b
     g.y = ctx->u;
     g.ldy = c.ffn_hidden;
     g.vec = w->b[l];
-    DF_TRY(launch_gemm_tc(ctx, g, s));
-    g = gemm_args(ctx);
-    g.x = ctx->u;
-    g.W = w->Wd[l];
-    g.n_out = c.d_model;
-    g.k = c.ffn_hidden;
-    g.m_p = mp;
-    g.m_a = ma;
-    g.epi = EPI_COUPLE_ADD;
-    g.y = h;
-    g.ldy = c.d_model;
-    g.vec = w->c[l];
-    return launch_gemm_tc(ctx, g, s);
+    DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_gemm_tc(ctx, g, s); }));
+    GemmArgs d = gemm_args(ctx);
+    d.x = ctx->u;
+    d.W = w->Wd[l];
+    d.n_out = c.d_model;
+    d.k = c.ffn_hidden;
+    d.m_p = mp;
+    d.m_a = ma;
+    d.epi = EPI_COUPLE_ADD;
+    d.y = h;
+    d.ldy = c.d_model;
+    d.vec = w->c[l];
+    return L(DF_PROF_DOWN, [&] { return launch_gemm_tc(ctx, d, s); });
   }
   const int M = mp + ma, F = c.ffn_hidden;
-  DF_TRY(launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wgu[l], 2 * F, c.d_model, ctx->raw, 0, s));
-  DF_TRY(launch_swiglu_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->b[l], (float*)ctx->u, s));
-  DF_TRY(launch_linear_f32(ctx, (const float*)ctx->u, M, (const float*)w->Wd[l], c.d_model, F, ctx->raw, 0, s));
-  return launch_couple_add_f32(ctx, ctx->raw, batch, aux_on, c.d_model, (const float*)w->c[l], h, s);
+  DF_TRY(L(DF_PROF_GATEUP, [&] {
+    return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wgu[l], 2 * F, c.d_model, ctx->raw, 0, s);
+  }));
+  DF_TRY(L(DF_PROF_OTHER,
+           [&] { return launch_swiglu_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->b[l], (float*)ctx->u, s); }));
+  DF_TRY(L(DF_PROF_DOWN, [&] {
+    return launch_linear_f32(ctx, (const float*)ctx->u, M, (const float*)w->Wd[l], c.d_model, F, ctx->raw, 0, s);
+  }));
+  return L(DF_PROF_OTHER, [&] {
+    return launch_couple_add_f32(ctx, ctx->raw, batch, aux_on, c.d_model, (const float*)w->c[l], h, s);
+  });
 }
 
 // ------------------------------------------------------------------ the whole step
@@ -214,9 +250,15 @@ int run_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv
   const int mp = batch, ma = aux_on ? batch : 0, M = mp + ma;
   const bool bf16 = c.dtype == DF_DTYPE_BF16;
   const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
-  DF_TRY(launch_embed_rmsnorm(ctx, w->E1, w->E2, tokens, c.n_layers > 0 ? w->g_attn[0] : w->g_final, batch, aux_on, s));
+  reset_counts(ctx);
+  Launcher L{ctx, s};
+  DF_TRY(L(DF_PROF_NORM, [&] {
+    return launch_embed_rmsnorm(ctx, w->E1, w->E2, tokens, c.n_layers > 0 ? w->g_attn[0] : w->g_final, batch,
+                                aux_on, s);
+  }));
   for (int l = 0; l < c.n_layers; ++l) {
-    if (l > 0) DF_TRY(launch_rmsnorm(ctx, ctx->h, w->g_attn[l], ctx->x, batch, aux_on, s));
+    if (l > 0)
+      DF_TRY(L(DF_PROF_NORM, [&] { return launch_rmsnorm(ctx, ctx->h, w->g_attn[l], ctx->x, batch, aux_on, s); }));
     if (bf16) {
       GemmArgs g = gemm_args(ctx);
       g.x = ctx->x;
@@ -232,30 +274,40 @@ int run_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv
       g.k_cache = kv->k[l];
       g.v_cache = kv->v[l];
       g.page_table = kv->page_table;
-      DF_TRY(launch_gemm_tc(ctx, g, s));
-      DF_TRY(launch_attention_bf16(ctx, attn_args(ctx, kv, l, batch, 1, aux_on), s));
-      g = gemm_args(ctx);
-      g.x = ctx->o;
-      g.W = w->Wo[l];
-      g.n_out = c.d_model;
-      g.k = qd;
-      g.m_p = mp;
-      g.m_a = ma;
-      g.epi = EPI_ADD_F32;
-      g.y = ctx->h;
-      g.ldy = c.d_model;
-      DF_TRY(launch_gemm_tc(ctx, g, s));
+      DF_TRY(L(DF_PROF_QKV, [&] { return launch_gemm_tc(ctx, g, s); }));
+      const AttnArgs at = attn_args(ctx, kv, l, batch, 1, aux_on);
+      DF_TRY(L(DF_PROF_ATTN, [&] { return launch_attention_bf16(ctx, at, s); }));
+      GemmArgs o = gemm_args(ctx);
+      o.x = ctx->o;
+      o.W = w->Wo[l];
+      o.n_out = c.d_model;
+      o.k = qd;
+      o.m_p = mp;
+      o.m_a = ma;
+      o.epi = EPI_ADD_F32;
+      o.y = ctx->h;
+      o.ldy = c.d_model;
+      DF_TRY(L(DF_PROF_OPROJ, [&] { return launch_gemm_tc(ctx, o, s); }));
     } else {
-      DF_TRY(launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wqkv[l], qkv_n, c.d_model, ctx->raw, 0, s));
-      DF_TRY(launch_qkv_post_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->a[l], kv->k[l], kv->v[l],
-                                 kv->page_table, kv->seq_len, (float*)ctx->q, s));
-      DF_TRY(launch_attention_f32(ctx, (const float*)ctx->q, (float*)ctx->o, kv->k[l], kv->v[l], kv->page_table,
-                                  kv->seq_len, batch, 1, aux_on, s));
-      DF_TRY(launch_linear_f32(ctx, (const float*)ctx->o, M, (const float*)w->Wo[l], c.d_model, qd, ctx->h, 1, s));
+      DF_TRY(L(DF_PROF_QKV, [&] {
+        return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wqkv[l], qkv_n, c.d_model, ctx->raw,
+                                 0, s);
+      }));
+      DF_TRY(L(DF_PROF_OTHER, [&] {
+        return launch_qkv_post_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->a[l], kv->k[l], kv->v[l],
+                                   kv->page_table, kv->seq_len, (float*)ctx->q, s);
+      }));
+      DF_TRY(L(DF_PROF_ATTN, [&] {
+        return launch_attention_f32(ctx, (const float*)ctx->q, (float*)ctx->o, kv->k[l], kv->v[l], kv->page_table,
+                                    kv->seq_len, batch, 1, aux_on, s);
+      }));
+      DF_TRY(L(DF_PROF_OPROJ, [&] {
+        return launch_linear_f32(ctx, (const float*)ctx->o, M, (const float*)w->Wo[l], c.d_model, qd, ctx->h, 1, s);
+      }));
     }
     DF_TRY(run_mlp(ctx, ctx->h, w, l, batch, aux_on, s));
   }
-  DF_TRY(launch_rmsnorm(ctx, ctx->h, w->g_final, ctx->x, batch, aux_on, s));
+  DF_TRY(L(DF_PROF_NORM, [&] { return launch_rmsnorm(ctx, ctx->h, w->g_final, ctx->x, batch, aux_on, s); }));
   if (bf16) {
     GemmArgs g = gemm_args(ctx);
     g.x = ctx->x;
@@ -267,9 +319,11 @@ int run_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv
     g.epi = EPI_STORE_F32;
     g.y = logits;
     g.ldy = c.vocab;
-    return launch_gemm_tc(ctx, g, s);
+    return L(DF_PROF_LMHEAD, [&] { return launch_gemm_tc(ctx, g, s); });
   }
-  return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->W_lm, c.vocab, c.d_model, logits, 0, s);
+  return L(DF_PROF_LMHEAD, [&] {
+    return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->W_lm, c.vocab, c.d_model, logits, 0, s);
+  });
 }
 
 void graph_key(std::vector<uint64_t>& k, const dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
@@ -281,6 +335,7 @@ void graph_key(std::vector<uint64_t>& k, const dualflow_ctx* ctx, const dualflow
   P(logits);
   k.push_back((uint64_t)batch);
   k.push_back((uint64_t)aux_on);
+  k.push_back((uint64_t)ctx->profiling);
   P(w->E1), P(w->E2), P(w->W_lm), P(w->g_final);
   P(kv->seq_len), P(kv->page_table);
   for (int l = 0; l < L; ++l) {
@@ -358,28 +413,6 @@ int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
     return fail(DF_ERR_OOM);
   if (dalloc(&ctx->attn_cnt, (size_t)pairs * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
   cudaMemset(ctx->attn_cnt, 0, (size_t)pairs * sizeof(int32_t));
-  // split-K partials: the largest need among the step's and the attention call's projections
-  if (c.dtype == DF_DTYPE_BF16) {
-    const int n_pad = ((MB + 15) / 16) * 16;
-    struct Shape { int n, k, epi; };
-    const Shape shapes[] = {{qkv_n, c.d_model, EPI_QKV}, {c.d_model, qd, EPI_ADD_F32},
-                            {c.ffn_hidden, c.d_model, EPI_SWIGLU}, {c.d_model, c.ffn_hidden, EPI_COUPLE_ADD},
-                            {c.vocab, c.d_model, EPI_STORE_F32}, {qd, c.d_model, EPI_Q2}};
-    size_t need = 0;
-    int tiles = 1;
-    for (const Shape& sh : shapes) {
-      if (sh.n <= 0 || sh.k <= 0) continue;
-      const int t = sh.epi == EPI_SWIGLU ? sh.n / 64 : (sh.n + kGemmTileN - 1) / kGemmTileN;
-      const int sp = gemm_splits(ctx, sh.n, sh.k, sh.epi);
-      if (sp > 1) need = std::max(need, (size_t)sp * t * n_pad * kGemmTileN);
-      tiles = std::max(tiles, t);
-    }
-    ctx->gemm_part_floats = need;
-    ctx->gemm_cnt_n = tiles;
-    if (dalloc(&ctx->gemm_part, need * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
-    if (dalloc(&ctx->gemm_cnt, (size_t)tiles * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
-    cudaMemset(ctx->gemm_cnt, 0, (size_t)tiles * sizeof(int32_t));
-  }
   const size_t xw = std::max({c.d_model, c.ffn_hidden, qd});
   const size_t raw_n = std::max({qkv_n, 2 * c.ffn_hidden, c.d_model, c.vocab, qd});
   if (dalloc(&ctx->h, (size_t)MB * c.d_model * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
@@ -400,7 +433,11 @@ int dualflow_free(dualflow_ctx* ctx) {
   if (!ctx) return DF_OK;
   cudaDeviceSynchronize();
   drop_graphs(ctx);
-  void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->gemm_part, ctx->gemm_cnt, ctx->h,
+  for (auto& r : ctx->prof) {
+    if (r.a) cudaEventDestroy(r.a);
+    if (r.b) cudaEventDestroy(r.b);
+  }
+  void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
                   ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -474,11 +511,6 @@ int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_primary,
             : epilogue == DF_EPI_STORE_BF16 ? EPI_STORE_BF16
             : epilogue == DF_EPI_ADD_F32 ? EPI_ADD_F32
                                           : EPI_COUPLE_ADD;
-    const size_t n_pad = ((size_t)(m_primary + m_aux) + 15) / 16 * 16;
-    const int sp = gemm_splits(ctx, n, k, g.epi);
-    const int tiles = (n + kGemmTileN - 1) / kGemmTileN;
-    if (sp > 1 && ((size_t)sp * tiles * n_pad * kGemmTileN > ctx->gemm_part_floats || tiles > ctx->gemm_cnt_n))
-      return DF_ERR_SHAPE;
     return launch_gemm_tc(ctx, g, s);
   }
   const int M = m_primary + m_aux;
@@ -500,6 +532,7 @@ int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w,
   if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
   if (layer < 0 || layer >= ctx->cfg.n_layers) return DF_ERR_ARG;
   DF_TRY(check_weights(ctx, w));
+  reset_counts(ctx);
   return run_mlp(ctx, h, w, layer, batch, aux_on, S(stream));
 }
 
@@ -562,6 +595,37 @@ int dualflow_set_graphs(dualflow_ctx* ctx, int32_t enabled) {
   if (!ctx || (enabled != 0 && enabled != 1)) return DF_ERR_ARG;
   ctx->graphs_enabled = enabled;
   if (!enabled) drop_graphs(ctx);
+  return DF_OK;
+}
+
+int dualflow_set_profiling(dualflow_ctx* ctx, int32_t enabled) {
+  if (!ctx || (enabled != 0 && enabled != 1)) return DF_ERR_ARG;
+  if (enabled && ctx->prof.empty()) {
+    const int n = 8 * std::max(ctx->cfg.n_layers, 1) + 16;
+    ctx->prof.resize(n);
+    for (auto& r : ctx->prof)
+      if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return DF_ERR_CUDA;
+  }
+  if (ctx->profiling != enabled) drop_graphs(ctx);
+  ctx->profiling = enabled;
+  return DF_OK;
+}
+
+int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches, int32_t n_families) {
+  if (!ctx || n_families < 0) return DF_ERR_ARG;
+  const int n = std::min<int>(n_families, DF_PROF_FAMILIES);
+  if (cudaDeviceSynchronize() != cudaSuccess) return DF_ERR_CUDA;
+  if (launches)
+    for (int f = 0; f < n; ++f) launches[f] = ctx->step_launches[f];
+  if (ms) {
+    for (int f = 0; f < n; ++f) ms[f] = 0.f;
+    if (ctx->profiling)
+      for (int i = 0; i < ctx->prof_n; ++i) {
+        float t = 0.f;
+        if (cudaEventElapsedTime(&t, ctx->prof[i].a, ctx->prof[i].b) != cudaSuccess) return DF_ERR_CUDA;
+        if (ctx->prof[i].fam < n) ms[ctx->prof[i].fam] += t;
+      }
+  }
   return DF_OK;
 }
 

@@ -5,7 +5,8 @@
 // both flows. For every (sequence b, KV head g) the kernel scores the 2*G query rows of group g --
 // the G primary heads and the G coupled auxiliary heads -- against the same tile:
 //   S^T (16 keys x 8 rows) = K_tile (16 x 128) . Q^T   and   O^T (128 x 8) += V^T . P^T
-// with mma.sync m16n8k16 (keys as M, the 8 query rows as N: no padding). Tiles of 64 keys are
+// with mma.sync m16n8k16 (keys as M, the 8 query rows as N: no padding; P enters as a bf16
+// hi/lo pair, two MMAs, so the probabilities are not truncated to 8 significant bits). Tiles of 64 keys are
 // staged in shared memory by TMA (128-byte swizzle) through a 3-stage mbarrier pipeline fed by a
 // producer warp; four consumer warps take 16 keys each and keep their own online-softmax state
 // (running max via warp shuffles), merged at the end of a segment.
@@ -86,7 +87,7 @@ __device__ __forceinline__ int owner_of(long long t, long long T, int C) { retur
 
 __device__ __forceinline__ uint32_t swz(int key, int chunk) { return (uint32_t)(key * 128 + ((chunk ^ (key & 7)) << 4)); }
 
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_kernel(const __grid_constant__ CUtensorMap map_k,
+__global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid_constant__ CUtensorMap map_k,
                                                                      const __grid_constant__ CUtensorMap map_v,
                                                                      const AttnParams P) {
   extern __shared__ uint8_t smem_raw[];
@@ -286,9 +287,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_kernel(const __grid
         o[mt][2] *= cr0;
         o[mt][3] *= cr1;
       }
-      // P^T (keys x rows) -> B fragments via an in-register 8x8 transpose
-      const uint32_t pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
-      const uint32_t pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+      // P^T (keys x rows) -> B fragments via an in-register 8x8 transpose. P is carried as a bf16
+      // pair hi + lo (lo = the rounding residual of hi), so the probabilities enter the fp32
+      // accumulation with ~16 significant bits instead of bf16's 8.
+      uint32_t ph0, ph1, pl0, pl1;
+      {
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1), h23 = __floats2bfloat162_rn(p2, p3);
+        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+        ph0 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h01));
+        ph1 = movmatrix_trans(*reinterpret_cast<const uint32_t*>(&h23));
+        pl0 = movmatrix_trans(pack_bf16x2(p0 - f01.x, p1 - f01.y));
+        pl1 = movmatrix_trans(pack_bf16x2(p2 - f23.x, p3 - f23.y));
+      }
       // O^T += V^T . P^T
       {
         const int mi = lane >> 3;
@@ -298,7 +308,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_bf16_kernel(const __grid
           const int chunk = ((mt & 3) << 1) + (mi & 1);
           uint32_t a0, a1, a2, a3;
           ldmatrix_x4_trans(Vb + (mt >> 2) * kHalf + swz(key, chunk), a0, a1, a2, a3);
-          mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+          mma_bf16_16816(o[mt], a0, a1, a2, a3, ph0, ph1);
+          mma_bf16_16816(o[mt], a0, a1, a2, a3, pl0, pl1);
         }
       }
       if (zeroed) fence_proxy_async_smem();
@@ -461,8 +472,9 @@ int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s) 
   p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
   const size_t smem = 1024 + (size_t)kStagesA * kStageBytes + 2 * kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
                       (size_t)(a.batch + 1) * 4;
-  cudaError_t e = cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return DF_ERR_CUDA;
+  if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return DF_ERR_CUDA;
   attn_bf16_kernel<<<ctx->attn_ctas, kAttnThreads, smem, s>>>(mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

@@ -6,9 +6,12 @@
 // flows ("Custos de Inferencia vs. Treinamento": grouping keeps the unique weights read unchanged).
 // Weight and activation tiles are staged by TMA (128-byte swizzle) through a 4-stage mbarrier
 // pipeline; one elected thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in TMEM).
-// When the output has too few tiles to fill the GPU the reduction dimension is split across CTAs;
-// the last CTA to finish a tile sums the fp32 partials in split order (deterministic, independent
-// of which flows are present) and runs the epilogue:
+// When the output has too few tiles to fill the GPU the reduction dimension is split across the S
+// CTAs of a thread-block cluster (S <= 8). Each CTA parks its fp32 partial tile in shared memory;
+// after a cluster barrier every CTA sums, over distributed shared memory and in rank order (so the
+// result is deterministic and independent of which flows are present), its own 1/S slice of the
+// tile's features -- feature i and its RoPE / gate-up partner i + 64 travel together -- and runs
+// the epilogue on that slice:
 //   EPI_QKV      q1 = Wq.x1, q2 = Wq.x2 + a (*) q1 (before RoPE), RoPE(q1, q2, k1) at position
 //                seq_len[b], q stored bf16, primary k1/v1 appended to the cache at slot seq_len[b]
 //                ("Atencao de KV Compartilhada Assimetrica": the auxiliary flow writes no K/V)
@@ -29,11 +32,9 @@ constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per s
 struct GemmParams {
   GemmArgs a;
   int n_pad;     // activation rows padded to a multiple of 16 (the MMA's N)
-  int splits;
+  int splits;    // CTAs of the cluster sharing one tile's reduction (1, 2, 4 or 8)
   int kb_total;  // k / 64
   int n_tiles;
-  float* part;   // [splits][n_tiles][n_pad][128] fp32 partials (splits > 1)
-  int32_t* cnt;  // [n_tiles] arrival counters, left at zero
   int32_t* status;
 };
 
@@ -44,11 +45,6 @@ __device__ __forceinline__ float bf2f(const void* p, size_t i) {
 }
 
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
-
-// RoPE of the pair (x at feature f, xp at the partner f ^ 64) for D = 128 (rotate-half).
-__device__ __forceinline__ float rope_rot(float x, float xp, int f, float2 cs) {
-  return (f < 64) ? (x * cs.x - xp * cs.y) : (x * cs.x + xp * cs.y);
-}
 
 __device__ __forceinline__ size_t cache_slot(const GemmArgs& a, int b, int hk, int pos, int32_t* status, bool* ok) {
   *ok = true;
@@ -81,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty = full + kStages;
   uint64_t* done = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] error, [1] last arriver
+  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] error
   float* acc_s = reinterpret_cast<float*>(smem);       // [n_pad][128], reuses the pipeline after the mainloop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,7 +95,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(done, 1);
     flags[0] = 0;
-    flags[1] = 0;
     fence_mbar_init();
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_x);
@@ -163,171 +158,201 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
 
-  // ---- accumulator: TMEM -> registers -> (smem tile | global split partial) ----
+  // ---- accumulator: TMEM -> registers -> this CTA's fp32 partial tile acc_s[n][128] ----
   const bool acc_ok = mbar_wait(done, 0);
   tc_fence_after();
   if (!acc_ok) set_status(p.status, DF_ERR_TIMEOUT);
-  const int f = threadIdx.x;  // output feature within the tile == TMEM lane
-  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-  float* my_part = (p.splits > 1) ? p.part + ((size_t)split * p.n_tiles + tile) * p.n_pad * kGemmTileN : nullptr;
-  for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
-    float v[16];
-    tmem_ld16(lane_base + (uint32_t)c0, v);
-    if (p.splits == 1) {
+  {
+    const int f = threadIdx.x;  // TMEM lane == output feature within the tile
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
+      float v[16];
+      tmem_ld16(lane_base + (uint32_t)c0, v);
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc_s[(c0 + j) * kGemmTileN + f] = v[j];
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) my_part[(size_t)(c0 + j) * kGemmTileN + f] = v[j];
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, ncols);
 
-  if (p.splits > 1) {
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const int prev = atomicAdd(&p.cnt[tile], 1);
-      flags[1] = (prev == p.splits - 1);
+  // ---- split reduction over distributed shared memory: this CTA owns features
+  //      [lo0, lo0 + nl) and [64 + lo0, 64 + lo0 + nl) of the tile ----
+  const int S = p.splits;
+  const int nl = 64 / S, lo0 = split * nl, nf = 2 * nl;
+  float* red = acc_s + p.n_pad * kGemmTileN;  // [n_pad][nf] (S > 1)
+  if (S > 1) {
+    cluster_sync();
+    const int quads = nf / 4;
+    const uint32_t base = smem_u32(acc_s);
+    for (int it = threadIdx.x; it < p.n_pad * quads; it += kThreads) {
+      const int n = it / quads, qd = it % quads;
+      const int fl = qd * 4;
+      const int f = fl < nl ? lo0 + fl : 64 + lo0 + (fl - nl);
+      const uint32_t off = base + (uint32_t)((n * kGemmTileN + f) * 4);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int r = 0; r < S; ++r) {
+        const float4 v = ld_dsmem_f4(mapa_shared(off, (uint32_t)r));
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      *reinterpret_cast<float4*>(red + n * nf + fl) = acc;
     }
-    __syncthreads();
-    if (!flags[1]) return;
-    __threadfence();
-    for (int n = 0; n < p.n_pad; ++n) {
-      float s = 0.f;
-      for (int sp = 0; sp < p.splits; ++sp)
-        s += __ldcg(p.part + (((size_t)sp * p.n_tiles + tile) * p.n_pad + n) * kGemmTileN + f);
-      acc_s[n * kGemmTileN + f] = s;
-    }
-    if (threadIdx.x == 0) p.cnt[tile] = 0;
     __syncthreads();
   }
+  // reduced value of activation row n, tile feature f (f in this CTA's slice)
+  auto acc = [&](int n, int f) -> float {
+    if (S == 1) return acc_s[n * kGemmTileN + f];
+    return red[n * nf + (f < 64 ? f - lo0 : nl + f - 64 - lo0)];
+  };
 
-  // ---- epilogues (thread f owns output feature tile*128 + f; acc_s[n][f] = row n) ----
+  // ---- epilogues: unit (i, b) covers features i and i + 64 of rows b (and m_p + b) ----
   const GemmArgs& a = p.a;
   const int m = a.m_p + a.m_a;
   if (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || EPI == EPI_ADD_F32) {
-    const int fg = tile * kGemmTileN + f;
-    if (fg < a.n_out) {
-      for (int n = 0; n < m; ++n) {
-        const float v = acc_s[n * kGemmTileN + f];
+    for (int it = threadIdx.x; it < nl * m; it += kThreads) {
+      const int i = lo0 + it % nl, n = it / nl;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int f = i + 64 * hh, fg = tile * kGemmTileN + f;
+        if (fg >= a.n_out) continue;
+        const float v = acc(n, f);
         if (EPI == EPI_STORE_F32) reinterpret_cast<float*>(a.y)[(size_t)n * a.ldy + fg] = v;
         if (EPI == EPI_ADD_F32) reinterpret_cast<float*>(a.y)[(size_t)n * a.ldy + fg] += v;
-        if (EPI == EPI_STORE_BF16) reinterpret_cast<__nv_bfloat16*>(a.y)[(size_t)n * a.ldy + fg] = __float2bfloat16_rn(v);
+        if (EPI == EPI_STORE_BF16)
+          reinterpret_cast<__nv_bfloat16*>(a.y)[(size_t)n * a.ldy + fg] = __float2bfloat16_rn(v);
       }
     }
   } else if (EPI == EPI_COUPLE_ADD) {
-    const int fg = tile * kGemmTileN + f;
-    if (fg < a.n_out) {
-      float* y = reinterpret_cast<float*>(a.y);
-      const float c = bf2f(a.vec, fg);
-      for (int b = 0; b < a.m_p; ++b) {
-        const float z1 = acc_s[b * kGemmTileN + f];
+    float* y = reinterpret_cast<float*>(a.y);
+    for (int it = threadIdx.x; it < nl * a.m_p; it += kThreads) {
+      const int i = lo0 + it % nl, b = it / nl;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int f = i + 64 * hh, fg = tile * kGemmTileN + f;
+        if (fg >= a.n_out) continue;
+        const float z1 = acc(b, f);
         y[(size_t)b * a.ldy + fg] += z1;
-        if (a.m_a > 0) {
-          const float z2 = acc_s[(a.m_p + b) * kGemmTileN + f] + c * z1;
-          y[(size_t)(a.m_p + b) * a.ldy + fg] += z2;
-        }
+        if (a.m_a > 0) y[(size_t)(a.m_p + b) * a.ldy + fg] += acc(a.m_p + b, f) + bf2f(a.vec, fg) * z1;
       }
     }
   } else if (EPI == EPI_SWIGLU) {
-    if (f < 64) {
-      const int j = tile * 64 + f;  // hidden unit
-      __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(a.y);
-      const float bc = bf2f(a.vec, j);
-      for (int b = 0; b < a.m_p; ++b) {
-        const float u1 = silu(acc_s[b * kGemmTileN + f]) * acc_s[b * kGemmTileN + f + 64];
-        u[(size_t)b * a.ldy + j] = __float2bfloat16_rn(u1);
-        if (a.m_a > 0) {
-          const int r = a.m_p + b;
-          const float u2 = silu(acc_s[r * kGemmTileN + f]) * acc_s[r * kGemmTileN + f + 64] + bc * u1;
-          u[(size_t)r * a.ldy + j] = __float2bfloat16_rn(u2);
-        }
+    __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(a.y);
+    for (int it = threadIdx.x; it < nl * a.m_p; it += kThreads) {
+      const int i = lo0 + it % nl, b = it / nl;
+      const int j = tile * 64 + i;  // hidden unit: gate at tile feature i, up at i + 64
+      const float u1 = silu(acc(b, i)) * acc(b, i + 64);
+      u[(size_t)b * a.ldy + j] = __float2bfloat16_rn(u1);
+      if (a.m_a > 0) {
+        const int r = a.m_p + b;
+        u[(size_t)r * a.ldy + j] = __float2bfloat16_rn(silu(acc(r, i)) * acc(r, i + 64) + bf2f(a.vec, j) * u1);
       }
     }
   } else if (EPI == EPI_QKV) {
     const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, B = a.m_p;
-    const int fp = f ^ 64;
     __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(a.q_out);
-    if (tile < Hq) {
-      const int h = tile;
-      const float af = bf2f(a.vec, h * kHeadDim + f), afp = bf2f(a.vec, h * kHeadDim + fp);
-      for (int b = 0; b < B; ++b) {
-        const int pos = a.seq_len[b];
-        if (pos < 0 || pos > a.max_ctx) {
-          set_status(p.status, DF_ERR_DEVICE_BOUNDS);
-          continue;
-        }
-        const float2 cs = a.rope[(size_t)pos * 64 + (f & 63)];
-        const float x1 = acc_s[b * kGemmTileN + f], x1p = acc_s[b * kGemmTileN + fp];
-        qo[(((size_t)0 * B + b) * Hq + h) * kHeadDim + f] = __float2bfloat16_rn(rope_rot(x1, x1p, f, cs));
-        if (a.m_a > 0) {
-          const float x2 = acc_s[(B + b) * kGemmTileN + f] + af * x1;
-          const float x2p = acc_s[(B + b) * kGemmTileN + fp] + afp * x1p;
-          qo[(((size_t)1 * B + b) * Hq + h) * kHeadDim + f] = __float2bfloat16_rn(rope_rot(x2, x2p, f, cs));
-        }
-      }
-    } else {
-      const bool is_k = tile < Hq + Hkv;
-      const int hk = is_k ? tile - Hq : tile - Hq - Hkv;
-      __nv_bfloat16* cache = reinterpret_cast<__nv_bfloat16*>(is_k ? a.k_cache : a.v_cache);
-      for (int b = 0; b < B; ++b) {
-        const int pos = a.seq_len[b];
-        bool ok;
-        const size_t off = cache_slot(a, b, hk, pos, p.status, &ok);
-        if (!ok) continue;
-        float v = acc_s[b * kGemmTileN + f];
-        if (is_k) v = rope_rot(v, acc_s[b * kGemmTileN + fp], f, a.rope[(size_t)pos * 64 + (f & 63)]);
-        cache[off + f] = __float2bfloat16_rn(v);
-      }
-    }
-  } else if (EPI == EPI_Q2) {
-    const int Hq = a.n_q_heads, B = a.m_a;
-    const int h = tile, fp = f ^ 64;
-    __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(a.q_out);
-    const float af = bf2f(a.vec, h * kHeadDim + f), afp = bf2f(a.vec, h * kHeadDim + fp);
-    for (int b = 0; b < B; ++b) {
+    for (int it = threadIdx.x; it < nl * B; it += kThreads) {
+      const int i = lo0 + it % nl, b = it / nl;
       const int pos = a.seq_len[b];
       if (pos < 0 || pos > a.max_ctx) {
         set_status(p.status, DF_ERR_DEVICE_BOUNDS);
         continue;
       }
-      const float2 cs = a.rope[(size_t)pos * 64 + (f & 63)];
+      const float2 cs = a.rope[(size_t)pos * 64 + i];
+      if (tile < Hq) {
+        const int h = tile;
+        const float x1 = acc(b, i), x1p = acc(b, i + 64);
+        const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
+        qo[o1 + i] = __float2bfloat16_rn(x1 * cs.x - x1p * cs.y);
+        qo[o1 + i + 64] = __float2bfloat16_rn(x1p * cs.x + x1 * cs.y);
+        if (a.m_a > 0) {
+          const float x2 = acc(B + b, i) + bf2f(a.vec, h * kHeadDim + i) * x1;
+          const float x2p = acc(B + b, i + 64) + bf2f(a.vec, h * kHeadDim + i + 64) * x1p;
+          const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
+          qo[o2 + i] = __float2bfloat16_rn(x2 * cs.x - x2p * cs.y);
+          qo[o2 + i + 64] = __float2bfloat16_rn(x2p * cs.x + x2 * cs.y);
+        }
+      } else {
+        const bool is_k = tile < Hq + Hkv;
+        const int hk = is_k ? tile - Hq : tile - Hq - Hkv;
+        bool ok;
+        const size_t off = cache_slot(a, b, hk, pos, p.status, &ok);
+        if (!ok) continue;
+        __nv_bfloat16* cache = reinterpret_cast<__nv_bfloat16*>(is_k ? a.k_cache : a.v_cache);
+        float v0 = acc(b, i), v1 = acc(b, i + 64);
+        if (is_k) {
+          const float t0 = v0 * cs.x - v1 * cs.y, t1 = v1 * cs.x + v0 * cs.y;
+          v0 = t0;
+          v1 = t1;
+        }
+        cache[off + i] = __float2bfloat16_rn(v0);
+        cache[off + i + 64] = __float2bfloat16_rn(v1);
+      }
+    }
+  } else if (EPI == EPI_Q2) {
+    const int Hq = a.n_q_heads, B = a.m_a, h = tile;
+    __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(a.q_out);
+    for (int it = threadIdx.x; it < nl * B; it += kThreads) {
+      const int i = lo0 + it % nl, b = it / nl;
+      const int pos = a.seq_len[b];
+      if (pos < 0 || pos > a.max_ctx) {
+        set_status(p.status, DF_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      const float2 cs = a.rope[(size_t)pos * 64 + i];
       const size_t qi = ((size_t)b * Hq + h) * kHeadDim;
-      const float x1 = bf2f(a.q1_in, qi + f), x1p = bf2f(a.q1_in, qi + fp);
-      qo[(((size_t)0 * B + b) * Hq + h) * kHeadDim + f] = __float2bfloat16_rn(rope_rot(x1, x1p, f, cs));
-      const float x2 = acc_s[b * kGemmTileN + f] + af * x1;
-      const float x2p = acc_s[b * kGemmTileN + fp] + afp * x1p;
-      qo[(((size_t)1 * B + b) * Hq + h) * kHeadDim + f] = __float2bfloat16_rn(rope_rot(x2, x2p, f, cs));
+      const float x1 = bf2f(a.q1_in, qi + i), x1p = bf2f(a.q1_in, qi + i + 64);
+      const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
+      qo[o1 + i] = __float2bfloat16_rn(x1 * cs.x - x1p * cs.y);
+      qo[o1 + i + 64] = __float2bfloat16_rn(x1p * cs.x + x1 * cs.y);
+      const float x2 = acc(b, i) + bf2f(a.vec, h * kHeadDim + i) * x1;
+      const float x2p = acc(b, i + 64) + bf2f(a.vec, h * kHeadDim + i + 64) * x1p;
+      const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
+      qo[o2 + i] = __float2bfloat16_rn(x2 * cs.x - x2p * cs.y);
+      qo[o2 + i + 64] = __float2bfloat16_rn(x2p * cs.x + x2 * cs.y);
     }
   }
+  // no CTA may leave while a peer can still read its partial tile
+  if (S > 1) cluster_sync();
 }
 
 template <int EPI>
 int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, size_t smem, cudaStream_t s) {
   auto kern = gemm_tc_kernel<EPI>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return DF_ERR_CUDA;
-  dim3 grid(p.n_tiles, p.splits);
-  kern<<<grid, kThreads, smem, s>>>(mw, mx, p);
-  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return DF_ERR_CUDA;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return DF_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_tiles, p.splits, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)p.splits;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mw, mx, p) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
 }  // namespace
 
 int gemm_tiles(int n_out, int epi) { return epi == EPI_SWIGLU ? n_out / 64 : (n_out + kGemmTileN - 1) / kGemmTileN; }
 
-// Reduction splits: enough CTAs to cover every SM once, never fewer than 2 k-blocks per split.
-// Depends only on the weight shape, never on which flows are present.
+// Reduction splits (cluster size): the smallest power of two, at most 8, that gives every SM a
+// tile slice, with at least 2 k-blocks per CTA. Depends only on the weight shape, never on which
+// flows are present.
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi) {
   const int tiles = gemm_tiles(n_out, epi);
   const int kb = k / kGemmTileK;
-  if (tiles >= ctx->num_sms) return 1;
-  int s = (ctx->num_sms + tiles - 1) / tiles;
-  if (s > kb / 2) s = kb / 2;
-  return s < 1 ? 1 : s;
+  int s = 1;
+  while (s < 8 && tiles * s < ctx->num_sms && 2 * (2 * s) <= kb) s *= 2;
+  return s;
 }
 
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
@@ -342,18 +367,14 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   p.n_tiles = gemm_tiles(a.n_out, a.epi);
   p.splits = gemm_splits(ctx, a.n_out, a.k, a.epi);
   p.status = ctx->status;
-  p.part = ctx->gemm_part;
-  p.cnt = ctx->gemm_cnt;
-  if (p.splits > 1) {
-    const size_t need = (size_t)p.splits * p.n_tiles * p.n_pad * kGemmTileN;
-    if (need > ctx->gemm_part_floats || p.n_tiles > ctx->gemm_cnt_n) return DF_ERR_SHAPE;
-  }
   const uint64_t w_rows = (a.epi == EPI_SWIGLU) ? 2ull * a.n_out : (uint64_t)a.n_out;
   CUtensorMap mw, mx;
   int rc = encode_map_2d_bf16(&mw, a.W, (uint64_t)a.k, w_rows, (uint64_t)a.k * 2, kGemmTileK, 64);
   if (rc != DF_OK) return rc;
   rc = encode_map_2d_bf16(&mx, a.x, (uint64_t)a.k, (uint64_t)m, (uint64_t)a.k * 2, kGemmTileK, (uint32_t)p.n_pad);
   if (rc != DF_OK) return rc;
+  // pipeline stages; after the main loop the same bytes hold the partial tile (512 B per row) and
+  // the reduced slice (512 / S B per row): 65536 + 512 n_pad >= 768 n_pad for n_pad <= 256
   const size_t smem = 1024 + (size_t)kStages * (kABytes + p.n_pad * 128) + 256;
   switch (a.epi) {
     case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(mw, mx, p, smem, s);

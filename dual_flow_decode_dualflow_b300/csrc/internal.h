@@ -71,6 +71,11 @@ struct AttnArgs {
   int aux_on;
 };
 
+struct ProfRec {
+  int fam = 0;
+  cudaEvent_t a = nullptr, b = nullptr;
+};
+
 struct GraphEntry {
   std::vector<uint64_t> key;
   cudaGraphExec_t exec = nullptr;
@@ -89,11 +94,6 @@ struct dualflow_ctx {
   int32_t* attn_cnt = nullptr;
   int attn_ctas = 0;               // persistent grid size of the attention kernel
   int attn_slots = 0;
-  // tcgen05 split-K workspace
-  float* gemm_part = nullptr;
-  size_t gemm_part_floats = 0;
-  int32_t* gemm_cnt = nullptr;
-  int gemm_cnt_n = 0;
   // step activations
   float* h = nullptr;              // [2, max_batch, d] fp32 residual
   void* x = nullptr;               // [2 * max_batch, max(d, F)] storage dtype (normed input)
@@ -105,6 +105,11 @@ struct dualflow_ctx {
   float* logits_dev = nullptr;
   int graphs_enabled = 1;
   std::vector<df::GraphEntry> graphs;
+  // per-kernel timing of the step (events reused across steps)
+  int profiling = 0;
+  std::vector<df::ProfRec> prof;
+  int prof_n = 0;
+  int step_launches[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 };
 
 namespace df {

@@ -15,20 +15,6 @@ namespace {
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
 
-template <typename T>
-__device__ __forceinline__ float ldv(const T* p, size_t i);
-template <>
-__device__ __forceinline__ float ldv<float>(const float* p, size_t i) { return p[i]; }
-template <>
-__device__ __forceinline__ float ldv<__nv_bfloat16>(const __nv_bfloat16* p, size_t i) { return __bfloat162float(p[i]); }
-
-template <typename T>
-__device__ __forceinline__ void stv(T* p, size_t i, float v);
-template <>
-__device__ __forceinline__ void stv<float>(float* p, size_t i, float v) { p[i] = v; }
-template <>
-__device__ __forceinline__ void stv<__nv_bfloat16>(__nv_bfloat16* p, size_t i, float v) { p[i] = __float2bfloat16_rn(v); }
-
 // Sum over the block (blockDim.x a multiple of 32, <= 1024).
 __device__ float block_sum(float v, float* red) {
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -52,40 +38,57 @@ __device__ float block_max(float v, float* red) {
   return s;
 }
 
-// Row n = f * B + b: h_n = E_f[token_b] (fp32) and x_n = RMSNorm(h_n) * g in the storage dtype.
-template <typename T>
-__global__ void embed_rmsnorm_kernel(const T* E1, const T* E2, const int32_t* tokens, const T* g, float* h, T* x,
-                                     int B, int d, int V, float eps, int32_t* status) {
-  __shared__ float red[32];
-  const int n = blockIdx.x, f = n / B, b = n % B;
-  int tok = tokens[b];
-  if (tok < 0 || tok >= V) {
-    if (threadIdx.x == 0) set_status(status, DF_ERR_DEVICE_BOUNDS);
-    tok = 0;
-  }
-  const T* E = f ? E2 : E1;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = ldv(E, (size_t)tok * d + i);
-    h[(size_t)n * d + i] = v;
-    ss += v * v;
-  }
-  const float r = 1.0f / sqrtf(block_sum(ss, red) / (float)d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x)
-    stv(x, (size_t)n * d + i, h[(size_t)n * d + i] * r * ldv(g, i));
+// Four consecutive storage-dtype elements <-> float4.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
 }
 
+// One warp per row n = f * B + b. With E1/E2 given, the row is first gathered from the flow's
+// embedding (h_n = E_f[token_b], written to the fp32 residual); then x_n = h_n / rms(h_n) * g in
+// the storage dtype. d must be a multiple of 4.
 template <typename T>
-__global__ void rmsnorm_kernel(const float* h, const T* g, T* x, int d, float eps) {
-  __shared__ float red[32];
-  const int n = blockIdx.x;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    const float v = h[(size_t)n * d + i];
-    ss += v * v;
+__global__ void rmsnorm_rows_kernel(float* h, const T* E1, const T* E2, const int32_t* tokens, const T* g, T* x,
+                                    int rows, int B, int d, int V, float eps, int32_t* status) {
+  const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (n >= rows) return;
+  const T* src = nullptr;
+  if (E1 != nullptr) {
+    int tok = tokens[n % B];
+    if (tok < 0 || tok >= V) {
+      if (lane == 0) set_status(status, DF_ERR_DEVICE_BOUNDS);
+      tok = 0;
+    }
+    src = (n / B ? E2 : E1) + (size_t)tok * d;
   }
-  const float r = 1.0f / sqrtf(block_sum(ss, red) / (float)d + eps);
-  for (int i = threadIdx.x; i < d; i += blockDim.x) stv(x, (size_t)n * d + i, h[(size_t)n * d + i] * r * ldv(g, i));
+  float* hr = h + (size_t)n * d;
+  float ss = 0.f;
+#pragma unroll 4
+  for (int q = lane * 4; q < d; q += 128) {
+    const float4 v = src ? ld4(src + q) : ld4(hr + q);
+    if (src) st4(hr + q, v);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  const float r = 1.0f / sqrtf(ss / (float)d + eps);
+  T* xr = x + (size_t)n * d;
+#pragma unroll 4
+  for (int q = lane * 4; q < d; q += 128) {
+    const float4 v = src ? ld4(src + q) : ld4(hr + q);
+    const float4 gg = ld4(g + q);
+    st4(xr + q, make_float4(v.x * r * gg.x, v.y * r * gg.y, v.z * r * gg.z, v.w * r * gg.w));
+  }
 }
 
 // Attention-only call without the auxiliary flow: q[0, b, h] = RoPE(q1[b, h]) at position seq_len[b].
@@ -307,25 +310,30 @@ int launch_embed_rmsnorm(dualflow_ctx* ctx, const void* E1, const void* E2, cons
                          int batch, int aux_on, cudaStream_t s) {
   const dualflow_config& c = ctx->cfg;
   const int rows = aux_on ? 2 * batch : batch;
+  const int blocks = (rows + 3) / 4;
   if (c.dtype == DF_DTYPE_BF16)
-    embed_rmsnorm_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(
-        (const __nv_bfloat16*)E1, (const __nv_bfloat16*)E2, tokens, (const __nv_bfloat16*)g, ctx->h,
-        (__nv_bfloat16*)ctx->x, batch, c.d_model, c.vocab, c.rms_eps, ctx->status);
+    rmsnorm_rows_kernel<__nv_bfloat16><<<blocks, 128, 0, s>>>(
+        ctx->h, (const __nv_bfloat16*)E1, (const __nv_bfloat16*)E2, tokens, (const __nv_bfloat16*)g,
+        (__nv_bfloat16*)ctx->x, rows, batch, c.d_model, c.vocab, c.rms_eps, ctx->status);
   else
-    embed_rmsnorm_kernel<float><<<rows, 256, 0, s>>>((const float*)E1, (const float*)E2, tokens, (const float*)g,
-                                                     ctx->h, (float*)ctx->x, batch, c.d_model, c.vocab, c.rms_eps,
-                                                     ctx->status);
+    rmsnorm_rows_kernel<float><<<blocks, 128, 0, s>>>(ctx->h, (const float*)E1, (const float*)E2, tokens,
+                                                      (const float*)g, (float*)ctx->x, rows, batch, c.d_model,
+                                                      c.vocab, c.rms_eps, ctx->status);
   return ok_launch();
 }
 
 int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s) {
   const dualflow_config& c = ctx->cfg;
   const int rows = aux_on ? 2 * batch : batch;
+  const int blocks = (rows + 3) / 4;
   if (c.dtype == DF_DTYPE_BF16)
-    rmsnorm_kernel<__nv_bfloat16><<<rows, 256, 0, s>>>(h, (const __nv_bfloat16*)g, (__nv_bfloat16*)x, c.d_model,
-                                                       c.rms_eps);
+    rmsnorm_rows_kernel<__nv_bfloat16><<<blocks, 128, 0, s>>>(const_cast<float*>(h), nullptr, nullptr, nullptr,
+                                                              (const __nv_bfloat16*)g, (__nv_bfloat16*)x, rows, batch,
+                                                              c.d_model, 0, c.rms_eps, ctx->status);
   else
-    rmsnorm_kernel<float><<<rows, 256, 0, s>>>(h, (const float*)g, (float*)x, c.d_model, c.rms_eps);
+    rmsnorm_rows_kernel<float><<<blocks, 128, 0, s>>>(const_cast<float*>(h), nullptr, nullptr, nullptr,
+                                                      (const float*)g, (float*)x, rows, batch, c.d_model, 0,
+                                                      c.rms_eps, ctx->status);
   return ok_launch();
 }
 

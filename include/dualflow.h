@@ -202,6 +202,29 @@ DF_API int dualflow_step_host(dualflow_ctx* ctx, const dualflow_weights* w, cons
 /* Enables (1, default) or disables (0) CUDA-graph capture and replay in dualflow_step. */
 DF_API int dualflow_set_graphs(dualflow_ctx* ctx, int32_t enabled);
 
+/* Kernel families reported by dualflow_profile_read. */
+enum {
+  DF_PROF_NORM = 0,      /* embedding gather and RMSNorm */
+  DF_PROF_QKV = 1,       /* QKV projection with query coupling, RoPE and KV append */
+  DF_PROF_ATTN = 2,      /* shared-KV decode attention */
+  DF_PROF_OPROJ = 3,     /* O projection and residual */
+  DF_PROF_GATEUP = 4,    /* gate/up projection with SwiGLU and b coupling */
+  DF_PROF_DOWN = 5,      /* down projection with c coupling and residual */
+  DF_PROF_LMHEAD = 6,    /* shared LM head */
+  DF_PROF_OTHER = 7,     /* fp32-path helpers */
+  DF_PROF_FAMILIES = 8
+};
+
+/* Enables (1) or disables (0, default) per-kernel timing in dualflow_step: every kernel the step
+ * launches is bracketed by a CUDA event pair on the launching stream (captured into the step's
+ * CUDA graph when graphs are on). Toggling drops the cached graphs. */
+DF_API int dualflow_set_profiling(dualflow_ctx* ctx, int32_t enabled);
+
+/* Synchronizes the device and reports the last dualflow_step: launches[f] = kernels of family f
+ * it launched (always available) and ms[f] = their summed device time (0 unless profiling was on).
+ * Either array may be NULL; n_families entries are written (at most DF_PROF_FAMILIES). */
+DF_API int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches, int32_t n_families);
+
 /* Synchronizes `stream`, then returns and clears the device status word: DF_OK, or the first
  * DF_ERR_DEVICE_BOUNDS / DF_ERR_TIMEOUT latched by a kernel since the last call. */
 DF_API int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream);
