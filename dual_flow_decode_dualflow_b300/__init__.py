@@ -22,7 +22,8 @@ DF_EPI_STORE_F32, DF_EPI_STORE_BF16, DF_EPI_ADD_F32, DF_EPI_COUPLE_ADD = 0, 1, 2
 
 C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dualflow_decode_attention",
                "dualflow_stacked_linear", "dualflow_coupled_mlp", "dualflow_step", "dualflow_step_host",
-               "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status")
+               "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
+               "dualflow_decode_attention_noalloc")
 DF_PROF_FAMILIES = 8
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
@@ -80,6 +81,8 @@ def load_library(path: str = LIB_PATH):
         "dualflow_set_profiling": ([vp, i32], i32),
         "dualflow_profile_read": ([vp, POINTER(c_float), POINTER(i32), i32], i32),
         "dualflow_sync_status": ([vp, vp], i32),
+        "dualflow_decode_attention_noalloc": ([POINTER(dualflow_config), vp, POINTER(dualflow_kv), i32, i32, vp, i32,
+                                               vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -185,6 +188,15 @@ def dualflow_profile_read(ctx) -> tuple[list[float], list[int]]:
     n = (c_int32 * DF_PROF_FAMILIES)()
     _check("dualflow_profile_read", load_library().dualflow_profile_read(ctx, ms, n, DF_PROF_FAMILIES))
     return list(ms), list(n)
+
+
+def dualflow_decode_attention_noalloc(cfg: dualflow_config, q, kv: "dualflow_kv", layer: int, batch: int, o,
+                                      aux_on: int, status=None, stream=None) -> None:
+    """Decode attention without a context and without any device allocation (the library keeps
+    the kernel's scratch in a static device array). q: both flows' coupled, rotated queries."""
+    rc = load_library().dualflow_decode_attention_noalloc(ctypes.byref(cfg), _ptr(q), ctypes.byref(kv), layer, batch,
+                                                          _ptr(o), aux_on, _ptr(status), _stream(stream))
+    _check("dualflow_decode_attention_noalloc", rc)
 
 
 def dualflow_sync_status(ctx, stream=None) -> int:

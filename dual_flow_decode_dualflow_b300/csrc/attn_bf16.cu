@@ -480,3 +480,46 @@ int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s) 
 }
 
 }  // namespace df
+
+namespace df {
+
+int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, float* part, int32_t* cnt,
+                             int32_t* status, int ctas, cudaStream_t s) {
+  if (a.batch <= 0) return DF_OK;
+  if (ctas <= 0 || !part || !cnt || !status) return DF_ERR_ARG;
+  CUtensorMap mk, mv;
+  int rc;
+  if (!a.paged) {
+    const uint64_t rows = (uint64_t)cfg.max_batch * cfg.n_kv_heads;
+    const uint64_t seq_stride = (uint64_t)cfg.max_ctx * kHeadDim * 2;
+    rc = encode_map_3d_bf16(&mk, a.k_cache, kHeadDim, (uint64_t)cfg.max_ctx, rows, kHeadDim * 2, seq_stride, 64,
+                            kAttnTileKeys, 1);
+    if (rc == DF_OK)
+      rc = encode_map_3d_bf16(&mv, a.v_cache, kHeadDim, (uint64_t)cfg.max_ctx, rows, kHeadDim * 2, seq_stride, 64,
+                              kAttnTileKeys, 1);
+  } else {
+    const uint64_t rows = (uint64_t)cfg.max_pages * cfg.n_kv_heads;
+    const uint64_t page_stride = (uint64_t)cfg.page_size * kHeadDim * 2;
+    rc = encode_map_3d_bf16(&mk, a.k_cache, kHeadDim, (uint64_t)cfg.page_size, rows, kHeadDim * 2, page_stride, 64,
+                            (uint32_t)cfg.page_size, 1);
+    if (rc == DF_OK)
+      rc = encode_map_3d_bf16(&mv, a.v_cache, kHeadDim, (uint64_t)cfg.page_size, rows, kHeadDim * 2, page_stride, 64,
+                              (uint32_t)cfg.page_size, 1);
+  }
+  if (rc != DF_OK) return rc;
+  AttnParams p;
+  p.a = a;
+  p.part = part;
+  p.cnt = cnt;
+  p.status = status;
+  p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+  const size_t smem = 1024 + (size_t)kStagesA * kStageBytes + 2 * kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
+                      (size_t)(a.batch + 1) * 4;
+  if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+      cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return DF_ERR_CUDA;
+  attn_bf16_kernel<<<ctas, kAttnThreads, smem, s>>>(mk, mv, p);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+}  // namespace df

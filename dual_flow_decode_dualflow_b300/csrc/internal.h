@@ -124,6 +124,11 @@ int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s);
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi);
 int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s);
+// The same kernel with caller-chosen workspace: split partials (>= pairs + ctas slots of
+// kAttnPartFloats), per-pair merge counters (zero on entry), the status word, and a grid of `ctas`
+// CTAs; cache geometry is taken from `cfg`. Used by the allocation-free entry point.
+int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, float* part, int32_t* cnt,
+                             int32_t* status, int ctas, cudaStream_t s);
 
 int launch_embed_rmsnorm(dualflow_ctx* ctx, const void* E1, const void* E2, const int32_t* tokens, const void* g,
                          int batch, int aux_on, cudaStream_t s);

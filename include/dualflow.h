@@ -229,6 +229,39 @@ DF_API int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches
  * DF_ERR_DEVICE_BOUNDS / DF_ERR_TIMEOUT latched by a kernel since the last call. */
 DF_API int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream);
 
+/* Largest batch * n_kv_heads that dualflow_decode_attention_noalloc accepts. */
+#define DF_NOALLOC_MAX_PAIRS 512
+
+/* Shared-KV decode attention (the attention kernel of dualflow_decode_attention) that allocates
+ * nothing. The pages describe no such call: it exists for callers that may not call cudaMalloc --
+ * an application whose own pool owns all device memory, a plugin restricted to the buffers it is
+ * handed, or a latency-critical program that cannot accept cudaMalloc's implicit device-wide
+ * synchronisation -- and so cannot create a context (dualflow_init allocates its workspace).
+ *
+ * It takes no context. The attention's scratch (split-KV partials, merge counters, a status word;
+ * about 3.4 MB) lives in one statically sized device array of the library, which every device
+ * that loads the library holds until the process exits. Limits: batch * cfg->n_kv_heads <=
+ * DF_NOALLOC_MAX_PAIRS, else DF_ERR_SHAPE before any launch; bf16 storage only, with the same
+ * head_dim / group / page-size limits as dualflow_init (DF_ERR_UNSUPPORTED otherwise).
+ *   cfg     host; n_q_heads, n_kv_heads, head_dim, dtype, paged, page_size, max_batch, max_ctx,
+ *           max_pages describe the cache layout exactly as for dualflow_init (other fields unused)
+ *   q       device bf16 [2, batch, Hq, D]: both flows' queries, already coupled and rotated (the
+ *           queries dualflow_decode_attention forms internally); flow 1 rows read only if aux_on
+ *   kv      host struct of device pointers, as for dualflow_decode_attention; layer selects k/v
+ *   o       device bf16 [2, batch, Hq, D]: o_f = softmax(q_f K1^T / sqrt(D)) V1 over the cached
+ *           positions 0..seq_len[b]-1; seq_len[b] == 0 gives o = 0; flow 1 written only if aux_on
+ *   status  device int32 or NULL: a device-side bounds error (out-of-range page id or length) is
+ *           latched there (set only if it holds 0; the caller clears it). With NULL the code is
+ *           latched in the library's array, where the caller cannot read it.
+ * The first call on a device (with that device current) looks up the array's device address;
+ * make that first call before any stream capture. Every call clears the merge counters it uses
+ * with cudaMemsetAsync on `stream`, then launches one kernel there. All calls on a device share
+ * the one array, so calls that may overlap on the GPU (other streams, other host threads) race on
+ * it and must be serialised by the caller. */
+DF_API int dualflow_decode_attention_noalloc(const dualflow_config* cfg, const void* q, const dualflow_kv* kv,
+                                             int32_t layer, int32_t batch, void* o, int32_t aux_on,
+                                             int32_t* status, dualflow_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
