@@ -155,16 +155,21 @@ int check_kv(const dualflow_ctx* ctx, const dualflow_kv* kv, int layer) {
   return DF_OK;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every weight pointer must be non-null and 16-byte aligned (TMA and vector loads).
 int check_weights(const dualflow_ctx* ctx, const dualflow_weights* w) {
   const dualflow_config& c = ctx->cfg;
   if (!w || w->n_layers != c.n_layers) return DF_ERR_ARG;
-  if (!w->E1 || !w->E2 || !w->W_lm || !w->g_final) return DF_ERR_ARG;
+  auto ok = [](const void* p) { return p != nullptr && aligned16(p); };
+  if (!ok(w->E1) || !ok(w->E2) || !ok(w->W_lm) || !ok(w->g_final)) return DF_ERR_ARG;
   if (!w->g_attn || !w->g_mlp || !w->Wqkv || !w->Wo || !w->a || !w->b || !w->c) return DF_ERR_ARG;
   if (c.n_experts == 0 && (!w->Wgu || !w->Wd)) return DF_ERR_ARG;
   for (int l = 0; l < c.n_layers; ++l) {
-    if (!w->g_attn[l] || !w->g_mlp[l] || !w->Wqkv[l] || !w->Wo[l] || !w->a[l] || !w->b[l] || !w->c[l])
+    if (!ok(w->g_attn[l]) || !ok(w->g_mlp[l]) || !ok(w->Wqkv[l]) || !ok(w->Wo[l]) || !ok(w->a[l]) || !ok(w->b[l]) ||
+        !ok(w->c[l]))
       return DF_ERR_ARG;
-    if (c.n_experts == 0 && (!w->Wgu[l] || !w->Wd[l])) return DF_ERR_ARG;
+    if (c.n_experts == 0 && (!ok(w->Wgu[l]) || !ok(w->Wd[l]))) return DF_ERR_ARG;
   }
   return DF_OK;
 }
@@ -202,9 +207,15 @@ int run_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int b
   const dualflow_config& c = ctx->cfg;
   const int mp = batch, ma = aux_on ? batch : 0;
   Launcher L{ctx, s};
-  DF_TRY(L(DF_PROF_NORM, [&] { return launch_rmsnorm(ctx, h, w->g_mlp[l], ctx->x, batch, aux_on, s); }));
   if (c.dtype == DF_DTYPE_BF16) {
+    // x = bf16(h (*) g_mlp) with per-row sums of squares; gate/up scales its rows by 1 / rms
+    DF_TRY(L(DF_PROF_NORM, [&] { return launch_norm_prep(ctx, h, w->g_mlp[l], batch, aux_on, s); }));
     GemmArgs g = gemm_args(ctx);
+    g.ss_in = ctx->ss;
+    g.ss_parts = 1;
+    g.ss_ld = ctx->ss_ld;
+    g.inv_d = 1.0f / (float)c.d_model;
+    g.eps = c.rms_eps;
     g.x = ctx->x;
     g.W = w->Wgu[l];
     g.n_out = c.ffn_hidden;
@@ -230,6 +241,7 @@ int run_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int b
     return L(DF_PROF_DOWN, [&] { return launch_gemm_tc(ctx, d, s); });
   }
   const int M = mp + ma, F = c.ffn_hidden;
+  DF_TRY(L(DF_PROF_NORM, [&] { return launch_rmsnorm(ctx, h, w->g_mlp[l], ctx->x, batch, aux_on, s); }));
   DF_TRY(L(DF_PROF_GATEUP, [&] {
     return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wgu[l], 2 * F, c.d_model, ctx->raw, 0, s);
   }));
@@ -244,13 +256,125 @@ int run_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int b
 }
 
 // ------------------------------------------------------------------ the whole step
+// bf16: five kernels per layer. RMSNorm is carried between kernels (see gemm_tc.cu): the residual
+// epilogues (O projection, down projection) and the embedding kernel write x = bf16(h (*) g) and
+// per-tile row sums of h^2; the next projection scales its rows by 1 / rms. Every kernel after the
+// first is launched with programmatic dependent launch, so it becomes resident and starts
+// streaming its weights while its predecessor drains.
+int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
+                  int batch, float* logits, int aux_on, cudaStream_t s) {
+  const dualflow_config& c = ctx->cfg;
+  const int mp = batch, ma = aux_on ? batch : 0;
+  const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
+  const int d_tiles = (c.d_model + kGemmTileN - 1) / kGemmTileN;
+  const int ss_ld = ctx->ss_ld;
+  // row sums of squares left by the O projection and by the down projection: one per CTA
+  const int o_parts = d_tiles * gemm_splits(ctx, c.d_model, qd, EPI_ADD_F32);
+  const int d_parts = d_tiles * gemm_splits(ctx, c.d_model, c.ffn_hidden, EPI_COUPLE_ADD);
+  Launcher L{ctx, s};
+  DF_TRY(L(DF_PROF_NORM, [&] {
+    return launch_embed_prep(ctx, w->E1, w->E2, tokens, c.n_layers > 0 ? w->g_attn[0] : w->g_final, batch, aux_on,
+                             s);
+  }));
+  // programmatic dependent launch on explicit streams (the legacy default stream keeps plain order)
+  const int pdl = s != nullptr ? 1 : 0;
+  int ss_parts = 1;  // partial sums of squares behind the rows currently in ctx->x
+  auto normed_input = [&](GemmArgs& g) {
+    g.ss_in = ctx->ss;
+    g.ss_parts = ss_parts;
+    g.ss_ld = ss_ld;
+    g.inv_d = 1.0f / (float)c.d_model;
+    g.eps = c.rms_eps;
+    g.pdl = pdl;
+  };
+  auto norm_output = [&](GemmArgs& g, const void* g_next) {
+    g.g_next = g_next;
+    g.x_next = ctx->x;
+    g.ss_out = ctx->ss;
+    g.ss_ld = ss_ld;
+    g.pdl = pdl;
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
+    GemmArgs g = gemm_args(ctx);
+    g.x = ctx->x;
+    g.W = w->Wqkv[l];
+    g.n_out = qkv_n;
+    g.k = c.d_model;
+    g.m_p = mp;
+    g.m_a = ma;
+    g.epi = EPI_QKV;
+    g.vec = w->a[l];
+    g.q_out = ctx->q;
+    g.seq_len = kv->seq_len;
+    g.k_cache = kv->k[l];
+    g.v_cache = kv->v[l];
+    g.page_table = kv->page_table;
+    normed_input(g);
+    DF_TRY(L(DF_PROF_QKV, [&] { return launch_gemm_tc(ctx, g, s); }));
+    const AttnArgs at = attn_args(ctx, kv, l, batch, 1, aux_on);
+    DF_TRY(L(DF_PROF_ATTN, [&] { return launch_attention_bf16(ctx, at, s, pdl); }));
+    GemmArgs o = gemm_args(ctx);
+    o.x = ctx->o;
+    o.W = w->Wo[l];
+    o.n_out = c.d_model;
+    o.k = qd;
+    o.m_p = mp;
+    o.m_a = ma;
+    o.epi = EPI_ADD_F32;
+    o.y = ctx->h;
+    o.ldy = c.d_model;
+    norm_output(o, w->g_mlp[l]);
+    DF_TRY(L(DF_PROF_OPROJ, [&] { return launch_gemm_tc(ctx, o, s); }));
+    ss_parts = o_parts;
+    GemmArgs gu = gemm_args(ctx);
+    gu.x = ctx->x;
+    gu.W = w->Wgu[l];
+    gu.n_out = c.ffn_hidden;
+    gu.k = c.d_model;
+    gu.m_p = mp;
+    gu.m_a = ma;
+    gu.epi = EPI_SWIGLU;
+    gu.y = ctx->u;
+    gu.ldy = c.ffn_hidden;
+    gu.vec = w->b[l];
+    normed_input(gu);
+    DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_gemm_tc(ctx, gu, s); }));
+    GemmArgs dn = gemm_args(ctx);
+    dn.x = ctx->u;
+    dn.W = w->Wd[l];
+    dn.n_out = c.d_model;
+    dn.k = c.ffn_hidden;
+    dn.m_p = mp;
+    dn.m_a = ma;
+    dn.epi = EPI_COUPLE_ADD;
+    dn.y = ctx->h;
+    dn.ldy = c.d_model;
+    dn.vec = w->c[l];
+    norm_output(dn, l + 1 < c.n_layers ? w->g_attn[l + 1] : w->g_final);
+    DF_TRY(L(DF_PROF_DOWN, [&] { return launch_gemm_tc(ctx, dn, s); }));
+    ss_parts = d_parts;
+  }
+  GemmArgs g = gemm_args(ctx);
+  g.x = ctx->x;
+  g.W = w->W_lm;
+  g.n_out = c.vocab;
+  g.k = c.d_model;
+  g.m_p = mp;
+  g.m_a = ma;
+  g.epi = EPI_STORE_F32;
+  g.y = logits;
+  g.ldy = c.vocab;
+  normed_input(g);
+  return L(DF_PROF_LMHEAD, [&] { return launch_gemm_tc(ctx, g, s); });
+}
+
 int run_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens, int batch,
              float* logits, int aux_on, cudaStream_t s) {
   const dualflow_config& c = ctx->cfg;
-  const int mp = batch, ma = aux_on ? batch : 0, M = mp + ma;
-  const bool bf16 = c.dtype == DF_DTYPE_BF16;
-  const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
   reset_counts(ctx);
+  if (c.dtype == DF_DTYPE_BF16) return run_step_bf16(ctx, w, kv, tokens, batch, logits, aux_on, s);
+  const int mp = batch, ma = aux_on ? batch : 0, M = mp + ma;
+  const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
   Launcher L{ctx, s};
   DF_TRY(L(DF_PROF_NORM, [&] {
     return launch_embed_rmsnorm(ctx, w->E1, w->E2, tokens, c.n_layers > 0 ? w->g_attn[0] : w->g_final, batch,
@@ -259,68 +383,24 @@ int run_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv
   for (int l = 0; l < c.n_layers; ++l) {
     if (l > 0)
       DF_TRY(L(DF_PROF_NORM, [&] { return launch_rmsnorm(ctx, ctx->h, w->g_attn[l], ctx->x, batch, aux_on, s); }));
-    if (bf16) {
-      GemmArgs g = gemm_args(ctx);
-      g.x = ctx->x;
-      g.W = w->Wqkv[l];
-      g.n_out = qkv_n;
-      g.k = c.d_model;
-      g.m_p = mp;
-      g.m_a = ma;
-      g.epi = EPI_QKV;
-      g.vec = w->a[l];
-      g.q_out = ctx->q;
-      g.seq_len = kv->seq_len;
-      g.k_cache = kv->k[l];
-      g.v_cache = kv->v[l];
-      g.page_table = kv->page_table;
-      DF_TRY(L(DF_PROF_QKV, [&] { return launch_gemm_tc(ctx, g, s); }));
-      const AttnArgs at = attn_args(ctx, kv, l, batch, 1, aux_on);
-      DF_TRY(L(DF_PROF_ATTN, [&] { return launch_attention_bf16(ctx, at, s); }));
-      GemmArgs o = gemm_args(ctx);
-      o.x = ctx->o;
-      o.W = w->Wo[l];
-      o.n_out = c.d_model;
-      o.k = qd;
-      o.m_p = mp;
-      o.m_a = ma;
-      o.epi = EPI_ADD_F32;
-      o.y = ctx->h;
-      o.ldy = c.d_model;
-      DF_TRY(L(DF_PROF_OPROJ, [&] { return launch_gemm_tc(ctx, o, s); }));
-    } else {
-      DF_TRY(L(DF_PROF_QKV, [&] {
-        return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wqkv[l], qkv_n, c.d_model, ctx->raw,
-                                 0, s);
-      }));
-      DF_TRY(L(DF_PROF_OTHER, [&] {
-        return launch_qkv_post_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->a[l], kv->k[l], kv->v[l],
-                                   kv->page_table, kv->seq_len, (float*)ctx->q, s);
-      }));
-      DF_TRY(L(DF_PROF_ATTN, [&] {
-        return launch_attention_f32(ctx, (const float*)ctx->q, (float*)ctx->o, kv->k[l], kv->v[l], kv->page_table,
-                                    kv->seq_len, batch, 1, aux_on, s);
-      }));
-      DF_TRY(L(DF_PROF_OPROJ, [&] {
-        return launch_linear_f32(ctx, (const float*)ctx->o, M, (const float*)w->Wo[l], c.d_model, qd, ctx->h, 1, s);
-      }));
-    }
+    DF_TRY(L(DF_PROF_QKV, [&] {
+      return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->Wqkv[l], qkv_n, c.d_model, ctx->raw,
+                               0, s);
+    }));
+    DF_TRY(L(DF_PROF_OTHER, [&] {
+      return launch_qkv_post_f32(ctx, ctx->raw, batch, aux_on, (const float*)w->a[l], kv->k[l], kv->v[l],
+                                 kv->page_table, kv->seq_len, (float*)ctx->q, s);
+    }));
+    DF_TRY(L(DF_PROF_ATTN, [&] {
+      return launch_attention_f32(ctx, (const float*)ctx->q, (float*)ctx->o, kv->k[l], kv->v[l], kv->page_table,
+                                  kv->seq_len, batch, 1, aux_on, s);
+    }));
+    DF_TRY(L(DF_PROF_OPROJ, [&] {
+      return launch_linear_f32(ctx, (const float*)ctx->o, M, (const float*)w->Wo[l], c.d_model, qd, ctx->h, 1, s);
+    }));
     DF_TRY(run_mlp(ctx, ctx->h, w, l, batch, aux_on, s));
   }
   DF_TRY(L(DF_PROF_NORM, [&] { return launch_rmsnorm(ctx, ctx->h, w->g_final, ctx->x, batch, aux_on, s); }));
-  if (bf16) {
-    GemmArgs g = gemm_args(ctx);
-    g.x = ctx->x;
-    g.W = w->W_lm;
-    g.n_out = c.vocab;
-    g.k = c.d_model;
-    g.m_p = mp;
-    g.m_a = ma;
-    g.epi = EPI_STORE_F32;
-    g.y = logits;
-    g.ldy = c.vocab;
-    return L(DF_PROF_LMHEAD, [&] { return launch_gemm_tc(ctx, g, s); });
-  }
   return L(DF_PROF_LMHEAD, [&] {
     return launch_linear_f32(ctx, (const float*)ctx->x, M, (const float*)w->W_lm, c.vocab, c.d_model, logits, 0, s);
   });
@@ -422,6 +502,8 @@ int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
   if (dalloc(&ctx->u, (size_t)MB * std::max(c.ffn_hidden, 1) * es) != DF_OK) return fail(DF_ERR_OOM);
   if (c.dtype == DF_DTYPE_F32 && dalloc(&ctx->raw, (size_t)MB * raw_n * sizeof(float)) != DF_OK)
     return fail(DF_ERR_OOM);
+  ctx->ss_ld = 8 * ((c.d_model + kGemmTileN - 1) / kGemmTileN);
+  if (dalloc(&ctx->ss, (size_t)ctx->ss_ld * MB * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
   if (dalloc(&ctx->tokens_dev, (size_t)c.max_batch * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
   if (dalloc(&ctx->logits_dev, (size_t)MB * std::max(c.vocab, 1) * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(DF_ERR_CUDA);
@@ -438,7 +520,7 @@ int dualflow_free(dualflow_ctx* ctx) {
     if (r.b) cudaEventDestroy(r.b);
   }
   void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
-                  ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev};
+                  ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete ctx;
@@ -451,6 +533,7 @@ int dualflow_decode_attention(dualflow_ctx* ctx, const void* q1, const void* h2,
   if (!ctx || !q1 || !o) return DF_ERR_ARG;
   if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
   if (aux_on && (!h2 || !Wq || !a)) return DF_ERR_ARG;
+  if (!aligned16(q1) || (aux_on && (!aligned16(h2) || !aligned16(Wq) || !aligned16(a)))) return DF_ERR_ARG;
   if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
   DF_TRY(check_kv(ctx, kv, layer));
   const dualflow_config& c = ctx->cfg;
@@ -493,6 +576,7 @@ int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_primary,
   if (m_primary < 0 || m_aux < 0 || m_primary + m_aux <= 0 || n <= 0 || k <= 0) return DF_ERR_ARG;
   if (epilogue < DF_EPI_STORE_F32 || epilogue > DF_EPI_COUPLE_ADD) return DF_ERR_ARG;
   if (epilogue == DF_EPI_COUPLE_ADD && (!epi_arg || (m_aux != 0 && m_aux != m_primary))) return DF_ERR_ARG;
+  if (epilogue == DF_EPI_COUPLE_ADD && !aligned16(epi_arg)) return DF_ERR_ARG;
   const dualflow_config& c = ctx->cfg;
   cudaStream_t s = S(stream);
   if (c.dtype == DF_DTYPE_BF16) {
@@ -527,7 +611,7 @@ int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_primary,
 int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int32_t layer, int32_t batch,
                          int32_t aux_on, int32_t* expert_ids_out, dualflow_stream stream) {
   (void)expert_ids_out;
-  if (!ctx || !h || !w) return DF_ERR_ARG;
+  if (!ctx || !h || !w || !aligned16(h)) return DF_ERR_ARG;
   if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
   if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
   if (layer < 0 || layer >= ctx->cfg.n_layers) return DF_ERR_ARG;

@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
   uint64_t* empty = full + kStagesA;
   volatile int* err = reinterpret_cast<volatile int*>(empty + kStagesA);
   int* sched = const_cast<int*>(err) + 4;  // [B + 1] exclusive prefix of tiles
+  int* lens = sched + B + 1;                // [B] attended positions of each sequence
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x;
@@ -112,18 +113,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
     int acc = 0;
     for (int b = 0; b < B; ++b) {
       sched[b] = acc;
+      // seq_len is an input of the call, never written by the preceding kernel: read before the
+      // programmatic wait
       const int L = a.seq_len[b] + a.extra;
       int tb = (L + kAttnTileKeys - 1) / kAttnTileKeys;
       if (L < 0 || L > a.max_ctx) {  // out-of-range length: skip the sequence, report it
         set_status(P.status, DF_ERR_DEVICE_BOUNDS);
         tb = 0;
       }
+      lens[b] = L;
       acc += tb * Hkv;
     }
     sched[B] = acc;
     fence_mbar_init();
   }
   __syncthreads();
+  griddep_launch_dependents();
   const long long T = sched[B];
   // Cut the T tiles over C = min(grid, T) CTAs so that every participating CTA owns at least one
   // tile (the partial-merge counts rely on it); CTAs beyond C only zero empty sequences.
@@ -138,14 +143,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
       const uint64_t pol = policy_evict_first();
       Walker w;
       walker_seek(w, sched, B, Hkv, (int)t0);
+      // Under programmatic dependent launch the first stages' tiles are requested before waiting
+      // for the preceding kernel, unless they hold the slot that kernel appends (seq_len[b] when
+      // extra = 1): the older cache positions are never written by it.
+      bool waited = false;
       for (long long t = t0, i = 0; t < t1; ++t, ++i) {
         const int s = (int)(i % kStagesA);
         const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
+        const int key0 = w.j * kAttnTileKeys;
+        const int Leff = lens[w.b];
+        if (!waited && (i >= kStagesA || (a.extra && key0 + kAttnTileKeys >= Leff))) {
+          griddep_wait();
+          waited = true;
+        }
         if (!wait_or_fail(&empty[s], ph ^ 1u, err, P.status)) break;
         uint8_t* Kst = smem + s * kStageBytes;
         uint8_t* Vst = Kst + kTileBytes;
-        const int key0 = w.j * kAttnTileKeys;
-        const int Leff = a.seq_len[w.b] + a.extra;
         if (!a.paged) {
           const int row = w.b * Hkv + w.g;
           mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
@@ -183,11 +196,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
         }
         walker_next(w, sched, B, Hkv);
       }
+      if (!waited) griddep_wait();
     }
     return;
   }
 
   // ------------------------------ consumers ------------------------------
+  griddep_wait();  // q is written by the preceding kernel; o may still be read by an older one
   // sequences with nothing to attend: o = 0
   for (int b = c; b < B; b += gridDim.x) {
     if (sched[b + 1] != sched[b]) continue;
@@ -215,7 +230,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
   walker_seek(w, sched, B, Hkv, (int)t0);
   bool new_seg = true;
   for (long long t = t0, i = 0; t < t1; ++t, ++i) {
-    const int Leff = a.seq_len[w.b] + a.extra;
+    const int Leff = lens[w.b];
     if (new_seg) {
       // load this group's 2G query rows (primary heads, then auxiliary heads) as B fragments
       const int f = qn / G, hh = qn % G;
@@ -443,7 +458,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
 
 }  // namespace
 
-int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s) {
+int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl) {
   const dualflow_config& cfg = ctx->cfg;
   if (a.batch <= 0) return DF_OK;
   CUtensorMap mk, mv;
@@ -471,12 +486,21 @@ int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s) 
   p.status = ctx->status;
   p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
   const size_t smem = 1024 + (size_t)kStagesA * kStageBytes + 2 * kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
-                      (size_t)(a.batch + 1) * 4;
+                      (size_t)(2 * a.batch + 1) * 4;
   if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return DF_ERR_CUDA;
-  attn_bf16_kernel<<<ctx->attn_ctas, kAttnThreads, smem, s>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(ctx->attn_ctas, 1, 1);
+  lc.blockDim = dim3(kAttnThreads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, attn_bf16_kernel, mk, mv, p) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
 }  // namespace df
@@ -514,7 +538,7 @@ int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, floa
   p.status = status;
   p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
   const size_t smem = 1024 + (size_t)kStagesA * kStageBytes + 2 * kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
-                      (size_t)(a.batch + 1) * 4;
+                      (size_t)(2 * a.batch + 1) * 4;
   if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return DF_ERR_CUDA;

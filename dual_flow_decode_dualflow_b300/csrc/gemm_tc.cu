@@ -6,12 +6,15 @@
 // flows ("Custos de Inferencia vs. Treinamento": grouping keeps the unique weights read unchanged).
 // Weight and activation tiles are staged by TMA (128-byte swizzle) through a 4-stage mbarrier
 // pipeline; one elected thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in TMEM).
+// Under programmatic dependent launch the weight tiles of the first stages are requested before
+// the kernel waits for its predecessor: weights never depend on it, activations do.
+//
 // When the output has too few tiles to fill the GPU the reduction dimension is split across the S
 // CTAs of a thread-block cluster (S <= 8). Each CTA parks its fp32 partial tile in shared memory;
 // after a cluster barrier every CTA sums, over distributed shared memory and in rank order (so the
 // result is deterministic and independent of which flows are present), its own 1/S slice of the
-// tile's features -- feature i and its RoPE / gate-up partner i + 64 travel together -- and runs
-// the epilogue on that slice:
+// tile's features -- feature i and its RoPE / gate-up partner i + 64 travel together, four at a
+// time -- and runs the epilogue on that slice:
 //   EPI_QKV      q1 = Wq.x1, q2 = Wq.x2 + a (*) q1 (before RoPE), RoPE(q1, q2, k1) at position
 //                seq_len[b], q stored bf16, primary k1/v1 appended to the cache at slot seq_len[b]
 //                ("Atencao de KV Compartilhada Assimetrica": the auxiliary flow writes no K/V)
@@ -19,6 +22,11 @@
 //   EPI_SWIGLU   u = silu(gate) (*) up for both flows, then u2 += b (*) u1 ("Acoplamento Leve")
 //   EPI_COUPLE_ADD  y2 += c (*) y1, then h += y (MLP output coupling and residual)
 //   EPI_ADD_F32 / EPI_STORE_F32 / EPI_STORE_BF16  residual update, logits, plain stores
+//
+// RMSNorm across kernels (decode step). RMSNorm(h) . W^T = (1/rms(h)) ((h (*) g) . W^T): a residual
+// epilogue that has just produced h also writes x_next = bf16(h (*) g_next) and, per row, the sum
+// of h^2 over its 128-feature tile; the kernel that consumes x_next multiplies each accumulated
+// row by 1 / sqrt(sum / d + eps). No separate normalisation pass over h is needed.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -28,6 +36,7 @@ namespace {
 constexpr int kStages = 4;
 constexpr int kThreads = 128;
 constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per stage
+constexpr int kSplitMaxRows = 208;                    // padded activation rows a split CTA can hold
 
 struct GemmParams {
   GemmArgs a;
@@ -35,16 +44,65 @@ struct GemmParams {
   int splits;    // CTAs of the cluster sharing one tile's reduction (1, 2, 4 or 8)
   int kb_total;  // k / 64
   int n_tiles;
+  int vec_ok;    // y / u rows allow 16-byte (fp32) or 8-byte (bf16) vector access
+  int region;    // bytes of the data region (pipeline stages, later the partial tiles)
   int32_t* status;
 };
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
 
-__device__ __forceinline__ float bf2f(const void* p, size_t i) {
-  return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
-}
-
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ float4 ld_bf16x4(const void* p, size_t i) {
+  const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void st_bf16x4(void* p, size_t i, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(p) + i) = u;
+}
+// Element-wise helpers with explicit rounding (no contraction across them): a primary row and an
+// auxiliary row with equal inputs get bit-equal results whatever code surrounds them.
+__device__ __forceinline__ float4 f4_add(float4 a, float4 b) {
+  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z), __fadd_rn(a.w, b.w));
+}
+__device__ __forceinline__ float4 f4_mul(float4 a, float4 b) {
+  return make_float4(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y), __fmul_rn(a.z, b.z), __fmul_rn(a.w, b.w));
+}
+__device__ __forceinline__ float4 f4_scale(float4 a, float s) {
+  return make_float4(__fmul_rn(a.x, s), __fmul_rn(a.y, s), __fmul_rn(a.z, s), __fmul_rn(a.w, s));
+}
+__device__ __forceinline__ float4 f4_fma(float4 a, float4 b, float4 c) {  // a * b + c, one rounding
+  return make_float4(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y), __fmaf_rn(a.z, b.z, c.z),
+                     __fmaf_rn(a.w, b.w, c.w));
+}
+// acc + a.x^2 + a.y^2 + a.z^2 + a.w^2, accumulated in that order
+__device__ __forceinline__ float f4_sumsq_acc(float acc, float4 a) {
+  return __fmaf_rn(a.w, a.w, __fmaf_rn(a.z, a.z, __fmaf_rn(a.y, a.y, __fmaf_rn(a.x, a.x, acc))));
+}
+__device__ __forceinline__ float4 f4_silu_mul(float4 g, float4 u) {
+  return make_float4(__fmul_rn(silu(g.x), u.x), __fmul_rn(silu(g.y), u.y), __fmul_rn(silu(g.z), u.z),
+                     __fmul_rn(silu(g.w), u.w));
+}
+__device__ __forceinline__ float f4_get(const float4& v, int j) { return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w; }
+
+// Rotary pair (x at feature i, xp at i + 64) by the angles of features i..i+3 at one position:
+// lo = x cos - xp sin, hi = xp cos + x sin (each with one final rounding of a fused product).
+__device__ __forceinline__ float rot_lo(float x, float xp, float c, float s) { return __fmaf_rn(x, c, -__fmul_rn(xp, s)); }
+__device__ __forceinline__ float rot_hi(float x, float xp, float c, float s) { return __fmaf_rn(xp, c, __fmul_rn(x, s)); }
+__device__ __forceinline__ void rope4(const float2* cs, float4 x, float4 xp, float4& lo, float4& hi) {
+  const float4 c0 = *reinterpret_cast<const float4*>(cs), c1 = *reinterpret_cast<const float4*>(cs + 2);
+  // c0 = (cos0, sin0, cos1, sin1), c1 = (cos2, sin2, cos3, sin3)
+  lo = make_float4(rot_lo(x.x, xp.x, c0.x, c0.y), rot_lo(x.y, xp.y, c0.z, c0.w), rot_lo(x.z, xp.z, c1.x, c1.y),
+                   rot_lo(x.w, xp.w, c1.z, c1.w));
+  hi = make_float4(rot_hi(x.x, xp.x, c0.x, c0.y), rot_hi(x.y, xp.y, c0.z, c0.w), rot_hi(x.z, xp.z, c1.x, c1.y),
+                   rot_hi(x.w, xp.w, c1.z, c1.w));
+}
 
 __device__ __forceinline__ size_t cache_slot(const GemmArgs& a, int b, int hk, int pos, int32_t* status, bool* ok) {
   *ok = true;
@@ -64,6 +122,57 @@ __device__ __forceinline__ size_t cache_slot(const GemmArgs& a, int b, int hk, i
   return (((size_t)pid * a.n_kv_heads + hk) * a.page_size + (pos % a.page_size)) * kHeadDim;
 }
 
+// Where a CTA finds the fp32 partial tiles of its output slice. S == 1: its own accumulator tile
+// acc[n][128]. S > 1: the S partials of its slice received from the cluster's CTAs, recv[r][n][2 nl]
+// (features lo0.. lo0+nl then 64+lo0.. 64+lo0+nl of every row n, from rank r).
+struct RedSrc {
+  const float* base;
+  int S, n_pad, nl;
+};
+
+// Reduced accumulators of activation row n at the slice's quad qd: low features (lo) and their
+// partners 64 apart (hi), summed over the S partials in rank order.
+__device__ __forceinline__ void reduce_pair(const RedSrc& r, int lo0, int n, int qd, float4& lo, float4& hi) {
+  if (r.S == 1) {
+    const float* e = r.base + n * kGemmTileN + lo0 + 4 * qd;
+    lo = *reinterpret_cast<const float4*>(e);
+    hi = *reinterpret_cast<const float4*>(e + 64);
+    return;
+  }
+  const int nfs = 2 * r.nl;
+  const float* e = r.base + n * nfs + 4 * qd;
+  const int rs = r.n_pad * nfs;
+  lo = *reinterpret_cast<const float4*>(e);
+  hi = *reinterpret_cast<const float4*>(e + r.nl);
+  for (int k = 1; k < r.S; ++k) {
+    lo = f4_add(lo, *reinterpret_cast<const float4*>(e + k * rs));
+    hi = f4_add(hi, *reinterpret_cast<const float4*>(e + k * rs + r.nl));
+  }
+}
+
+// Stores four features fg..fg+3 of one output row (vector when the row allows it).
+template <int EPI>
+__device__ __forceinline__ void store4(const GemmArgs& a, int vec_ok, int n, int fg, float4 v) {
+  if (EPI == EPI_STORE_BF16) {
+    if (vec_ok && fg + 3 < a.n_out) {
+      st_bf16x4(a.y, (size_t)n * a.ldy + fg, v);
+    } else {
+      for (int j = 0; j < 4; ++j)
+        if (fg + j < a.n_out)
+          reinterpret_cast<__nv_bfloat16*>(a.y)[(size_t)n * a.ldy + fg + j] = __float2bfloat16_rn(f4_get(v, j));
+    }
+    return;
+  }
+  float* y = reinterpret_cast<float*>(a.y) + (size_t)n * a.ldy + fg;
+  if (vec_ok && fg + 3 < a.n_out) {
+    if (EPI == EPI_ADD_F32) v = f4_add(v, *reinterpret_cast<const float4*>(y));
+    *reinterpret_cast<float4*>(y) = v;
+  } else {
+    for (int j = 0; j < 4; ++j)
+      if (fg + j < a.n_out) y[j] = (EPI == EPI_ADD_F32 ? y[j] : 0.f) + f4_get(v, j);
+  }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
@@ -73,20 +182,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b_bytes = p.n_pad * 128;
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * b_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.region);
   uint64_t* empty = full + kStages;
   uint64_t* done = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  int* flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] error
-  float* acc_s = reinterpret_cast<float*>(smem);       // [n_pad][128], reuses the pipeline after the mainloop
+  uint64_t* recv_bar = done + 1;                             // S > 1: the cluster's partials arrived
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
+  float* rstd_s = reinterpret_cast<float*>(tmem_slot + 4);  // [256] 1 / rms of each activation row
+  // After the main loop the pipeline bytes hold, for S == 1, the accumulator tile acc[n][128];
+  // for S > 1, the staged partial split into S slices [S][n_pad * 2nl + 8] (the 8-float pad
+  // spreads the slices over the shared-memory banks) followed by the receive area [S][n_pad][2nl].
+  float* acc_s = reinterpret_cast<float*>(smem);
 
+  const GemmArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile = blockIdx.x, split = blockIdx.y;
   const int kb0 = (int)((long long)split * p.kb_total / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.kb_total / p.splits);
   const int nkb = kb1 - kb0;
+  const int m = a.m_p + a.m_a;
   uint32_t ncols = 32;
   while ((int)ncols < p.n_pad) ncols <<= 1;
+  const int S = p.splits;
+  const int nl = 64 / S, lo0 = split * nl, nq = nl / 4, nfs = 2 * nl;
+  const int slice_floats = p.n_pad * nfs;          // one rank's partial of one slice
+  const int stage_stride = slice_floats + 8;       // staged slices, bank-spread
+  float* recv_s = acc_s + S * stage_stride;        // [S][n_pad][nfs]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -94,8 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
-    flags[0] = 0;
+    mbar_init(recv_bar, 1);
     fence_mbar_init();
+    // the S slices of this CTA's output arrive by bulk copy from the cluster's CTAs
+    if (S > 1) mbar_arrive_expect_tx(recv_bar, (uint32_t)(S * slice_floats * 4));
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_x);
   }
@@ -106,12 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
 
   int row0, row1;
   if (EPI == EPI_SWIGLU) {
     row0 = 64 * tile;                 // gate rows of hidden units [64 tile, 64 tile + 64)
-    row1 = p.a.n_out + 64 * tile;     // up rows of the same units
+    row1 = a.n_out + 64 * tile;       // up rows of the same units
   } else {
     row0 = kGemmTileN * tile;
     row1 = row0 + 64;
@@ -121,11 +244,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA producer: weights are streamed once (evict-first), activations stay L2-resident.
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
-    for (int i = 0; i < nkb; ++i) {
+    const int npre = nkb < kStages ? nkb : kStages;
+    // weights of the first stages do not depend on the preceding kernel: request them first
+    for (int i = 0; i < npre; ++i) {
+      mbar_arrive_expect_tx(&full[i], (uint32_t)(kABytes + b_bytes));
+      const int kc = (kb0 + i) * kGemmTileK;
+      tma_load_2d_hint(sA + i * kABytes, &map_w, &full[i], kc, row0, pol_w);
+      tma_load_2d_hint(sA + i * kABytes + kABytes / 2, &map_w, &full[i], kc, row1, pol_w);
+    }
+    griddep_wait();
+    for (int i = 0; i < npre; ++i)
+      tma_load_2d_hint(sB + i * b_bytes, &map_x, &full[i], (kb0 + i) * kGemmTileK, 0, pol_x);
+    for (int i = npre; i < nkb; ++i) {
       const int s = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
       if (!mbar_wait(&empty[s], ph ^ 1u)) {
-        flags[0] = 1;
         set_status(p.status, DF_ERR_TIMEOUT);
         break;
       }
@@ -142,7 +275,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
       if (!mbar_wait(&full[s], ph)) {
-        flags[0] = 1;
         set_status(p.status, DF_ERR_TIMEOUT);
         break;
       }
@@ -155,167 +287,260 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&empty[s]);
     }
     umma_commit(done);
+  } else if (warp >= 2 && a.ss_in != nullptr) {
+    // idle during the main loop: 1 / rms of every activation row, from the producer's partials
+    griddep_wait();
+    for (int n = threadIdx.x - 64; n < m; n += 64) {
+      const float* row = a.ss_in + (size_t)n * a.ss_ld;
+      float ss = 0.f;
+      int q = 0;
+      if ((a.ss_ld & 3) == 0)
+        for (; q + 4 <= a.ss_parts; q += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(row + q);
+          ss += v.x;
+          ss += v.y;
+          ss += v.z;
+          ss += v.w;
+        }
+      for (; q < a.ss_parts; ++q) ss += row[q];
+      rstd_s[n] = 1.0f / sqrtf(ss * a.inv_d + a.eps);
+    }
   }
   __syncwarp();
 
-  // ---- accumulator: TMEM -> registers -> this CTA's fp32 partial tile acc_s[n][128] ----
+  // ---- accumulator: TMEM -> registers -> shared memory ----
   const bool acc_ok = mbar_wait(done, 0);
   tc_fence_after();
   if (!acc_ok) set_status(p.status, DF_ERR_TIMEOUT);
+  // this CTA's pipeline buffers are free: the cluster's CTAs may write into them once all arrive
+  if (S > 1) cluster_arrive();
   {
     const int f = threadIdx.x;  // TMEM lane == output feature within the tile
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float* dst;
+    int stride;
+    if (S == 1) {
+      dst = acc_s + f;
+      stride = kGemmTileN;
+    } else {
+      const int hf = f & 63, j = hf / nl;  // slice (destination rank) of feature f
+      dst = acc_s + j * stage_stride + (f >> 6) * nl + hf % nl;
+      stride = nfs;
+    }
     for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
       float v[16];
       tmem_ld16(lane_base + (uint32_t)c0, v);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc_s[(c0 + j) * kGemmTileN + f] = v[j];
+      for (int j = 0; j < 16; ++j) dst[(c0 + j) * stride] = v[j];
     }
   }
+  fence_proxy_async_smem();  // the staged slices are read by the bulk-copy engine
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, ncols);
+  griddep_wait();  // the epilogue reads and writes buffers of the preceding kernels
 
-  // ---- split reduction over distributed shared memory: this CTA owns features
-  //      [lo0, lo0 + nl) and [64 + lo0, 64 + lo0 + nl) of the tile ----
-  const int S = p.splits;
-  const int nl = 64 / S, lo0 = split * nl, nf = 2 * nl;
-  float* red = acc_s + p.n_pad * kGemmTileN;  // [n_pad][nf] (S > 1)
+  // ---- split-K reduction: every CTA pushes slice r of its partial into rank r's receive area
+  //      (one bulk copy each), then sums the S partials of its own slice in rank order, so the
+  //      result is deterministic and independent of which flows are present ----
   if (S > 1) {
-    cluster_sync();
-    const int quads = nf / 4;
-    const uint32_t base = smem_u32(acc_s);
-    for (int it = threadIdx.x; it < p.n_pad * quads; it += kThreads) {
-      const int n = it / quads, qd = it % quads;
-      const int fl = qd * 4;
-      const int f = fl < nl ? lo0 + fl : 64 + lo0 + (fl - nl);
-      const uint32_t off = base + (uint32_t)((n * kGemmTileN + f) * 4);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int r = 0; r < S; ++r) {
-        const float4 v = ld_dsmem_f4(mapa_shared(off, (uint32_t)r));
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-      }
-      *reinterpret_cast<float4*>(red + n * nf + fl) = acc;
+    cluster_wait();  // every CTA of the cluster has drained its pipeline
+    if (threadIdx.x == 0) {
+      const uint32_t src0 = smem_u32(acc_s), dst_local = smem_u32(recv_s + split * slice_floats);
+      const uint32_t bar_local = smem_u32(recv_bar);
+      for (int r = 0; r < S; ++r)
+        bulk_copy_to_cluster(mapa_shared(dst_local, (uint32_t)r), src0 + (uint32_t)(r * stage_stride * 4),
+                             (uint32_t)(slice_floats * 4), mapa_shared(bar_local, (uint32_t)r));
     }
-    __syncthreads();
+    if (!mbar_wait(recv_bar, 0)) set_status(p.status, DF_ERR_TIMEOUT);
+    cluster_arrive();  // this CTA has received everything sent to it (its own copies are done too)
   }
-  // reduced value of activation row n, tile feature f (f in this CTA's slice)
-  auto acc = [&](int n, int f) -> float {
-    if (S == 1) return acc_s[n * kGemmTileN + f];
-    return red[n * nf + (f < 64 ? f - lo0 : nl + f - 64 - lo0)];
-  };
-
-  // ---- epilogues: unit (i, b) covers features i and i + 64 of rows b (and m_p + b) ----
-  const GemmArgs& a = p.a;
-  const int m = a.m_p + a.m_a;
-  if (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || EPI == EPI_ADD_F32) {
-    for (int it = threadIdx.x; it < nl * m; it += kThreads) {
-      const int i = lo0 + it % nl, n = it / nl;
+  RedSrc red;
+  red.base = S == 1 ? acc_s : recv_s;
+  red.S = S;
+  red.n_pad = p.n_pad;
+  red.nl = nl;
+  const bool scaled = a.ss_in != nullptr;
+  const bool norm_out = (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD) && a.g_next != nullptr;
+  // units of work: (activation row, quad); paired epilogues take the primary row and its auxiliary row
+  const bool paired = EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV;
+  const int rows = (EPI == EPI_Q2) ? a.m_a : paired ? a.m_p : m;
+  const int units = rows * nq;
+  for (int base = 0; base < units; base += kThreads) {
+    const int it = base + threadIdx.x;
+    const bool live = it < units;
+    const int n = live ? it / nq : 0, qd = it % nq;
+    const int fa = lo0 + 4 * qd;        // tile feature of the low quad
+    const int fg = tile * kGemmTileN + fa;
+    float ss0 = 0.f, ss1 = 0.f;         // norm outputs: sum of h^2 of row n (and its auxiliary row)
+    if (live) {
+      float4 lo, hi;
+      reduce_pair(red, lo0, n, qd, lo, hi);
+      if (scaled) {
+        const float r = rstd_s[n];
+        lo = f4_scale(lo, r);
+        hi = f4_scale(hi, r);
+      }
+      if (EPI == EPI_STORE_F32 || EPI == EPI_STORE_BF16 || (EPI == EPI_ADD_F32 && !norm_out)) {
+        store4<EPI>(a, p.vec_ok, n, fg, lo);
+        store4<EPI>(a, p.vec_ok, n, fg + 64, hi);
+      } else if (EPI == EPI_ADD_F32) {
+        // residual update, then the next norm's input (n_out is d, a multiple of 64)
+        float* y = reinterpret_cast<float*>(a.y) + (size_t)n * a.ldy;
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int f = i + 64 * hh, fg = tile * kGemmTileN + f;
-        if (fg >= a.n_out) continue;
-        const float v = acc(n, f);
-        if (EPI == EPI_STORE_F32) reinterpret_cast<float*>(a.y)[(size_t)n * a.ldy + fg] = v;
-        if (EPI == EPI_ADD_F32) reinterpret_cast<float*>(a.y)[(size_t)n * a.ldy + fg] += v;
-        if (EPI == EPI_STORE_BF16)
-          reinterpret_cast<__nv_bfloat16*>(a.y)[(size_t)n * a.ldy + fg] = __float2bfloat16_rn(v);
-      }
-    }
-  } else if (EPI == EPI_COUPLE_ADD) {
-    float* y = reinterpret_cast<float*>(a.y);
-    for (int it = threadIdx.x; it < nl * a.m_p; it += kThreads) {
-      const int i = lo0 + it % nl, b = it / nl;
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int f = i + 64 * hh, fg = tile * kGemmTileN + f;
-        if (fg >= a.n_out) continue;
-        const float z1 = acc(b, f);
-        y[(size_t)b * a.ldy + fg] += z1;
-        if (a.m_a > 0) y[(size_t)(a.m_p + b) * a.ldy + fg] += acc(a.m_p + b, f) + bf2f(a.vec, fg) * z1;
-      }
-    }
-  } else if (EPI == EPI_SWIGLU) {
-    __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(a.y);
-    for (int it = threadIdx.x; it < nl * a.m_p; it += kThreads) {
-      const int i = lo0 + it % nl, b = it / nl;
-      const int j = tile * 64 + i;  // hidden unit: gate at tile feature i, up at i + 64
-      const float u1 = silu(acc(b, i)) * acc(b, i + 64);
-      u[(size_t)b * a.ldy + j] = __float2bfloat16_rn(u1);
-      if (a.m_a > 0) {
-        const int r = a.m_p + b;
-        u[(size_t)r * a.ldy + j] = __float2bfloat16_rn(silu(acc(r, i)) * acc(r, i + 64) + bf2f(a.vec, j) * u1);
-      }
-    }
-  } else if (EPI == EPI_QKV) {
-    const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, B = a.m_p;
-    __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(a.q_out);
-    for (int it = threadIdx.x; it < nl * B; it += kThreads) {
-      const int i = lo0 + it % nl, b = it / nl;
-      const int pos = a.seq_len[b];
-      if (pos < 0 || pos > a.max_ctx) {
-        set_status(p.status, DF_ERR_DEVICE_BOUNDS);
-        continue;
-      }
-      const float2 cs = a.rope[(size_t)pos * 64 + i];
-      if (tile < Hq) {
-        const int h = tile;
-        const float x1 = acc(b, i), x1p = acc(b, i + 64);
-        const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
-        qo[o1 + i] = __float2bfloat16_rn(x1 * cs.x - x1p * cs.y);
-        qo[o1 + i + 64] = __float2bfloat16_rn(x1p * cs.x + x1 * cs.y);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int f = fg + 64 * hh;
+          if (f >= a.n_out) continue;
+          const float4 hv = f4_add(*reinterpret_cast<const float4*>(y + f), hh ? hi : lo);
+          *reinterpret_cast<float4*>(y + f) = hv;
+          st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(hv, ld_bf16x4(a.g_next, f)));
+          ss0 = f4_sumsq_acc(ss0, hv);
+        }
+      } else if (EPI == EPI_COUPLE_ADD) {
+        float4 z2lo = make_float4(0.f, 0.f, 0.f, 0.f), z2hi = z2lo;
         if (a.m_a > 0) {
-          const float x2 = acc(B + b, i) + bf2f(a.vec, h * kHeadDim + i) * x1;
-          const float x2p = acc(B + b, i + 64) + bf2f(a.vec, h * kHeadDim + i + 64) * x1p;
+          reduce_pair(red, lo0, a.m_p + n, qd, z2lo, z2hi);
+          if (scaled) {
+            const float r = rstd_s[a.m_p + n];
+            z2lo = f4_scale(z2lo, r);
+            z2hi = f4_scale(z2hi, r);
+          }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int f = fg + 64 * hh;
+          const float4 z1 = hh ? hi : lo;
+          const float4 z2 = hh ? z2hi : z2lo;
+          if (p.vec_ok && f + 3 < a.n_out) {
+            float* y1 = reinterpret_cast<float*>(a.y) + (size_t)n * a.ldy + f;
+            const float4 h1 = f4_add(*reinterpret_cast<const float4*>(y1), z1);
+            *reinterpret_cast<float4*>(y1) = h1;
+            float4 h2 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (a.m_a > 0) {
+              float* y2 = reinterpret_cast<float*>(a.y) + (size_t)(a.m_p + n) * a.ldy + f;
+              h2 = f4_add(*reinterpret_cast<const float4*>(y2), f4_fma(ld_bf16x4(a.vec, f), z1, z2));
+              *reinterpret_cast<float4*>(y2) = h2;
+            }
+            if (norm_out) {
+              const float4 g = ld_bf16x4(a.g_next, f);
+              st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(h1, g));
+              ss0 = f4_sumsq_acc(ss0, h1);
+              if (a.m_a > 0) {
+                st_bf16x4(a.x_next, (size_t)(a.m_p + n) * a.n_out + f, f4_mul(h2, g));
+                ss1 = f4_sumsq_acc(ss1, h2);
+              }
+            }
+          } else {
+            for (int j = 0; j < 4; ++j) {
+              if (f + j >= a.n_out) continue;
+              float* y = reinterpret_cast<float*>(a.y);
+              const float z1j = f4_get(z1, j);
+              y[(size_t)n * a.ldy + f + j] += z1j;
+              if (a.m_a > 0)
+                y[(size_t)(a.m_p + n) * a.ldy + f + j] +=
+                    f4_get(z2, j) + __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.vec)[f + j]) * z1j;
+            }
+          }
+        }
+      } else if (EPI == EPI_SWIGLU) {
+        const int j = tile * 64 + fa;  // hidden unit: gate at tile feature fa, up at fa + 64
+        const float4 u1 = f4_silu_mul(lo, hi);
+        st_bf16x4(a.y, (size_t)n * a.ldy + j, u1);
+        if (a.m_a > 0) {
+          float4 g2, p2;
+          reduce_pair(red, lo0, a.m_p + n, qd, g2, p2);
+          if (scaled) {
+            const float r = rstd_s[a.m_p + n];
+            g2 = f4_scale(g2, r);
+            p2 = f4_scale(p2, r);
+          }
+          st_bf16x4(a.y, (size_t)(a.m_p + n) * a.ldy + j, f4_fma(ld_bf16x4(a.vec, j), u1, f4_silu_mul(g2, p2)));
+        }
+      } else if (EPI == EPI_QKV) {
+        const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, B = a.m_p, b = n;
+        const int pos = a.seq_len[b];
+        if (pos < 0 || pos > a.max_ctx) {
+          set_status(p.status, DF_ERR_DEVICE_BOUNDS);
+        } else {
+          const float2* cs = a.rope + (size_t)pos * 64 + fa;
+          float4 r_lo, r_hi;
+          if (tile < Hq) {
+            const int h = tile;
+            rope4(cs, lo, hi, r_lo, r_hi);
+            const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
+            st_bf16x4(a.q_out, o1 + fa, r_lo);
+            st_bf16x4(a.q_out, o1 + fa + 64, r_hi);
+            if (a.m_a > 0) {
+              float4 x2, x2p;
+              reduce_pair(red, lo0, B + b, qd, x2, x2p);
+              if (scaled) {
+                const float r = rstd_s[B + b];
+                x2 = f4_scale(x2, r);
+                x2p = f4_scale(x2p, r);
+              }
+              x2 = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa), lo, x2);
+              x2p = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa + 64), hi, x2p);
+              rope4(cs, x2, x2p, r_lo, r_hi);
+              const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
+              st_bf16x4(a.q_out, o2 + fa, r_lo);
+              st_bf16x4(a.q_out, o2 + fa + 64, r_hi);
+            }
+          } else {
+            const bool is_k = tile < Hq + Hkv;
+            const int hk = is_k ? tile - Hq : tile - Hq - Hkv;
+            bool ok;
+            const size_t off = cache_slot(a, b, hk, pos, p.status, &ok);
+            if (ok) {
+              void* cache = is_k ? a.k_cache : a.v_cache;
+              if (is_k) {
+                rope4(cs, lo, hi, r_lo, r_hi);
+              } else {
+                r_lo = lo;
+                r_hi = hi;
+              }
+              st_bf16x4(cache, off + fa, r_lo);
+              st_bf16x4(cache, off + fa + 64, r_hi);
+            }
+          }
+        }
+      } else if (EPI == EPI_Q2) {
+        const int Hq = a.n_q_heads, B = a.m_a, h = tile, b = n;
+        const int pos = a.seq_len[b];
+        if (pos < 0 || pos > a.max_ctx) {
+          set_status(p.status, DF_ERR_DEVICE_BOUNDS);
+        } else {
+          const float2* cs = a.rope + (size_t)pos * 64 + fa;
+          const size_t qi = ((size_t)b * Hq + h) * kHeadDim;
+          const float4 x1 = ld_bf16x4(a.q1_in, qi + fa), x1p = ld_bf16x4(a.q1_in, qi + fa + 64);
+          float4 r_lo, r_hi;
+          rope4(cs, x1, x1p, r_lo, r_hi);
+          const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
+          st_bf16x4(a.q_out, o1 + fa, r_lo);
+          st_bf16x4(a.q_out, o1 + fa + 64, r_hi);
+          const float4 x2 = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa), x1, lo);
+          const float4 x2p = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa + 64), x1p, hi);
+          rope4(cs, x2, x2p, r_lo, r_hi);
           const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
-          qo[o2 + i] = __float2bfloat16_rn(x2 * cs.x - x2p * cs.y);
-          qo[o2 + i + 64] = __float2bfloat16_rn(x2p * cs.x + x2 * cs.y);
+          st_bf16x4(a.q_out, o2 + fa, r_lo);
+          st_bf16x4(a.q_out, o2 + fa + 64, r_hi);
         }
-      } else {
-        const bool is_k = tile < Hq + Hkv;
-        const int hk = is_k ? tile - Hq : tile - Hq - Hkv;
-        bool ok;
-        const size_t off = cache_slot(a, b, hk, pos, p.status, &ok);
-        if (!ok) continue;
-        __nv_bfloat16* cache = reinterpret_cast<__nv_bfloat16*>(is_k ? a.k_cache : a.v_cache);
-        float v0 = acc(b, i), v1 = acc(b, i + 64);
-        if (is_k) {
-          const float t0 = v0 * cs.x - v1 * cs.y, t1 = v1 * cs.x + v0 * cs.y;
-          v0 = t0;
-          v1 = t1;
-        }
-        cache[off + i] = __float2bfloat16_rn(v0);
-        cache[off + i + 64] = __float2bfloat16_rn(v1);
       }
     }
-  } else if (EPI == EPI_Q2) {
-    const int Hq = a.n_q_heads, B = a.m_a, h = tile;
-    __nv_bfloat16* qo = reinterpret_cast<__nv_bfloat16*>(a.q_out);
-    for (int it = threadIdx.x; it < nl * B; it += kThreads) {
-      const int i = lo0 + it % nl, b = it / nl;
-      const int pos = a.seq_len[b];
-      if (pos < 0 || pos > a.max_ctx) {
-        set_status(p.status, DF_ERR_DEVICE_BOUNDS);
-        continue;
+    if (norm_out) {
+      // sum of h^2 over this CTA's features of each row: the nq units of a row are adjacent lanes
+      for (int off = 1; off < nq; off <<= 1) {
+        ss0 += __shfl_xor_sync(0xffffffffu, ss0, off);
+        ss1 += __shfl_xor_sync(0xffffffffu, ss1, off);
       }
-      const float2 cs = a.rope[(size_t)pos * 64 + i];
-      const size_t qi = ((size_t)b * Hq + h) * kHeadDim;
-      const float x1 = bf2f(a.q1_in, qi + i), x1p = bf2f(a.q1_in, qi + i + 64);
-      const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
-      qo[o1 + i] = __float2bfloat16_rn(x1 * cs.x - x1p * cs.y);
-      qo[o1 + i + 64] = __float2bfloat16_rn(x1p * cs.x + x1 * cs.y);
-      const float x2 = acc(b, i) + bf2f(a.vec, h * kHeadDim + i) * x1;
-      const float x2p = acc(b, i + 64) + bf2f(a.vec, h * kHeadDim + i + 64) * x1p;
-      const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
-      qo[o2 + i] = __float2bfloat16_rn(x2 * cs.x - x2p * cs.y);
-      qo[o2 + i + 64] = __float2bfloat16_rn(x2p * cs.x + x2 * cs.y);
+      if (live && qd == 0) {
+        const int part = tile * S + split;  // this CTA's features of row n
+        a.ss_out[(size_t)n * a.ss_ld + part] = ss0;
+        if (EPI == EPI_COUPLE_ADD && a.m_a > 0) a.ss_out[(size_t)(a.m_p + n) * a.ss_ld + part] = ss1;
+      }
     }
   }
-  // no CTA may leave while a peer can still read its partial tile
-  if (S > 1) cluster_sync();
+  // no CTA may leave before every copy into or out of its shared memory has completed
+  if (S > 1) cluster_wait();
 }
 
 template <int EPI>
@@ -330,13 +555,20 @@ int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = (unsigned)p.splits;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = 1;
+  attr[na].val.clusterDim.y = (unsigned)p.splits;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
+  if (p.a.pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, kern, mw, mx, p) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
@@ -345,11 +577,15 @@ int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p
 int gemm_tiles(int n_out, int epi) { return epi == EPI_SWIGLU ? n_out / 64 : (n_out + kGemmTileN - 1) / kGemmTileN; }
 
 // Reduction splits (cluster size): the smallest power of two, at most 8, that gives every SM a
-// tile slice, with at least 2 k-blocks per CTA. Depends only on the weight shape, never on which
-// flows are present.
+// tile slice, with at least 2 k-blocks per CTA. Depends only on the weight shape and the context's
+// capacity, never on which flows are present. A split CTA holds its partial tile and the S
+// received slices at once (1 KB per padded activation row), so contexts with more than 208 rows
+// of capacity do not split.
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi) {
   const int tiles = gemm_tiles(n_out, epi);
   const int kb = k / kGemmTileK;
+  const int max_rows = ((2 * ctx->cfg.max_batch + 15) / 16) * 16;
+  if (max_rows > kSplitMaxRows) return 1;
   int s = 1;
   while (s < 8 && tiles * s < ctx->num_sms && 2 * (2 * s) <= kb) s *= 2;
   return s;
@@ -358,8 +594,9 @@ int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi) {
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   const int m = a.m_p + a.m_a;
   if (m <= 0) return DF_OK;
-  if (m > kGemmMaxAct || a.k % kGemmTileK != 0 || a.k <= 0) return DF_ERR_SHAPE;
+  if (m > kGemmMaxAct || m > 2 * ctx->cfg.max_batch || a.k % kGemmTileK != 0 || a.k <= 0) return DF_ERR_SHAPE;
   if (a.epi == EPI_SWIGLU && a.n_out % 64 != 0) return DF_ERR_SHAPE;
+  if (a.g_next != nullptr && (a.n_out % 64 != 0 || !a.x_next || !a.ss_out)) return DF_ERR_ARG;
   GemmParams p;
   p.a = a;
   p.n_pad = ((m + 15) / 16) * 16;
@@ -367,15 +604,22 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   p.n_tiles = gemm_tiles(a.n_out, a.epi);
   p.splits = gemm_splits(ctx, a.n_out, a.k, a.epi);
   p.status = ctx->status;
+  const uintptr_t align = (a.epi == EPI_STORE_BF16 || a.epi == EPI_SWIGLU) ? 8 : 16;
+  p.vec_ok = a.y != nullptr && (reinterpret_cast<uintptr_t>(a.y) % align == 0) && (a.ldy % 4 == 0) ? 1 : 0;
+  if (a.g_next != nullptr && !p.vec_ok) return DF_ERR_ARG;
   const uint64_t w_rows = (a.epi == EPI_SWIGLU) ? 2ull * a.n_out : (uint64_t)a.n_out;
   CUtensorMap mw, mx;
   int rc = encode_map_2d_bf16(&mw, a.W, (uint64_t)a.k, w_rows, (uint64_t)a.k * 2, kGemmTileK, 64);
   if (rc != DF_OK) return rc;
   rc = encode_map_2d_bf16(&mx, a.x, (uint64_t)a.k, (uint64_t)m, (uint64_t)a.k * 2, kGemmTileK, (uint32_t)p.n_pad);
   if (rc != DF_OK) return rc;
-  // pipeline stages; after the main loop the same bytes hold the partial tile (512 B per row) and
-  // the reduced slice (512 / S B per row): 65536 + 512 n_pad >= 768 n_pad for n_pad <= 256
-  const size_t smem = 1024 + (size_t)kStages * (kABytes + p.n_pad * 128) + 256;
+  // data region: the pipeline stages; after the main loop the partial tile (512 B per activation
+  // row) or, when split, the staged slices plus the receive area (1 KB per row + bank pads). Then
+  // the barriers, the TMEM address slot and the 256-float row-scale array.
+  const int pipe = kStages * (kABytes + p.n_pad * 128);
+  const int parts = p.splits > 1 ? 1024 * p.n_pad + 32 * p.splits : 512 * p.n_pad;
+  p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
+  const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 4;
   switch (a.epi) {
     case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(mw, mx, p, smem, s);
     case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(mw, mx, p, smem, s);

@@ -56,6 +56,19 @@ struct GemmArgs {
   void* v_cache;
   const int32_t* page_table;
   int paged, page_size, max_ctx, max_pages, pages_per_seq;
+  // RMSNorm carried across kernels (decode step). When ss_in is set, the rows of x hold h (*) g
+  // and each output row is scaled by 1 / sqrt(sum_p ss_in[row * ss_ld + p] * inv_d + eps),
+  // p = 0 .. ss_parts - 1 in order.
+  const float* ss_in;
+  int ss_parts, ss_ld;
+  float inv_d, eps;
+  // Residual epilogues (ADD_F32, COUPLE_ADD) with g_next set also write the next norm's input
+  // x_next[row] = bf16(h_new (*) g_next) ([m, n_out]) and ss_out[row * ss_ld + tile * S + split] =
+  // the sum of h_new^2 over that CTA's features (n_tiles * S partials per row).
+  const void* g_next;
+  void* x_next;
+  float* ss_out;
+  int pdl;  // launch with programmatic dependent launch (weights prefetched before the wait)
 };
 
 struct AttnArgs {
@@ -101,6 +114,8 @@ struct dualflow_ctx {
   void* o = nullptr;               // [2, max_batch, Hq * D]
   void* u = nullptr;               // [2 * max_batch, F]
   float* raw = nullptr;            // fp32 path: [2 * max_batch, max_n] projection scratch
+  float* ss = nullptr;             // [2 * max_batch][ss_ld] per-row partial sums of squares (bf16)
+  int ss_ld = 0;                   // ceil(d / 128) tiles x 8 splits
   int32_t* tokens_dev = nullptr;   // dualflow_step_host staging
   float* logits_dev = nullptr;
   int graphs_enabled = 1;
@@ -123,7 +138,7 @@ int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 // Launchers (return dualflow_status).
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s);
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi);
-int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s);
+int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl = 0);
 // The same kernel with caller-chosen workspace: split partials (>= pairs + ctas slots of
 // kAttnPartFloats), per-pair merge counters (zero on entry), the status word, and a grid of `ctas`
 // CTAs; cache geometry is taken from `cfg`. Used by the allocation-free entry point.
@@ -132,6 +147,11 @@ int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, floa
 
 int launch_embed_rmsnorm(dualflow_ctx* ctx, const void* E1, const void* E2, const int32_t* tokens, const void* g,
                          int batch, int aux_on, cudaStream_t s);
+// Decode step (bf16): h = E_f[token]; x = bf16(h (*) g); ss[row] = sum h^2 (one partial).
+int launch_embed_prep(dualflow_ctx* ctx, const void* E1, const void* E2, const int32_t* tokens, const void* g,
+                      int batch, int aux_on, cudaStream_t s);
+// The same from the residual h (bf16): x = bf16(h (*) g); ss[row] = sum h^2 (one partial).
+int launch_norm_prep(dualflow_ctx* ctx, float* h, const void* g, int batch, int aux_on, cudaStream_t s);
 int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s);
 int launch_rope_q1(dualflow_ctx* ctx, const void* q1, void* q, const int32_t* seq_len, int batch, cudaStream_t s);
 

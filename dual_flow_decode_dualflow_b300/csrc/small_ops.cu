@@ -91,6 +91,40 @@ __global__ void rmsnorm_rows_kernel(float* h, const T* E1, const T* E2, const in
   }
 }
 
+// Input of a norm-fed bf16 projection (one warp per row n = f * B + b): x_n = bf16(h_n (*) g) and
+// ss[n] = sum h_n^2; the projection scales its fp32 product by 1 / sqrt(ss / d + eps). With E1/E2
+// given (first kernel of the decode step) the row is first gathered, h_n = E_f[token_b], and
+// written to the fp32 residual. d must be a multiple of 4.
+__global__ void norm_prep_kernel(float* h, const __nv_bfloat16* E1, const __nv_bfloat16* E2, const int32_t* tokens,
+                                 const __nv_bfloat16* g, __nv_bfloat16* x, float* ss, int ss_ld, int rows, int B, int d,
+                                 int V, int32_t* status) {
+  griddep_launch_dependents();
+  const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (n >= rows) return;
+  const __nv_bfloat16* src = nullptr;
+  if (E1 != nullptr) {
+    int tok = tokens[n % B];
+    if (tok < 0 || tok >= V) {
+      if (lane == 0) set_status(status, DF_ERR_DEVICE_BOUNDS);
+      tok = 0;
+    }
+    src = (n / B ? E2 : E1) + (size_t)tok * d;
+  }
+  float* hr = h + (size_t)n * d;
+  __nv_bfloat16* xr = x + (size_t)n * d;
+  float s = 0.f;
+#pragma unroll 4
+  for (int q = lane * 4; q < d; q += 128) {
+    const float4 v = src ? ld4(src + q) : ld4(hr + q);
+    const float4 gg = ld4(g + q);
+    if (src) st4(hr + q, v);
+    st4(xr + q, make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w));
+    s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) ss[(size_t)n * ss_ld] = s;
+}
+
 // Attention-only call without the auxiliary flow: q[0, b, h] = RoPE(q1[b, h]) at position seq_len[b].
 __global__ void rope_q1_bf16_kernel(const __nv_bfloat16* q1, __nv_bfloat16* q, const int32_t* seq_len,
                                     const float2* rope, int Hq, int max_ctx, int32_t* status) {
@@ -319,6 +353,25 @@ int launch_embed_rmsnorm(dualflow_ctx* ctx, const void* E1, const void* E2, cons
     rmsnorm_rows_kernel<float><<<blocks, 128, 0, s>>>(ctx->h, (const float*)E1, (const float*)E2, tokens,
                                                       (const float*)g, (float*)ctx->x, rows, batch, c.d_model,
                                                       c.vocab, c.rms_eps, ctx->status);
+  return ok_launch();
+}
+
+int launch_embed_prep(dualflow_ctx* ctx, const void* E1, const void* E2, const int32_t* tokens, const void* g,
+                      int batch, int aux_on, cudaStream_t s) {
+  const dualflow_config& c = ctx->cfg;
+  const int rows = aux_on ? 2 * batch : batch;
+  norm_prep_kernel<<<(rows + 3) / 4, 128, 0, s>>>(ctx->h, (const __nv_bfloat16*)E1, (const __nv_bfloat16*)E2, tokens,
+                                                  (const __nv_bfloat16*)g, (__nv_bfloat16*)ctx->x, ctx->ss, ctx->ss_ld,
+                                                  rows, batch, c.d_model, c.vocab, ctx->status);
+  return ok_launch();
+}
+
+int launch_norm_prep(dualflow_ctx* ctx, float* h, const void* g, int batch, int aux_on, cudaStream_t s) {
+  const dualflow_config& c = ctx->cfg;
+  const int rows = aux_on ? 2 * batch : batch;
+  norm_prep_kernel<<<(rows + 3) / 4, 128, 0, s>>>(h, nullptr, nullptr, nullptr, (const __nv_bfloat16*)g,
+                                                  (__nv_bfloat16*)ctx->x, ctx->ss, ctx->ss_ld, rows, batch,
+                                                  c.d_model, 0, ctx->status);
   return ok_launch();
 }
 

@@ -165,8 +165,9 @@ enum {
 
 /* Stacked-activation linear: rows 0..m_primary-1 of x are the primary flow, the next m_aux rows
  * the auxiliary flow; one read of W serves all of them. x: device [m_primary + m_aux, k] storage
- * dtype; W: device [n, k] storage dtype; y per `epilogue`. k must be a multiple of 64 and
- * m_primary + m_aux <= 256 for bf16 contexts. */
+ * dtype; W: device [n, k] storage dtype; y per `epilogue`. For bf16 contexts k must be a multiple
+ * of 64, m_primary + m_aux <= 2 * max_batch (<= 256), x, W and epi_arg 16-byte aligned; each row's
+ * result does not depend on the other rows present. */
 DF_API int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_primary, int32_t m_aux, const void* W,
                             int32_t n, int32_t k, void* y, int32_t epilogue, const void* epi_arg,
                             dualflow_stream stream);

@@ -51,9 +51,11 @@ are silent, each one a choice of this implementation:
 
 Precision: inputs arrive as the stored values widened to fp64. With mirror=True and a bf16
 workload the oracle rounds (to nearest bf16, ties to even) exactly where the GPU path stores
-bf16: each normed activation x, the post-RoPE queries, the appended k1/v1, the attention
-output o and the SwiGLU output u (after coupling); router logits are rounded to fp32 before
-the top-k decision, the precision in which the GPU takes it. Everything else is fp64.
+bf16: the operand of each norm-fed projection (the gain-scaled row g (*) h, whose product is
+then scaled by 1/rms -- an exact rewriting of RMSNorm(h).W^T), the post-RoPE queries, the
+appended k1/v1, the attention output o and the SwiGLU output u (after coupling); router logits
+are rounded to fp32 before the top-k decision, the precision in which the GPU takes it.
+Everything else is fp64. With mirror=False every step is the plain fp64 definition.
 """
 from __future__ import annotations
 
@@ -91,9 +93,14 @@ def round_f32(x: np.ndarray) -> np.ndarray:
 # building blocks
 # ---------------------------------------------------------------------------------------------
 
+def rms_scale(h: np.ndarray, eps: float) -> np.ndarray:
+    """1 / sqrt(mean(h^2) + eps) of each row of h (R6)."""
+    return 1.0 / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)
+
+
 def rmsnorm(h: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
     """RMSNorm of each row of h with gain g (R6; LLaMA family of [T4], gains shared per [T3])."""
-    return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps) * g
+    return h * rms_scale(h, eps) * g
 
 
 def rope(x: np.ndarray, pos: int, base: float) -> np.ndarray:
@@ -189,6 +196,18 @@ class HParams:
 def _store(x, hp: HParams, mirror: bool):
     """The value the GPU path keeps at a bf16 storage point (identity otherwise)."""
     return round_bf16(x) if (mirror and hp.dtype == "bf16") else x
+
+
+def _normed(h, g, hp: HParams, mirror: bool):
+    """RMSNorm(h) with gain g as the input of a linear layer.
+
+    RMSNorm(h).W^T = (1/rms(h)) ((g (*) h).W^T). The bf16 GPU path stores the gain-scaled row
+    g (*) h as the product's operand and scales the fp32 product by 1/rms; mirror mode rounds at
+    that storage point (the scale commutes with the product, so it is applied to the operand here).
+    """
+    if mirror and hp.dtype == "bf16":
+        return round_bf16(h * g) * rms_scale(h, hp.rms_eps)
+    return rmsnorm(h, g, hp.rms_eps)
 
 
 def _attention_block(hp, P, x, cache, b, L, pos, aux_on, mirror, append):
@@ -324,12 +343,12 @@ def decode_step(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequenc
         P = layers[layer]
         for i, b in enumerate(rows):
             L = int(seq_len[b])
-            x = [_store(rmsnorm(h[f, i], P["g_attn"], hp.rms_eps), hp, mirror) for f in range(nf)]
+            x = [_normed(h[f, i], P["g_attn"], hp, mirror) for f in range(nf)]
             o, k_new[layer, i], v_new[layer, i] = _attention_block(
                 hp, P, x, caches[layer], b, L, L, aux_on, mirror, append=True)
             for f in range(nf):
                 h[f, i] = h[f, i] + P["Wo"] @ o[f]  # shared O projection, residual
-            x = [_store(rmsnorm(h[f, i], P["g_mlp"], hp.rms_eps), hp, mirror) for f in range(nf)]
+            x = [_normed(h[f, i], P["g_mlp"], hp, mirror) for f in range(nf)]
             if hp.n_experts == 0:
                 y = _dense_mlp(hp, P, x, aux_on, mirror)
             else:
@@ -345,7 +364,7 @@ def decode_step(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequenc
     logits = np.full((2, R, hp.vocab), np.nan)
     for f in range(nf):
         for i in range(R):
-            xf = _store(rmsnorm(h[f, i], glob["g_final"], hp.rms_eps), hp, mirror)
+            xf = _normed(h[f, i], glob["g_final"], hp, mirror)
             logits[f, i] = glob["W_lm"] @ xf  # shared LM head [T1]
     return dict(logits=logits, k_new=k_new, v_new=v_new, expert_ids=ids, router_logits=rlog, h=h)
 

@@ -406,6 +406,20 @@ def pin_moe_special_cases(O):
     close(res["h"][1, 0], h_mid[1] + y[1], 1e-12, "brute MoE auxiliary")
 
 
+def pin_mirror_tracks_exact(O):
+    """Mirror mode only rounds at the bf16 storage points: on a small bf16 model it stays within
+    bf16 rounding of the exact fp64 step. Residual rows of scale ~8 and gains of spread 0.4 make a
+    dropped 1/rms or a dropped gain in the mirrored norm show far above that rounding."""
+    hp = tiny_hp(O, dtype="bf16")
+    glob, layers, caches, tokens, L = tiny_model(O, hp, n_layers=2, seed=21)
+    glob = dict(glob, E1=glob["E1"] * 8.0, E2=glob["E2"] * 8.0, g_final=1.0 + 4.0 * (glob["g_final"] - 1.0))
+    layers = [dict(P, g_attn=1.0 + 4.0 * (P["g_attn"] - 1.0), g_mlp=1.0 + 4.0 * (P["g_mlp"] - 1.0)) for P in layers]
+    exact = O.decode_step(hp, glob, layers, caches, tokens, L, aux_on=True, mirror=False)
+    mirr = O.decode_step(hp, glob, layers, caches, tokens, L, aux_on=True, mirror=True)
+    close(mirr["logits"], exact["logits"], 3e-2, "mirrored bf16 step vs exact fp64 step")
+    assert not np.array_equal(mirr["logits"], exact["logits"]), "mirror mode rounds nothing"
+
+
 def pin_mixture_head(O):
     V = 10
     a, pm, tok = O.mixture_head(np.zeros(V), np.arange(V, dtype=F64))
@@ -423,4 +437,4 @@ def pin_mixture_head(O):
 
 ALL_PINS = [pin_round_bf16, pin_rmsnorm, pin_rope, pin_attention_closed_forms, pin_attention_gqa_vs_sdpa,
             pin_small_ops, pin_primary_is_standard_decoder, pin_flow_invariants, pin_coupling_special_cases, pin_query_coupling_source,
-            pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mixture_head]
+            pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mirror_tracks_exact, pin_mixture_head]

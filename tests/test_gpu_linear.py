@@ -16,19 +16,36 @@ def _bf16(seed, name, shape, sigma, dev):
     return t, dfsynth.bf16_bits_to_f32(host).astype(np.float64)
 
 
+def _ctx(max_batch):
+    cfg = dfl.make_config(n_layers=1, d_model=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, ffn_hidden=8192,
+                          vocab=32000, dtype=dfl.DF_DTYPE_BF16, max_batch=max_batch, max_ctx=64)
+    return dfl.dualflow_init(cfg)
+
+
 @pytest.fixture(scope="module")
 def ctx(cuda_device):
-    cfg = dfl.make_config(n_layers=1, d_model=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, ffn_hidden=8192,
-                          vocab=32000, dtype=dfl.DF_DTYPE_BF16, max_batch=128, max_ctx=64)
-    h = dfl.dualflow_init(cfg)
+    """Capacity 2 x 64 rows: the split-K (cluster) path is taken where the output has few tiles."""
+    h = _ctx(64)
     yield h
     dfl.dualflow_free(h)
 
 
-@pytest.mark.parametrize("mp,ma,n,k", [(1, 0, 128, 64), (3, 3, 200, 128), (8, 0, 2048, 2048), (32, 32, 2048, 2048),
-                                       (32, 32, 3072, 2048), (32, 32, 2048, 8192), (64, 64, 1000, 512),
-                                       (128, 128, 384, 256), (5, 5, 32000, 2048), (17, 0, 130, 192)])
-def test_store_f32(cuda_device, ctx, mp, ma, n, k):
+@pytest.fixture(scope="module")
+def ctx_wide(cuda_device):
+    """Capacity 2 x 128 rows: too many rows for a split CTA to hold, every launch is unsplit."""
+    h = _ctx(128)
+    yield h
+    dfl.dualflow_free(h)
+
+
+# (rows, n, k) chosen so that the reduction is split 8 ways (few tiles, long k), 4, 2 and not at all,
+# with ragged row counts and ragged output tiles
+SHAPES = [(1, 0, 128, 64), (3, 3, 200, 128), (8, 0, 2048, 2048), (32, 32, 2048, 2048), (32, 32, 3072, 2048),
+          (32, 32, 2048, 8192), (64, 64, 1000, 512), (5, 5, 32000, 2048), (17, 0, 130, 192), (32, 32, 16384, 2048),
+          (24, 24, 4096, 1024), (7, 7, 1000, 4096)]
+
+
+def _store_f32(cuda_device, ctx, mp, ma, n, k):
     x, xr = _bf16(11, "x", (mp + ma, k), 1.0, cuda_device)
     W, Wr = _bf16(12, "W", (n, k), 0.02, cuda_device)
     y = torch.full((mp + ma, n), float("nan"), device=cuda_device)
@@ -36,6 +53,25 @@ def test_store_f32(cuda_device, ctx, mp, ma, n, k):
     assert dfl.dualflow_sync_status(ctx) == 0
     ref = xr @ Wr.T
     assert H.rel_err(H.to_f64(y), ref) < 1e-5
+
+
+@pytest.mark.parametrize("mp,ma,n,k", SHAPES)
+def test_store_f32(cuda_device, ctx, mp, ma, n, k):
+    _store_f32(cuda_device, ctx, mp, ma, n, k)
+
+
+@pytest.mark.parametrize("mp,ma,n,k", [(128, 128, 384, 256), (100, 100, 2048, 2048)])
+def test_store_f32_wide(cuda_device, ctx_wide, mp, ma, n, k):
+    _store_f32(cuda_device, ctx_wide, mp, ma, n, k)
+
+
+def test_rows_beyond_capacity_rejected(cuda_device, ctx):
+    x, _ = _bf16(13, "x", (130, 128), 1.0, cuda_device)
+    W, _ = _bf16(14, "W", (128, 128), 0.02, cuda_device)
+    y = torch.zeros((130, 128), device=cuda_device)
+    with pytest.raises(dfl.DualFlowError) as e:
+        dfl.dualflow_stacked_linear(ctx, x, 65, 65, W, 128, 128, y, dfl.DF_EPI_STORE_F32)
+    assert e.value.code == dfl.DF_ERR_SHAPE
 
 
 @pytest.mark.parametrize("epi", [dfl.DF_EPI_STORE_BF16, dfl.DF_EPI_ADD_F32, dfl.DF_EPI_COUPLE_ADD])

@@ -38,8 +38,11 @@ MUTANTS = {
     "c_wrong_source": ('y[1] = y[1] + P["c"] * y[0]', 'y[1] = y[1] + P["c"] * y[1]'),
     "silu_is_sigmoid": ("return z / (1.0 + np.exp(-z))", "return 1.0 / (1.0 + np.exp(-z))"),
     "rmsnorm_wrong_axis": ("np.mean(h * h, axis=-1, keepdims=True)", "np.mean(h * h, axis=0, keepdims=True)"),
-    "rmsnorm_no_sqrt": ("return h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps) * g",
-                        "return h / (np.mean(h * h, axis=-1, keepdims=True) + eps) * g"),
+    "rmsnorm_no_sqrt": ("return 1.0 / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + eps)",
+                        "return 1.0 / (np.mean(h * h, axis=-1, keepdims=True) + eps)"),
+    "mirror_norm_unscaled": ("return round_bf16(h * g) * rms_scale(h, hp.rms_eps)", "return round_bf16(h * g)"),
+    "mirror_norm_no_gain": ("return round_bf16(h * g) * rms_scale(h, hp.rms_eps)",
+                            "return round_bf16(h) * rms_scale(h, hp.rms_eps)"),
     "primary_uses_E2": ('h[0, i] = glob["E1"][tokens[b]]', 'h[0, i] = glob["E2"][tokens[b]]'),
     "no_router_replay": ("S2 = topk_lower_index(r1, hp.topk_aux)", "S2 = topk_lower_index(r2, hp.topk_aux)"),
     "aux_weights_from_primary": ("    w2 = softmax(r2[S2])\n    return", "    w2 = softmax(r1[S2])\n    return"),
@@ -50,8 +53,7 @@ MUTANTS = {
     "o_proj_dropped": ('h[f, i] = h[f, i] + P["Wo"] @ o[f]', "h[f, i] = h[f, i]"),
     "paged_wrong_page": ("ks = [np.asarray(self.K[int(self.table[b, j])], dtype=F64) for j in range(n)]",
                          "ks = [np.asarray(self.K[int(self.table[b, n - 1 - j])], dtype=F64) for j in range(n)]"),
-    "final_norm_dropped": ('xf = _store(rmsnorm(h[f, i], glob["g_final"], hp.rms_eps), hp, mirror)',
-                           "xf = _store(h[f, i], hp, mirror)"),
+    "final_norm_dropped": ('xf = _normed(h[f, i], glob["g_final"], hp, mirror)', "xf = h[f, i]"),
 }
 
 
