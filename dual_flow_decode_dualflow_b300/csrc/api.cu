@@ -85,7 +85,7 @@ int validate_config(const dualflow_config* c) {
     if (c->d_model % 64 || c->ffn_hidden % 64 || (c->n_q_heads * c->head_dim) % 64) return DF_ERR_UNSUPPORTED;
     if (2 * c->max_batch > kGemmMaxAct) return DF_ERR_UNSUPPORTED;
     if (c->paged && c->page_size != 16 && c->page_size != 32 && c->page_size != 64) return DF_ERR_UNSUPPORTED;
-    if (c->n_experts > 0) return DF_ERR_UNSUPPORTED;
+    if (c->n_experts > 32) return DF_ERR_UNSUPPORTED;  // routing keeps one expert per lane of a warp
   } else {
     if (c->head_dim / 2 > 1024 || c->max_ctx > 40000 || c->d_model % 4) return DF_ERR_UNSUPPORTED;
     if (c->n_experts > 0) return DF_ERR_UNSUPPORTED;
@@ -165,11 +165,13 @@ int check_weights(const dualflow_ctx* ctx, const dualflow_weights* w) {
   if (!ok(w->E1) || !ok(w->E2) || !ok(w->W_lm) || !ok(w->g_final)) return DF_ERR_ARG;
   if (!w->g_attn || !w->g_mlp || !w->Wqkv || !w->Wo || !w->a || !w->b || !w->c) return DF_ERR_ARG;
   if (c.n_experts == 0 && (!w->Wgu || !w->Wd)) return DF_ERR_ARG;
+  if (c.n_experts > 0 && (!w->Wr || !w->We_gu || !w->We_d)) return DF_ERR_ARG;
   for (int l = 0; l < c.n_layers; ++l) {
     if (!ok(w->g_attn[l]) || !ok(w->g_mlp[l]) || !ok(w->Wqkv[l]) || !ok(w->Wo[l]) || !ok(w->a[l]) || !ok(w->b[l]) ||
         !ok(w->c[l]))
       return DF_ERR_ARG;
     if (c.n_experts == 0 && (!ok(w->Wgu[l]) || !ok(w->Wd[l]))) return DF_ERR_ARG;
+    if (c.n_experts > 0 && (!ok(w->Wr[l]) || !ok(w->We_gu[l]) || !ok(w->We_d[l]))) return DF_ERR_ARG;
   }
   return DF_OK;
 }
@@ -202,11 +204,85 @@ void reset_counts(dualflow_ctx* ctx) {
   ctx->prof_n = 0;
 }
 
+// ------------------------------------------------------------------ the MoE MLP (bf16)
+// x (the norm-fed operand, rows scaled by 1 / rms from ss_parts partials) -> router logits ->
+// routing decision -> every expert's gate/up for the rows that chose it -> every expert's down ->
+// combine with output coupling and residual into h (and, with g_next, the next norm's operand).
+int run_moe(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int batch, int aux_on, int ss_parts,
+            int32_t* ids, const void* g_next, int pdl, cudaStream_t s) {
+  const dualflow_config& c = ctx->cfg;
+  const int mp = batch, ma = aux_on ? batch : 0, E = c.n_experts, mrows = 2 * c.max_batch;
+  Launcher L{ctx, s};
+  auto normed = [&](GemmArgs& g) {
+    g.ss_in = ctx->ss;
+    g.ss_parts = ss_parts;
+    g.ss_ld = ctx->ss_ld;
+    g.inv_d = 1.0f / (float)c.d_model;
+    g.eps = c.rms_eps;
+    g.pdl = pdl;
+  };
+  GemmArgs r = gemm_args(ctx);
+  r.x = ctx->x;
+  r.W = w->Wr[l];
+  r.n_out = E;
+  r.k = c.d_model;
+  r.m_p = mp;
+  r.m_a = ma;
+  r.epi = EPI_STORE_F32;
+  r.y = ctx->rlog;
+  r.ldy = E;
+  normed(r);
+  DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_gemm_tc(ctx, r, s); }));
+  DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_moe_route(ctx, ctx->rlog, batch, aux_on, ids, s, pdl); }));
+  GemmArgs g = gemm_args(ctx);
+  g.x = ctx->x;
+  g.W = w->We_gu[l];
+  g.n_out = c.ffn_hidden;
+  g.k = c.d_model;
+  g.m_p = mp;
+  g.m_a = ma;
+  g.epi = EPI_MOE_GATEUP;
+  g.y = ctx->moe_u;
+  g.ldy = c.ffn_hidden;
+  g.vec = w->b[l];
+  g.n_groups = E;
+  g.w_group_rows = 2 * c.ffn_hidden;
+  g.y_group_stride = (size_t)mrows * c.ffn_hidden;
+  g.sel_pos = ctx->sel_pos;
+  normed(g);
+  DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_gemm_tc(ctx, g, s); }));
+  GemmArgs d = gemm_args(ctx);
+  d.x = ctx->moe_u;
+  d.W = w->We_d[l];
+  d.n_out = c.d_model;
+  d.k = c.ffn_hidden;
+  d.m_p = mp;
+  d.m_a = ma;
+  d.epi = EPI_MOE_DOWN;
+  d.y = ctx->moe_y;
+  d.ldy = c.d_model;
+  d.n_groups = E;
+  d.w_group_rows = c.d_model;
+  d.x_group_rows = mrows;
+  d.y_group_stride = (size_t)mrows * c.d_model;
+  d.sel_pos = ctx->sel_pos;
+  d.pdl = pdl;
+  DF_TRY(L(DF_PROF_DOWN, [&] { return launch_gemm_tc(ctx, d, s); }));
+  return L(DF_PROF_DOWN, [&] { return launch_moe_combine(ctx, h, batch, aux_on, w->c[l], g_next, s, pdl); });
+}
+
 // ------------------------------------------------------------------ the MLP block
 int run_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int batch, int aux_on, cudaStream_t s) {
   const dualflow_config& c = ctx->cfg;
   const int mp = batch, ma = aux_on ? batch : 0;
   Launcher L{ctx, s};
+  if (c.dtype == DF_DTYPE_BF16 && c.n_experts > 0) {
+    DF_TRY(L(DF_PROF_NORM, [&] { return launch_norm_prep(ctx, h, w->g_mlp[l], batch, aux_on, s); }));
+    const int kmax = std::max(c.topk_primary, c.topk_aux);
+    int32_t* ids = ctx->moe_ids + (size_t)l * 2 * batch * kmax;
+    DF_TRY(run_moe(ctx, h, w, l, batch, aux_on, 1, ids, nullptr, 0, s));
+    return DF_OK;
+  }
   if (c.dtype == DF_DTYPE_BF16) {
     // x = bf16(h (*) g_mlp) with per-row sums of squares; gate/up scales its rows by 1 / rms
     DF_TRY(L(DF_PROF_NORM, [&] { return launch_norm_prep(ctx, h, w->g_mlp[l], batch, aux_on, s); }));
@@ -270,6 +346,7 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
   const int ss_ld = ctx->ss_ld;
   // row sums of squares left by the O projection and by the down projection: one per CTA
   const int o_parts = d_tiles * gemm_splits(ctx, c.d_model, qd, EPI_ADD_F32);
+  const int kmax = std::max(c.topk_primary, c.topk_aux);
   const int d_parts = d_tiles * gemm_splits(ctx, c.d_model, c.ffn_hidden, EPI_COUPLE_ADD);
   Launcher L{ctx, s};
   DF_TRY(L(DF_PROF_NORM, [&] {
@@ -326,6 +403,13 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
     norm_output(o, w->g_mlp[l]);
     DF_TRY(L(DF_PROF_OPROJ, [&] { return launch_gemm_tc(ctx, o, s); }));
     ss_parts = o_parts;
+    const void* g_next = l + 1 < c.n_layers ? w->g_attn[l + 1] : w->g_final;
+    if (c.n_experts > 0) {
+      int32_t* ids = ctx->moe_ids + (size_t)l * 2 * batch * kmax;
+      DF_TRY(run_moe(ctx, ctx->h, w, l, batch, aux_on, ss_parts, ids, g_next, pdl, s));
+      ss_parts = (c.d_model + 511) / 512;
+      continue;
+    }
     GemmArgs gu = gemm_args(ctx);
     gu.x = ctx->x;
     gu.W = w->Wgu[l];
@@ -350,7 +434,7 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
     dn.y = ctx->h;
     dn.ldy = c.d_model;
     dn.vec = w->c[l];
-    norm_output(dn, l + 1 < c.n_layers ? w->g_attn[l + 1] : w->g_final);
+    norm_output(dn, g_next);
     DF_TRY(L(DF_PROF_DOWN, [&] { return launch_gemm_tc(ctx, dn, s); }));
     ss_parts = d_parts;
   }
@@ -504,6 +588,21 @@ int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
     return fail(DF_ERR_OOM);
   ctx->ss_ld = 8 * ((c.d_model + kGemmTileN - 1) / kGemmTileN);
   if (dalloc(&ctx->ss, (size_t)ctx->ss_ld * MB * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+  if (c.n_experts > 0) {
+    const size_t E = c.n_experts, kmax = std::max(c.topk_primary, c.topk_aux);
+    if (dalloc(&ctx->rlog, MB * E * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+    if (dalloc(&ctx->sel_pos, MB * E * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
+    if (dalloc(&ctx->sel_w, MB * E * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+    if (dalloc(&ctx->moe_u, E * MB * c.ffn_hidden * es) != DF_OK) return fail(DF_ERR_OOM);
+    if (dalloc(&ctx->moe_y, E * MB * c.d_model * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+    if (dalloc(&ctx->moe_ids, (size_t)std::max(c.n_layers, 1) * MB * kmax * sizeof(int32_t)) != DF_OK)
+      return fail(DF_ERR_OOM);
+    // expert intermediates of rows that did not choose an expert are read (and ignored) by that
+    // expert's down projection: start them at zero
+    if (cudaMemset(ctx->moe_u, 0, E * MB * c.ffn_hidden * es) != cudaSuccess) return fail(DF_ERR_CUDA);
+    if (cudaMemset(ctx->moe_ids, 0xff, (size_t)std::max(c.n_layers, 1) * MB * kmax * sizeof(int32_t)) != cudaSuccess)
+      return fail(DF_ERR_CUDA);
+  }
   if (dalloc(&ctx->tokens_dev, (size_t)c.max_batch * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
   if (dalloc(&ctx->logits_dev, (size_t)MB * std::max(c.vocab, 1) * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
   if (cudaDeviceSynchronize() != cudaSuccess) return fail(DF_ERR_CUDA);
@@ -520,7 +619,8 @@ int dualflow_free(dualflow_ctx* ctx) {
     if (r.b) cudaEventDestroy(r.b);
   }
   void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
-                  ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss};
+                  ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss,
+                  ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete ctx;
@@ -610,14 +710,34 @@ int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_primary,
 
 int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int32_t layer, int32_t batch,
                          int32_t aux_on, int32_t* expert_ids_out, dualflow_stream stream) {
-  (void)expert_ids_out;
   if (!ctx || !h || !w || !aligned16(h)) return DF_ERR_ARG;
   if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
   if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
   if (layer < 0 || layer >= ctx->cfg.n_layers) return DF_ERR_ARG;
   DF_TRY(check_weights(ctx, w));
   reset_counts(ctx);
-  return run_mlp(ctx, h, w, layer, batch, aux_on, S(stream));
+  DF_TRY(run_mlp(ctx, h, w, layer, batch, aux_on, S(stream)));
+  const dualflow_config& c = ctx->cfg;
+  if (expert_ids_out && c.n_experts > 0) {
+    const size_t kmax = std::max(c.topk_primary, c.topk_aux), n = 2 * (size_t)batch * kmax;
+    if (cudaMemcpyAsync(expert_ids_out, ctx->moe_ids + (size_t)layer * n, n * sizeof(int32_t),
+                        cudaMemcpyDeviceToDevice, S(stream)) != cudaSuccess)
+      return DF_ERR_CUDA;
+  }
+  return DF_OK;
+}
+
+int dualflow_expert_ids(dualflow_ctx* ctx, int32_t* ids, int32_t batch, dualflow_stream stream) {
+  if (!ctx || !ids) return DF_ERR_ARG;
+  const dualflow_config& c = ctx->cfg;
+  if (c.n_experts == 0) return DF_ERR_UNSUPPORTED;
+  if (batch <= 0 || batch > c.max_batch) return DF_ERR_SHAPE;
+  const size_t kmax = std::max(c.topk_primary, c.topk_aux);
+  const size_t n = (size_t)c.n_layers * 2 * batch * kmax;
+  if (n == 0) return DF_OK;
+  return cudaMemcpyAsync(ids, ctx->moe_ids, n * sizeof(int32_t), cudaMemcpyDeviceToDevice, S(stream)) == cudaSuccess
+             ? DF_OK
+             : DF_ERR_CUDA;
 }
 
 int dualflow_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,

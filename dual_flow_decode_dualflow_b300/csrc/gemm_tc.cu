@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const GemmArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, split = blockIdx.y;
+  const int tile = blockIdx.x, split = blockIdx.y, grp = blockIdx.z;
   const int kb0 = (int)((long long)split * p.kb_total / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.kb_total / p.splits);
   const int nkb = kb1 - kb0;
@@ -232,13 +232,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   int row0, row1;
-  if (EPI == EPI_SWIGLU) {
+  if (EPI == EPI_SWIGLU || EPI == EPI_MOE_GATEUP) {
     row0 = 64 * tile;                 // gate rows of hidden units [64 tile, 64 tile + 64)
     row1 = a.n_out + 64 * tile;       // up rows of the same units
   } else {
     row0 = kGemmTileN * tile;
     row1 = row0 + 64;
   }
+  row0 += grp * a.w_group_rows;       // this expert's weights (grouped launch)
+  row1 += grp * a.w_group_rows;
+  const int xrow = grp * a.x_group_rows;
 
   if (warp == 0 && lane == 0) {
     // TMA producer: weights are streamed once (evict-first), activations stay L2-resident.
@@ -254,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     griddep_wait();
     for (int i = 0; i < npre; ++i)
-      tma_load_2d_hint(sB + i * b_bytes, &map_x, &full[i], (kb0 + i) * kGemmTileK, 0, pol_x);
+      tma_load_2d_hint(sB + i * b_bytes, &map_x, &full[i], (kb0 + i) * kGemmTileK, xrow, pol_x);
     for (int i = npre; i < nkb; ++i) {
       const int s = i % kStages;
       const uint32_t ph = (uint32_t)(i / kStages) & 1u;
@@ -266,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kc = (kb0 + i) * kGemmTileK;
       tma_load_2d_hint(sA + s * kABytes, &map_w, &full[s], kc, row0, pol_w);
       tma_load_2d_hint(sA + s * kABytes + kABytes / 2, &map_w, &full[s], kc, row1, pol_w);
-      tma_load_2d_hint(sB + s * b_bytes, &map_x, &full[s], kc, 0, pol_x);
+      tma_load_2d_hint(sB + s * b_bytes, &map_x, &full[s], kc, xrow, pol_x);
     }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer: 4 x (M=128, N=n_pad, K=16) per stage, accumulate in TMEM.
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool scaled = a.ss_in != nullptr;
   const bool norm_out = (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD) && a.g_next != nullptr;
   // units of work: (activation row, quad); paired epilogues take the primary row and its auxiliary row
-  const bool paired = EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV;
+  const bool paired = EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV || EPI == EPI_MOE_GATEUP;
   const int rows = (EPI == EPI_Q2) ? a.m_a : paired ? a.m_p : m;
   const int units = rows * nq;
   for (int base = 0; base < units; base += kThreads) {
@@ -441,6 +444,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     f4_get(z2, j) + __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.vec)[f + j]) * z1j;
             }
           }
+        }
+      } else if (EPI == EPI_MOE_GATEUP) {
+        // expert grp: rows that selected it; the auxiliary row couples to the primary row only
+        // when the primary selected the same expert
+        const int E = a.n_groups, j = tile * 64 + fa;
+        __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(a.y) + (size_t)grp * a.y_group_stride;
+        const bool s1 = a.sel_pos[(size_t)n * E + grp] >= 0;
+        const bool s2 = a.m_a > 0 && a.sel_pos[(size_t)(a.m_p + n) * E + grp] >= 0;
+        const float4 u1 = f4_silu_mul(lo, hi);
+        if (s1) st_bf16x4(u, (size_t)n * a.ldy + j, u1);
+        if (s2) {
+          float4 g2, p2;
+          reduce_pair(red, lo0, a.m_p + n, qd, g2, p2);
+          if (scaled) {
+            const float r = rstd_s[a.m_p + n];
+            g2 = f4_scale(g2, r);
+            p2 = f4_scale(p2, r);
+          }
+          float4 u2 = f4_silu_mul(g2, p2);
+          if (s1) u2 = f4_fma(ld_bf16x4(a.vec, j), u1, u2);
+          st_bf16x4(u, (size_t)(a.m_p + n) * a.ldy + j, u2);
+        }
+      } else if (EPI == EPI_MOE_DOWN) {
+        if (a.sel_pos[(size_t)n * a.n_groups + grp] >= 0) {
+          float* y = reinterpret_cast<float*>(a.y) + (size_t)grp * a.y_group_stride + (size_t)n * a.ldy;
+          if (fg < a.n_out) *reinterpret_cast<float4*>(y + fg) = lo;
+          if (fg + 64 < a.n_out) *reinterpret_cast<float4*>(y + fg + 64) = hi;
         }
       } else if (EPI == EPI_SWIGLU) {
         const int j = tile * 64 + fa;  // hidden unit: gate at tile feature fa, up at fa + 64
@@ -551,7 +581,7 @@ int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p
   if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return DF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_tiles, p.splits, 1);
+  cfg.gridDim = dim3(p.n_tiles, p.splits, p.a.n_groups > 0 ? p.a.n_groups : 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -574,15 +604,17 @@ int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p
 
 }  // namespace
 
-int gemm_tiles(int n_out, int epi) { return epi == EPI_SWIGLU ? n_out / 64 : (n_out + kGemmTileN - 1) / kGemmTileN; }
+int gemm_tiles(int n_out, int epi) {
+  return (epi == EPI_SWIGLU || epi == EPI_MOE_GATEUP) ? n_out / 64 : (n_out + kGemmTileN - 1) / kGemmTileN;
+}
 
 // Reduction splits (cluster size): the smallest power of two, at most 8, that gives every SM a
 // tile slice, with at least 2 k-blocks per CTA. Depends only on the weight shape and the context's
 // capacity, never on which flows are present. A split CTA holds its partial tile and the S
 // received slices at once (1 KB per padded activation row), so contexts with more than 208 rows
 // of capacity do not split.
-int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi) {
-  const int tiles = gemm_tiles(n_out, epi);
+int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups) {
+  const int tiles = gemm_tiles(n_out, epi) * groups;
   const int kb = k / kGemmTileK;
   const int max_rows = ((2 * ctx->cfg.max_batch + 15) / 16) * 16;
   if (max_rows > kSplitMaxRows) return 1;
@@ -595,23 +627,29 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   const int m = a.m_p + a.m_a;
   if (m <= 0) return DF_OK;
   if (m > kGemmMaxAct || m > 2 * ctx->cfg.max_batch || a.k % kGemmTileK != 0 || a.k <= 0) return DF_ERR_SHAPE;
-  if (a.epi == EPI_SWIGLU && a.n_out % 64 != 0) return DF_ERR_SHAPE;
+  if ((a.epi == EPI_SWIGLU || a.epi == EPI_MOE_GATEUP) && a.n_out % 64 != 0) return DF_ERR_SHAPE;
+  const int groups = a.n_groups > 0 ? a.n_groups : 1;
+  if ((a.epi == EPI_MOE_GATEUP || a.epi == EPI_MOE_DOWN) && (!a.sel_pos || a.n_groups <= 0)) return DF_ERR_ARG;
+  if (a.epi == EPI_MOE_DOWN && a.n_out % 4 != 0) return DF_ERR_SHAPE;
   if (a.g_next != nullptr && (a.n_out % 64 != 0 || !a.x_next || !a.ss_out)) return DF_ERR_ARG;
   GemmParams p;
   p.a = a;
   p.n_pad = ((m + 15) / 16) * 16;
   p.kb_total = a.k / kGemmTileK;
   p.n_tiles = gemm_tiles(a.n_out, a.epi);
-  p.splits = gemm_splits(ctx, a.n_out, a.k, a.epi);
+  p.splits = gemm_splits(ctx, a.n_out, a.k, a.epi, groups);
   p.status = ctx->status;
-  const uintptr_t align = (a.epi == EPI_STORE_BF16 || a.epi == EPI_SWIGLU) ? 8 : 16;
+  const uintptr_t align = (a.epi == EPI_STORE_BF16 || a.epi == EPI_SWIGLU || a.epi == EPI_MOE_GATEUP) ? 8 : 16;
   p.vec_ok = a.y != nullptr && (reinterpret_cast<uintptr_t>(a.y) % align == 0) && (a.ldy % 4 == 0) ? 1 : 0;
   if (a.g_next != nullptr && !p.vec_ok) return DF_ERR_ARG;
-  const uint64_t w_rows = (a.epi == EPI_SWIGLU) ? 2ull * a.n_out : (uint64_t)a.n_out;
+  uint64_t w_rows = (a.epi == EPI_SWIGLU || a.epi == EPI_MOE_GATEUP) ? 2ull * a.n_out : (uint64_t)a.n_out;
+  if (groups > 1) w_rows = (uint64_t)groups * a.w_group_rows;
+  const uint64_t x_rows = (groups > 1 && a.x_group_rows > 0) ? (uint64_t)groups * a.x_group_rows : (uint64_t)m;
+  if (groups > 1 && a.x_group_rows > 0 && a.x_group_rows < m) return DF_ERR_ARG;
   CUtensorMap mw, mx;
   int rc = encode_map_2d_bf16(&mw, a.W, (uint64_t)a.k, w_rows, (uint64_t)a.k * 2, kGemmTileK, 64);
   if (rc != DF_OK) return rc;
-  rc = encode_map_2d_bf16(&mx, a.x, (uint64_t)a.k, (uint64_t)m, (uint64_t)a.k * 2, kGemmTileK, (uint32_t)p.n_pad);
+  rc = encode_map_2d_bf16(&mx, a.x, (uint64_t)a.k, x_rows, (uint64_t)a.k * 2, kGemmTileK, (uint32_t)p.n_pad);
   if (rc != DF_OK) return rc;
   // data region: the pipeline stages; after the main loop the partial tile (512 B per activation
   // row) or, when split, the staged slices plus the receive area (1 KB per row + bank pads). Then
@@ -628,6 +666,8 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
     case EPI_QKV: return launch_epi<EPI_QKV>(mw, mx, p, smem, s);
     case EPI_Q2: return launch_epi<EPI_Q2>(mw, mx, p, smem, s);
     case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(mw, mx, p, smem, s);
+    case EPI_MOE_GATEUP: return launch_epi<EPI_MOE_GATEUP>(mw, mx, p, smem, s);
+    case EPI_MOE_DOWN: return launch_epi<EPI_MOE_DOWN>(mw, mx, p, smem, s);
     default: return DF_ERR_ARG;
   }
 }

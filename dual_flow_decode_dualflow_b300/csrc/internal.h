@@ -32,6 +32,8 @@ enum GemmEpi : int {
   EPI_QKV = 4,        // query coupling a, RoPE, q store, primary K/V append
   EPI_Q2 = 5,         // attention-only: q2 = acc + a (*) q1, RoPE of q1 and q2
   EPI_SWIGLU = 6,     // u = silu(gate) (*) up, u2 += b (*) u1, bf16 store
+  EPI_MOE_GATEUP = 7, // per expert: SWIGLU for the rows that selected it, u2 += b (*) u1 if both did
+  EPI_MOE_DOWN = 8,   // per expert: fp32 store of the rows that selected it
 };
 
 struct GemmArgs {
@@ -69,6 +71,12 @@ struct GemmArgs {
   void* x_next;
   float* ss_out;
   int pdl;  // launch with programmatic dependent launch (weights prefetched before the wait)
+  // Grouped (MoE) launch: grid z = n_groups experts. Expert e's weight rows start at row
+  // e * w_group_rows of W, its activation rows at row e * x_group_rows of x (0: shared x), its
+  // output at y + e * y_group_stride elements; sel_pos[row * n_groups + e] >= 0 when row uses e.
+  int n_groups, w_group_rows, x_group_rows;
+  size_t y_group_stride;
+  const int32_t* sel_pos;
 };
 
 struct AttnArgs {
@@ -115,6 +123,13 @@ struct dualflow_ctx {
   void* u = nullptr;               // [2 * max_batch, F]
   float* raw = nullptr;            // fp32 path: [2 * max_batch, max_n] projection scratch
   float* ss = nullptr;             // [2 * max_batch][ss_ld] per-row partial sums of squares (bf16)
+  // MoE (bf16): router logits, routing decision, expert intermediates and outputs, expert ids
+  float* rlog = nullptr;           // [2 * max_batch][E]
+  int32_t* sel_pos = nullptr;      // [2 * max_batch][E] position in the row's expert set, -1 if unused
+  float* sel_w = nullptr;          // [2 * max_batch][E] mixing weight
+  void* moe_u = nullptr;           // [E][2 * max_batch][F] bf16
+  float* moe_y = nullptr;          // [E][2 * max_batch][d]
+  int32_t* moe_ids = nullptr;      // [n_layers][2][max_batch][kmax] experts chosen by the last step
   int ss_ld = 0;                   // ceil(d / 128) tiles x 8 splits
   int32_t* tokens_dev = nullptr;   // dualflow_step_host staging
   float* logits_dev = nullptr;
@@ -137,7 +152,7 @@ int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 
 // Launchers (return dualflow_status).
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s);
-int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi);
+int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups = 1);
 int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl = 0);
 // The same kernel with caller-chosen workspace: split partials (>= pairs + ctas slots of
 // kAttnPartFloats), per-pair merge counters (zero on entry), the status word, and a grid of `ctas`
@@ -152,6 +167,13 @@ int launch_embed_prep(dualflow_ctx* ctx, const void* E1, const void* E2, const i
                       int batch, int aux_on, cudaStream_t s);
 // The same from the residual h (bf16): x = bf16(h (*) g); ss[row] = sum h^2 (one partial).
 int launch_norm_prep(dualflow_ctx* ctx, float* h, const void* g, int batch, int aux_on, cudaStream_t s);
+// MoE: routing decision from ctx->rlog (ids [2][batch][kmax], nullable), and the combine of the
+// experts' outputs with output coupling and residual (g_next set: also the next norm's operand,
+// ceil(d / 512) partial sums of squares per row).
+int launch_moe_route(dualflow_ctx* ctx, const float* rlog, int batch, int aux_on, int32_t* ids, cudaStream_t s,
+                     int pdl);
+int launch_moe_combine(dualflow_ctx* ctx, float* h, int batch, int aux_on, const void* c_vec, const void* g_next,
+                       cudaStream_t s, int pdl);
 int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s);
 int launch_rope_q1(dualflow_ctx* ctx, const void* q1, void* q, const int32_t* seq_len, int batch, cudaStream_t s);
 

@@ -134,7 +134,8 @@ typedef struct {
 /* Creates a context for `cfg` on the current CUDA device and allocates its workspace.
  * Host-validates the config (DF_ERR_ARG / DF_ERR_SHAPE / DF_ERR_DTYPE before touching the GPU).
  * bf16 kernels need head_dim == 128, Hq / Hkv <= 4, d_model, ffn_hidden and Hq*head_dim
- * multiples of 64 (else DF_ERR_UNSUPPORTED). On failure *out is set to NULL. */
+ * multiples of 64, max_batch <= 128 and n_experts <= 32 (else DF_ERR_UNSUPPORTED); MoE models
+ * need bf16 storage. On failure *out is set to NULL. */
 DF_API int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out);
 
 /* Releases the context and its workspace. NULL-safe. Synchronizes the device first. */
@@ -182,6 +183,12 @@ DF_API int dualflow_stacked_linear(dualflow_ctx* ctx, const void* x, int32_t m_p
  * each row in descending router logit order (ties to the lower index), -1 padded. */
 DF_API int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int32_t layer, int32_t batch,
                          int32_t aux_on, int32_t* expert_ids_out, dualflow_stream stream);
+
+/* Experts chosen in every layer by the last dualflow_step of this context (MoE models only, else
+ * DF_ERR_UNSUPPORTED): copies [n_layers, 2, batch, max(k_primary, k_aux)] int32 into the device
+ * buffer ids (row order as expert_ids_out of dualflow_coupled_mlp; flow-1 rows are -1 when the
+ * step ran with aux_on = 0). batch must equal the step's batch. Asynchronous on `stream`. */
+DF_API int dualflow_expert_ids(dualflow_ctx* ctx, int32_t* ids, int32_t batch, dualflow_stream stream);
 
 /* One whole decode step of both flows: embeddings E1[tok], E2[tok] -> n_layers x {RMSNorm,
  * QKV with query coupling, RoPE and primary-only KV append, shared-KV attention, O projection,
