@@ -1,14 +1,16 @@
 #!/usr/bin/env python
-"""Dual-flow decode benchmark on B300: tokens/s of the whole decode step and achieved HBM bandwidth.
+"""Dual-flow decode benchmark on B300: tokens/s of the decode step and achieved HBM bandwidth.
 
-Workload: the 24-layer dense dual-flow model (d_model 2048, 16/4 heads of 128, SwiGLU 8192, vocab
-32000), batch 32, every sequence with 4096 cached positions, bf16 storage / fp32 accumulation,
-synthetic seeded inputs generated in place. One step = one decode step of both flows for the
-whole batch (embeddings -> 24 x {RMSNorm, QKV + query coupling + RoPE + KV append, shared-KV
-attention, O projection, RMSNorm, gate/up + SwiGLU + b coupling, down + c coupling} -> final
-RMSNorm -> LM head), replayed as one CUDA graph through dualflow_step.
+Default workload (--workload dense): the 24-layer dense dual-flow model (d_model 2048, 16/4 heads
+of 128, SwiGLU 8192, vocab 32000), batch 32, every sequence with 4096 cached positions, bf16
+storage / fp32 accumulation, synthetic seeded inputs generated in place. One step = one decode
+step of both flows for the whole batch (embeddings -> 24 x {QKV + query coupling + RoPE + KV
+append, shared-KV attention, O projection, gate/up + SwiGLU + b coupling, down + c coupling, with
+RMSNorm carried between them} -> LM head), replayed as one CUDA graph through dualflow_step.
+Other workloads: moe (16 layers, 16 experts, top-2 / top-4, batch 64), attn (attention-only layer,
+batch 8, 2048 positions), paged (attention-only layer, batch 64, ragged 1k-32k positions, paged).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
 
 Under torchrun every rank runs its own replica (independent sequences: no data-path collective);
 value = total tokens of all ranks / max-over-ranks step time. --impl reference times the CPU
@@ -24,6 +26,8 @@ import statistics
 import subprocess
 import sys
 import time
+
+import numpy as np
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -43,19 +47,27 @@ def load_peaks() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def workload():
+def workload(name: str = "dense"):
     from dfsynth import workloads as W
-    return W.DENSE_24L_B32_L4096
+    return {"dense": W.DENSE_24L_B32_L4096, "moe": W.MOE_16L_B64, "attn": W.ATTN_B8_L2048,
+            "paged": W.PAGED_RAGGED_B64}[name]
 
 
-def step_bytes(w) -> dict:
-    """Algorithmic HBM bytes of one step: every weight once, every cached K1/V1 element once, the
-    appended entries, the gathered embedding rows and the fp32 logits."""
+def step_bytes(w, experts_touched=None) -> dict:
+    """Algorithmic HBM bytes of one step: every weight once (for MoE, the router and the experts
+    some row selected, counted per layer), every cached K1/V1 element once, the appended entries,
+    the gathered embedding rows and the fp32 logits."""
     from dfsynth import workloads as W
     es = 2 if w.dtype == "bf16" else 4
     weights = sum(s.numel for s in W.global_specs(w) if s.name in ("W_lm", "g_final")) * es
     for l in range(w.n_layers):
-        weights += sum(s.numel for s in W.layer_specs(w, l) if not s.name.endswith((".K", ".V"))) * es
+        for spec in W.layer_specs(w, l):
+            if spec.name.endswith((".K", ".V")):
+                continue
+            n = spec.numel
+            if spec.name.endswith((".We_gu", ".We_d")) and experts_touched is not None:
+                n = n // w.n_experts * int(experts_touched[l])
+            weights += n * es
     lens = w.seq_lens()
     kv_per_pos = w.n_kv_heads * w.head_dim * es * 2  # K and V
     kv_read = int(lens.sum()) * kv_per_pos * w.n_layers
@@ -67,6 +79,18 @@ def step_bytes(w) -> dict:
     attn = int((lens + 1).sum()) * kv_per_pos + 2 * qo
     return dict(total=weights + kv_read + kv_write + emb + logits, weights=weights, kv_read=kv_read,
                 kv_write=kv_write, attention_per_launch=attn)
+
+
+def call_bytes(w) -> dict:
+    """Algorithmic HBM bytes of one attention-only call: Wq once, K1/V1 of the cached positions
+    once, q1 and h2 read, both flows' outputs written."""
+    es = 2
+    lens = w.seq_lens()
+    kv = int(lens.sum()) * w.n_kv_heads * w.head_dim * es * 2
+    wq = w.q_dim * w.d_model * es
+    act = (w.batch * w.q_dim + w.batch * w.d_model + w.q_dim) * es
+    out = 2 * w.batch * w.q_dim * es
+    return dict(total=kv + wq + act + out, kv_read=kv, weights=wq)
 
 
 def attention_traffic() -> float | None:
@@ -193,26 +217,195 @@ def blas_threads() -> int:
         return 1
 
 
+class AttentionOracleSample:
+    """The CPU oracle's attention-only call on a bounded sample of the sequences of the workload,
+    inputs drawn and widened beforehand (only the oracle's arithmetic is timed)."""
+
+    def __init__(self, w, rows):
+        import oracle as O
+        from tests import gpu_harness as H
+        self.O, self.w, self.rows = O, w, list(rows)
+        self.hp = H.hparams(w)
+        self.q1, self.h2 = H.host_f64(w, "q1"), H.host_f64(w, "h2")
+        self.Wq, self.a = H.host_f64(w, "Wq"), H.host_f64(w, "a")
+        self.lens = w.seq_lens()
+        if w.paged:
+            table, _ = w.page_table()
+            kp, vp = H.LazyPages(w, "K"), H.LazyPages(w, "V")
+            pids = {int(table[b, j]) for b in self.rows for j in range(-(-int(self.lens[b]) // w.page_size))}
+            self.cache = O.PagedCache({p: kp[p] for p in pids}, {p: vp[p] for p in pids}, table, w.page_size)
+        else:
+            kc, vc = H.LazySeqCache(w, "K"), H.LazySeqCache(w, "V")
+            self.cache = O.DenseCache({b: kc[b] for b in self.rows}, {b: vc[b] for b in self.rows})
+
+    def time_rows(self, rows) -> float:
+        t0 = time.perf_counter()
+        self.O.attention_only_step(self.hp, self.q1, self.h2, self.Wq, self.a, self.cache, self.lens, aux_on=True,
+                                   mirror=True, rows=rows)
+        return time.perf_counter() - t0
+
+    def full_call(self, seconds: float, rows) -> float:
+        # cost grows with the cached positions attended: scale by the workload's total over the sample's
+        return seconds * float(self.lens.sum()) / float(sum(int(self.lens[b]) for b in rows))
+
+    def describe(self, rows) -> str:
+        return (f"oracle (numpy fp64) attention-only call of both flows on sequences {list(rows)} of {self.w.batch} "
+                f"(inputs drawn beforehand), scaled to the full call by cached positions")
+
+
 def run_reference(args, w) -> dict:
     """The reference arm: the CPU oracle, as it stands, on a bounded sample per step (one sequence,
-    rotating through the batch, over the first layer and the LM head)."""
-    rows = list(range(min(8, w.batch)))
-    samp = OracleSample(w, rows, 1)
+    rotating through the batch, over the first layer and the LM head; for an attention-only
+    workload, one sequence's attention call)."""
     per = []
-    for i in range(args.warmup + args.steps):
-        t = samp.time_step([rows[i % len(rows)]])
-        if i >= args.warmup:
-            per.append(samp.full_step(t, 1))
-    desc = samp.describe(1)
+    if w.kind == "attention":
+        lens = w.seq_lens()
+        order = [int(b) for b in np.argsort(lens)[: max(1, min(8, w.batch))]]  # the shortest: bounded time
+        samp = AttentionOracleSample(w, order)
+        for i in range(args.warmup + args.steps):
+            rows = [order[i % len(order)]]
+            t = samp.time_rows(rows)
+            if i >= args.warmup:
+                per.append(samp.full_call(t, rows))
+        desc = samp.describe(order)
+    else:
+        rows = list(range(min(8, w.batch)))
+        samp = OracleSample(w, rows, 1)
+        for i in range(args.warmup + args.steps):
+            t = samp.time_step([rows[i % len(rows)]])
+            if i >= args.warmup:
+                per.append(samp.full_step(t, 1))
+        desc = samp.describe(1)
     s = statistics.median(per)
     value = w.batch / s
     cores = blas_threads()
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    unit = "tokens/s" if w.kind == "step" else "sequence-steps/s (one layer)"
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx_len, "layers": w.n_layers},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx_len or f"{w.ctx_lo}-{w.ctx_hi}",
+                       "layers": w.n_layers},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict | None:
+    """Attention-only workloads: one step = one dualflow_decode_attention call for the batch (the
+    auxiliary query projection with coupling and RoPE, then the shared-KV attention). Inputs are
+    rotated over enough copies that the working set of a round exceeds L2 three times over; the
+    round of calls is replayed as a CUDA graph."""
+    import torch
+
+    import dual_flow_decode_dualflow_b300 as dfl
+    from tests import gpu_harness as H
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = torch.distributed if world > 1 else None
+    nb = call_bytes(w)
+    copies = max(1, min(16, -(-3 * 126 * 2 ** 20 // nb["total"])))
+    runs = [H.DeviceRun(w, dev) for _ in range(copies)]
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for r in runs:
+                r.attention(aux_on=1, stream=stream)
+    stream.synchronize()
+    for r in runs:
+        st = dfl.dualflow_sync_status(r.ctx)
+        if st != 0:
+            raise RuntimeError(f"device status: {dfl.dualflow_status_string(st)}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        for r in runs:
+            r.attention(aux_on=1, stream=stream)
+    rounds = max(1, args.steps // copies)
+    steps = rounds * copies
+
+    def timed(sampler=None):
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup // copies)):
+                graph.replay()
+        stream.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with (sampler if sampler is not None else _Null()):
+            if sampler is not None:
+                sampler.mark(True)
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                for _ in range(rounds):
+                    graph.replay()
+                e1.record(stream)
+            e1.synchronize()
+            if sampler is not None:
+                sampler.mark(False)
+        ms = e0.elapsed_time(e1) / steps
+        if dist:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    ms = timed(sampler)
+    # end to end: q1 and h2 from pinned host memory, the call, o back to host, every step
+    r0 = runs[0]
+    q1_h = r0.t["q1"].cpu().pin_memory()
+    h2_h = r0.t["h2"].cpu().pin_memory()
+    o_h = torch.empty(r0.o.shape, dtype=r0.o.dtype).pin_memory()
+    e2e_steps = max(min(args.steps, 200), 3)
+    for i in range(3 + e2e_steps):
+        if i == 3:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            r0.t["q1"].copy_(q1_h, non_blocking=True)
+            r0.t["h2"].copy_(h2_h, non_blocking=True)
+            r0.attention(aux_on=1, stream=stream)
+            o_h.copy_(r0.o, non_blocking=True)
+        stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    graph.reset()
+    for r in runs:
+        r.close()
+    if rank != 0:
+        return None
+    peak, peak_kind = load_peaks()
+    gbs = nb["total"] / (ms * 1e-3) / 1e9
+    lens = w.seq_lens()
+    rows = [int(b) for b in np.argsort(lens)[:2]]
+    samp = AttentionOracleSample(w, rows)
+    cpu_s = samp.full_call(samp.time_rows(rows), rows)
+    unit = "sequence-steps/s (one layer)"
+    return {
+        "metric": METRIC, "value": world * w.batch / (ms * 1e-3), "unit": unit, "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
+        "data": "synthetic: seeded counter-hash generator, random-init weights of the workload's shapes",
+        "config": {"workload": w.name, "d_model": w.d_model, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads,
+                   "head_dim": w.head_dim, "batch_per_gpu": w.batch,
+                   "ctx": w.ctx_len or f"uniform {w.ctx_lo}-{w.ctx_hi}", "paged": w.paged,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"{copies} rotated input copies, {copies * nb['total'] / 1e6:.0f} MB per round vs 126 MB L2",
+                   "launch": "round of calls replayed as a CUDA graph"},
+        "hbm": {"call_bytes": nb["total"], "achieved_gbs": gbs, "frac_of_8000": gbs / NOMINAL_HBM_GBS,
+                f"frac_of_{peak_kind}": gbs / peak},
+        "roofline": {"kernel": "dualflow_decode_attention call (Q2 projection + shared-KV attention)",
+                     "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_kind": f"{peak_kind} copy bandwidth", "bytes_per_launch": nb["total"],
+                     "avg_launch_ms": ms, "traffic": None},
+        "cpu_baseline": {"value": w.batch / cpu_s, "unit": unit, "cores": blas_threads(), "kind": "oracle",
+                         "sample": samp.describe(rows)},
+        "e2e": {"value": world * w.batch / e2e_s, "unit": unit,
+                "h2d_bytes_per_step": int((q1_h.numel() + h2_h.numel()) * 2), "d2h_bytes_per_step": int(o_h.numel() * 2),
+                "api": "dualflow_decode_attention with q1, h2 copied from pinned host memory and o copied back, "
+                       "stream sync per step"},
+        "gpu_launches": 2 * steps, "launches_per_step": 2,
+        "clocks": sampler.summary(),
+    }
 
 
 def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
@@ -263,6 +456,13 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     st = dfl.dualflow_sync_status(run.ctx)
     if st != 0:
         raise RuntimeError(f"device status after the timed steps: {dfl.dualflow_status_string(st)}")
+    experts_touched = None
+    if w.n_experts > 0:  # distinct experts each layer's rows selected (their weights are read)
+        kmax = max(w.topk_primary, w.topk_aux)
+        ids = torch.empty((w.n_layers, 2, w.batch, kmax), dtype=torch.int32, device=dev)
+        dfl.dualflow_expert_ids(run.ctx, ids, w.batch, stream)
+        stream.synchronize()
+        experts_touched = [len(set(x for x in ids[l].flatten().tolist() if x >= 0)) for l in range(w.n_layers)]
     _, launches = dfl.dualflow_profile_read(run.ctx)
     if args.quick:
         run.close()
@@ -308,7 +508,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         return None
 
     peak, peak_kind = load_peaks()
-    nb = step_bytes(w)
+    nb = step_bytes(w, experts_touched)
     step_gbs = nb["total"] / (ms * 1e-3) / 1e9
     att_ms = fam_ms[dfl.PROF_NAMES.index("attention")] / max(fam_n[dfl.PROF_NAMES.index("attention")], 1)
     att_gbs = nb["attention_per_launch"] / (att_ms * 1e-3) / 1e9
@@ -325,6 +525,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         "config": {"workload": w.name, "layers": w.n_layers, "d_model": w.d_model, "q_heads": w.n_q_heads,
                    "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "ffn_hidden": w.ffn_hidden,
                    "vocab": w.vocab, "batch_per_gpu": w.batch, "ctx": w.ctx_len,
+                   "experts": w.n_experts, "topk": [w.topk_primary, w.topk_aux],
+                   "experts_touched_per_layer": experts_touched,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {nb['total'] / 1e9:.2f} GB per step vs 126 MB L2, no flush"},
         "hbm": {"step_bytes": nb["total"], "achieved_gbs": step_gbs, "frac_of_8000": step_gbs / NOMINAL_HBM_GBS,
@@ -365,9 +567,10 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: run the workload with this many layers")
     ap.add_argument("--quick", action="store_true", help="profiling captures only: time the step, skip the rest")
+    ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged"], default="dense")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
-    w = workload()
+    w = workload(args.workload)
     if args.layers:
         w = w.replace(n_layers=args.layers)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -382,7 +585,10 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    res = run_ours(args, w, rank, world, local_rank)
+    if w.kind == "attention":
+        res = run_ours_attention(args, w, rank, world, local_rank)
+    else:
+        res = run_ours(args, w, rank, world, local_rank)
     if res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:
