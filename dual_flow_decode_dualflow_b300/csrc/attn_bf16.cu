@@ -14,7 +14,9 @@
 // Work split (flash-decoding): all (b, g, tile) triples are laid end to end and cut into equal
 // contiguous ranges, one per CTA, so ragged lengths balance across the GPU. A pair cut across
 // several CTAs writes per-CTA partials (O, max, sum); the last CTA to arrive (atomic counter, no
-// waiting) merges them in CTA order, so the result does not depend on arrival order.
+// waiting) merges them in CTA order, with all four consumer warps, so the result does not depend
+// on arrival order. The query rows of a pair reach shared memory by bulk copy with the pair's
+// first tile.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -27,12 +29,13 @@ constexpr int kAttnThreads = (kConsumers + 1) * 32;
 constexpr int kHalf = kAttnTileKeys * 128;   // 64 keys x 64 dims x 2 B = 8 KB (one swizzled box)
 constexpr int kTileBytes = 2 * kHalf;         // K (or V) tile: 16 KB
 constexpr int kStageBytes = 2 * kTileBytes;   // K + V: 32 KB
-constexpr int kMergeFloats = 36 * 32;         // per warp: m0, m1, l0, l1, o[32] for 32 lanes
+constexpr int kQBytes = kMaxGroupRows * kHeadDim * 2;  // both flows' query rows of one group: 2 KB
+constexpr int kMergeFloats = 36 * 32;         // one warp's state: m0, m1, l0, l1, o[32] for 32 lanes
 
 struct AttnParams {
   AttnArgs a;
-  float* part;
-  int32_t* cnt;
+  float* part;       // partial slots [pairs + CTAs][kAttnPartFloats]
+  int32_t* cnt;      // [pairs] CTAs done with each pair (zero between launches)
   int32_t* status;
   float scale_log2;  // log2(e) / sqrt(D)
 };
@@ -87,6 +90,14 @@ __device__ __forceinline__ int owner_of(long long t, long long T, int C) { retur
 
 __device__ __forceinline__ uint32_t swz(int key, int chunk) { return (uint32_t)(key * 128 + ((chunk ^ (key & 7)) << 4)); }
 
+// Global -> shared bulk copy (16-byte aligned, size a multiple of 16), completion on an mbarrier.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid_constant__ CUtensorMap map_k,
                                                                      const __grid_constant__ CUtensorMap map_v,
                                                                      const AttnParams P) {
@@ -94,10 +105,11 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const AttnArgs& a = P.a;
   const int B = a.batch, Hkv = a.n_kv_heads, Hq = a.n_q_heads, G = Hq / Hkv;
-  float* mbuf = reinterpret_cast<float*>(smem + kStagesA * kStageBytes);      // 2 x kMergeFloats
-  uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + 2 * kMergeFloats);
+  uint8_t* qbuf = smem + kStagesA * kStageBytes;                           // [kStagesA][kQBytes]
+  float* mbuf = reinterpret_cast<float*>(qbuf + kStagesA * kQBytes);       // [kMergeFloats]
+  uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + kMergeFloats);
   uint64_t* empty = full + kStagesA;
-  volatile int* err = reinterpret_cast<volatile int*>(empty + kStagesA);
+  volatile int* err = reinterpret_cast<volatile int*>(empty + kStagesA);  // [0] error, [1] merge here
   int* sched = const_cast<int*>(err) + 4;  // [B + 1] exclusive prefix of tiles
   int* lens = sched + B + 1;                // [B] attended positions of each sequence
 
@@ -109,23 +121,21 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumers);
     }
-    *err = 0;
-    int acc = 0;
-    for (int b = 0; b < B; ++b) {
-      sched[b] = acc;
-      // seq_len is an input of the call, never written by the preceding kernel: read before the
-      // programmatic wait
-      const int L = a.seq_len[b] + a.extra;
-      int tb = (L + kAttnTileKeys - 1) / kAttnTileKeys;
-      if (L < 0 || L > a.max_ctx) {  // out-of-range length: skip the sequence, report it
-        set_status(P.status, DF_ERR_DEVICE_BOUNDS);
-        tb = 0;
-      }
-      lens[b] = L;
-      acc += tb * Hkv;
-    }
-    sched[B] = acc;
+    err[0] = 0;
     fence_mbar_init();
+  }
+  // seq_len is an input of the call, never written by the preceding kernel: read before the
+  // programmatic wait. lens[b] holds the attended positions, sched the prefix of tiles.
+  for (int b = threadIdx.x; b < B; b += kAttnThreads) {
+    const int L = a.seq_len[b] + a.extra;
+    lens[b] = (L < 0 || L > a.max_ctx) ? -1 : L;  // out-of-range length: skip the sequence, report it
+    if (L < 0 || L > a.max_ctx) set_status(P.status, DF_ERR_DEVICE_BOUNDS);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b <= B; b += kAttnThreads) {
+    int acc = 0;
+    for (int j = 0; j < b; ++j) acc += lens[j] > 0 ? (lens[j] + kAttnTileKeys - 1) / kAttnTileKeys * Hkv : 0;
+    sched[b] = acc;
   }
   __syncthreads();
   griddep_launch_dependents();
@@ -141,12 +151,23 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
       const uint64_t pol = policy_evict_first();
+      const int nf = a.aux_on ? 2 : 1;
+      const uint32_t qbytes = (uint32_t)(nf * G * kHeadDim * 2);
       Walker w;
       walker_seek(w, sched, B, Hkv, (int)t0);
       // Under programmatic dependent launch the first stages' tiles are requested before waiting
       // for the preceding kernel, unless they hold the slot that kernel appends (seq_len[b] when
-      // extra = 1): the older cache positions are never written by it.
+      // extra = 1): the older cache positions are never written by it. The query rows of a
+      // segment (written by the preceding kernel) follow the wait; they land in the query area of
+      // the stage that holds the segment's first tile, not refilled before the consumers read them.
       bool waited = false;
+      int pend_s[kStagesA], pend_b[kStagesA], pend_g[kStagesA], npend = 0;
+      auto issue_q = [&](int s, int b, int g) {
+        for (int f = 0; f < nf; ++f)
+          bulk_load(qbuf + s * kQBytes + f * G * kHeadDim * 2,
+                    reinterpret_cast<const __nv_bfloat16*>(a.q) + (((size_t)f * B + b) * Hq + g * G) * kHeadDim,
+                    (uint32_t)(G * kHeadDim * 2), &full[s]);
+      };
       for (long long t = t0, i = 0; t < t1; ++t, ++i) {
         const int s = (int)(i % kStagesA);
         const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
@@ -155,13 +176,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
         if (!waited && (i >= kStagesA || (a.extra && key0 + kAttnTileKeys >= Leff))) {
           griddep_wait();
           waited = true;
+          for (int k = 0; k < npend; ++k) issue_q(pend_s[k], pend_b[k], pend_g[k]);
+          npend = 0;
         }
         if (!wait_or_fail(&empty[s], ph ^ 1u, err, P.status)) break;
+        const bool seg_start = (w.j == 0) || (t == t0);
         uint8_t* Kst = smem + s * kStageBytes;
         uint8_t* Vst = Kst + kTileBytes;
         if (!a.paged) {
           const int row = w.b * Hkv + w.g;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes + (seg_start ? qbytes : 0u));
           tma_load_3d_hint(Kst, &map_k, &full[s], 0, key0, row, pol);
           tma_load_3d_hint(Kst + kHalf, &map_k, &full[s], 64, key0, row, pol);
           tma_load_3d_hint(Vst, &map_v, &full[s], 0, key0, row, pol);
@@ -169,7 +193,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
         } else {
           const int ps = a.page_size, npg = kAttnTileKeys / ps;
           int pid[kAttnTileKeys / 16];
-          uint32_t bytes = 0;
+          uint32_t bytes = seg_start ? qbytes : 0u;
           for (int jj = 0; jj < npg; ++jj) {
             const int lp = key0 / ps + jj;
             pid[jj] = -1;
@@ -194,9 +218,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
             tma_load_3d_hint(Vst + kHalf + off, &map_v, &full[s], 64, 0, row, pol);
           }
         }
+        if (seg_start) {
+          if (waited) {
+            issue_q(s, w.b, w.g);
+          } else {
+            pend_s[npend] = s;
+            pend_b[npend] = w.b;
+            pend_g[npend] = w.g;
+            ++npend;
+          }
+        }
         walker_next(w, sched, B, Hkv);
       }
-      if (!waited) griddep_wait();
+      if (!waited) {
+        griddep_wait();
+        for (int k = 0; k < npend; ++k) issue_q(pend_s[k], pend_b[k], pend_g[k]);
+      }
     }
     return;
   }
@@ -231,22 +268,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
   bool new_seg = true;
   for (long long t = t0, i = 0; t < t1; ++t, ++i) {
     const int Leff = lens[w.b];
-    if (new_seg) {
-      // load this group's 2G query rows (primary heads, then auxiliary heads) as B fragments
-      const int f = qn / G, hh = qn % G;
-      const bool valid = (qn < 2 * G) && (f == 0 || a.aux_on);
-      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(a.q);
-      const size_t base = (((size_t)f * B + w.b) * Hq + w.g * G + hh) * kHeadDim;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        qb[kk][0] = valid ? q32[(base + 16 * kk + q0) >> 1] : 0u;
-        qb[kk][1] = valid ? q32[(base + 16 * kk + 8 + q0) >> 1] : 0u;
-      }
-      new_seg = false;
-    }
     const int s = (int)(i % kStagesA);
     const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
     const bool ok = wait_or_fail(&full[s], ph, err, P.status);
+    if (new_seg) {
+      // this group's 2G query rows (primary heads, then auxiliary heads) as B fragments, from the
+      // stage's query area
+      const int f = qn / G;
+      const bool valid = ok && (qn < 2 * G) && (f == 0 || a.aux_on);
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qbuf + s * kQBytes + qn * kHeadDim * 2);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        qb[kk][0] = valid ? q32[(16 * kk + q0) >> 1] : 0u;
+        qb[kk][1] = valid ? q32[(16 * kk + 8 + q0) >> 1] : 0u;
+      }
+      new_seg = false;
+    }
     const int key0 = w.j * kAttnTileKeys;
     const int valid = Leff - key0;
     const uint32_t Kb = sbase + s * kStageBytes, Vb = Kb + kTileBytes;
@@ -340,20 +377,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
         l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
         l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
       }
-      auto put = [&](float* buf) {
-        buf[0 * 32 + lane] = m[0];
-        buf[1 * 32 + lane] = m[1];
-        buf[2 * 32 + lane] = l[0];
-        buf[3 * 32 + lane] = l[1];
+      auto put = [&]() {
+        mbuf[0 * 32 + lane] = m[0];
+        mbuf[1 * 32 + lane] = m[1];
+        mbuf[2 * 32 + lane] = l[0];
+        mbuf[3 * 32 + lane] = l[1];
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) buf[(4 + mt * 4 + r) * 32 + lane] = o[mt][r];
+          for (int r = 0; r < 4; ++r) mbuf[(4 + mt * 4 + r) * 32 + lane] = o[mt][r];
       };
-      auto merge = [&](const float* buf) {
+      auto merge = [&]() {
 #pragma unroll
         for (int qq = 0; qq < 2; ++qq) {
-          const float mb = buf[qq * 32 + lane], lb = buf[(2 + qq) * 32 + lane];
+          const float mb = mbuf[qq * 32 + lane], lb = mbuf[(2 + qq) * 32 + lane];
           const float M = fmaxf(m[qq], mb);
           const float sa = (M == NEG_INF) ? 0.f : exp2f(m[qq] - M);
           const float sb = (M == NEG_INF) ? 0.f : exp2f(mb - M);
@@ -361,40 +398,45 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
           m[qq] = M;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            o[mt][qq] = o[mt][qq] * sa + buf[(4 + mt * 4 + qq) * 32 + lane] * sb;
-            o[mt][qq + 2] = o[mt][qq + 2] * sa + buf[(4 + mt * 4 + qq + 2) * 32 + lane] * sb;
+            o[mt][qq] = o[mt][qq] * sa + mbuf[(4 + mt * 4 + qq) * 32 + lane] * sb;
+            o[mt][qq + 2] = o[mt][qq + 2] * sa + mbuf[(4 + mt * 4 + qq + 2) * 32 + lane] * sb;
           }
         }
       };
-      named_bar_sync(1, kConsumers * 32);
-      if (warp >= 2) put(mbuf + (warp - 2) * kMergeFloats);
-      named_bar_sync(1, kConsumers * 32);
-      if (warp < 2) merge(mbuf + warp * kMergeFloats);
-      named_bar_sync(1, kConsumers * 32);
-      if (warp == 1) put(mbuf);
-      named_bar_sync(1, kConsumers * 32);
-      if (warp == 0 && !*err) {
-        const int p = w.b * Hkv + w.g;
-        const long long pstart = sched[w.b] + (long long)w.g * w.tiles_b;
-        const int first = owner_of(pstart, T, C), last = owner_of(pstart + w.tiles_b - 1, T, C);
-        merge(mbuf);
-        __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(a.o);
-        auto store = [&](float (&acc)[8][4], const float (&den)[2]) {
+      // the four warps' states through one buffer: 3 -> 2, 1 -> 0, 2 -> 0
+      constexpr int kBar = 1, kBarThreads = kConsumers * 32;
+      named_bar_sync(kBar, kBarThreads);
+      if (warp == 3) put();
+      named_bar_sync(kBar, kBarThreads);
+      if (warp == 2) merge();
+      named_bar_sync(kBar, kBarThreads);
+      if (warp == 1) put();
+      named_bar_sync(kBar, kBarThreads);
+      if (warp == 0) merge();
+      named_bar_sync(kBar, kBarThreads);
+      if (warp == 2) put();
+      named_bar_sync(kBar, kBarThreads);
+      const int p = w.b * Hkv + w.g;
+      const long long pstart = sched[w.b] + (long long)w.g * w.tiles_b;
+      const int first = owner_of(pstart, T, C), last = owner_of(pstart + w.tiles_b - 1, T, C);
+      __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(a.o);
+      if (warp == 0) {
+        merge();
+        if (first == last) {
+          if (!err[0]) {
 #pragma unroll
-          for (int qq = 0; qq < 2; ++qq) {
-            const int q = q0 + qq, f = q / G, hh = q % G;
-            if (q >= 2 * G || (f == 1 && !a.aux_on)) continue;
-            const float inv = 1.0f / den[qq];
-            const size_t base = (((size_t)f * B + w.b) * Hq + w.g * G + hh) * kHeadDim;
+            for (int qq = 0; qq < 2; ++qq) {
+              const int q = q0 + qq, f = q / G, hh = q % G;
+              if (q >= 2 * G || (f == 1 && !a.aux_on)) continue;
+              const float inv = 1.0f / l[qq];
+              const size_t base = (((size_t)f * B + w.b) * Hq + w.g * G + hh) * kHeadDim;
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              ob[base + 16 * mt + qn] = __float2bfloat16_rn(acc[mt][qq] * inv);
-              ob[base + 16 * mt + qn + 8] = __float2bfloat16_rn(acc[mt][qq + 2] * inv);
+              for (int mt = 0; mt < 8; ++mt) {
+                ob[base + 16 * mt + qn] = __float2bfloat16_rn(o[mt][qq] * inv);
+                ob[base + 16 * mt + qn + 8] = __float2bfloat16_rn(o[mt][qq + 2] * inv);
+              }
             }
           }
-        };
-        if (first == last) {
-          store(o, l);
         } else {
           float* slot = P.part + (size_t)(p + c) * kAttnPartFloats;
 #pragma unroll
@@ -410,39 +452,56 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
             slot[8 * kHeadDim + 8 + q0] = l[0];
             slot[8 * kHeadDim + 8 + q0 + 1] = l[1];
           }
-          __threadfence();
+          // the warp's writes are ordered before lane 0's release of the count
           __syncwarp();
-          int prev = 0;
-          if (lane == 0) prev = atomicAdd(&P.cnt[p], 1);
-          prev = __shfl_sync(0xffffffffu, prev, 0);
-          if (prev == last - first) {
+          if (lane == 0) {
             __threadfence();
-            float M[2] = {NEG_INF, NEG_INF};
-            for (int cc = first; cc <= last; ++cc) {
-              const float* sl = P.part + (size_t)(p + cc) * kAttnPartFloats;
-              M[0] = fmaxf(M[0], __ldcg(sl + 8 * kHeadDim + q0));
-              M[1] = fmaxf(M[1], __ldcg(sl + 8 * kHeadDim + q0 + 1));
-            }
-            float acc[8][4], den[2] = {0.f, 0.f};
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
-            for (int cc = first; cc <= last; ++cc) {
-              const float* sl = P.part + (size_t)(p + cc) * kAttnPartFloats;
-#pragma unroll
-              for (int qq = 0; qq < 2; ++qq) {
-                const float ms = __ldcg(sl + 8 * kHeadDim + q0 + qq);
-                const float sc2 = (M[qq] == NEG_INF) ? 0.f : exp2f(ms - M[qq]);
-                den[qq] += __ldcg(sl + 8 * kHeadDim + 8 + q0 + qq) * sc2;
-#pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                  acc[mt][qq] += __ldcg(sl + (q0 + qq) * kHeadDim + 16 * mt + qn) * sc2;
-                  acc[mt][qq + 2] += __ldcg(sl + (q0 + qq) * kHeadDim + 16 * mt + qn + 8) * sc2;
-                }
-              }
-            }
-            store(acc, den);
-            if (lane == 0) P.cnt[p] = 0;
+            err[1] = (atomicAdd(&P.cnt[p], 1) == last - first) ? 1 : 0;
           }
+        }
+      }
+      if (first != last) {
+        named_bar_sync(kBar, kBarThreads);
+        if (err[1] && !err[0]) {
+          // this CTA finished the pair last: merge the partials of CTAs first..last in CTA order,
+          // 8 dims of one query row per consumer thread
+          __threadfence();
+          const int r = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
+          const float* part0 = P.part + (size_t)(p + first) * kAttnPartFloats;
+          const int n = last - first + 1;
+          float M = NEG_INF;
+#pragma unroll 4
+          for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(part0 + (size_t)k * kAttnPartFloats + 8 * kHeadDim + r));
+          float den = 0.f;
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+          for (int k = 0; k < n; ++k) {
+            const float* sl = part0 + (size_t)k * kAttnPartFloats;
+            const float mv = __ldcg(sl + 8 * kHeadDim + r), lv = __ldcg(sl + 8 * kHeadDim + 8 + r);
+            const float4 v0 = __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0));
+            const float4 v1 = __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0 + 4));
+            const float wt = (M == NEG_INF) ? 0.f : exp2f(mv - M);
+            den += lv * wt;
+            acc[0] += v0.x * wt;
+            acc[1] += v0.y * wt;
+            acc[2] += v0.z * wt;
+            acc[3] += v0.w * wt;
+            acc[4] += v1.x * wt;
+            acc[5] += v1.y * wt;
+            acc[6] += v1.z * wt;
+            acc[7] += v1.w * wt;
+          }
+          const int f = r / G, hh = r % G;
+          if (r < 2 * G && (f == 0 || a.aux_on)) {
+            const float inv = 1.0f / den;
+            uint4 u;
+            u.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            u.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            u.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+            u.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+            *reinterpret_cast<uint4*>(ob + (((size_t)f * B + w.b) * Hq + w.g * G + hh) * kHeadDim + d0) = u;
+          }
+          if (threadIdx.x == 0) P.cnt[p] = 0;
         }
       }
       // reset the running state for the next pair
@@ -461,6 +520,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
 int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl) {
   const dualflow_config& cfg = ctx->cfg;
   if (a.batch <= 0) return DF_OK;
+  if (reinterpret_cast<uintptr_t>(a.q) & 15u) return DF_ERR_ARG;  // bulk copies of query rows
   CUtensorMap mk, mv;
   int rc;
   if (!a.paged) {
@@ -485,7 +545,7 @@ int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, 
   p.cnt = ctx->attn_cnt;
   p.status = ctx->status;
   p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
-  const size_t smem = 1024 + (size_t)kStagesA * kStageBytes + 2 * kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
+  const size_t smem = 1024 + (size_t)kStagesA * (kStageBytes + kQBytes) + kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
                       (size_t)(2 * a.batch + 1) * 4;
   if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
@@ -511,6 +571,7 @@ int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, floa
                              int32_t* status, int ctas, cudaStream_t s) {
   if (a.batch <= 0) return DF_OK;
   if (ctas <= 0 || !part || !cnt || !status) return DF_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(a.q) & 15u) return DF_ERR_ARG;  // bulk copies of query rows
   CUtensorMap mk, mv;
   int rc;
   if (!a.paged) {
@@ -537,7 +598,7 @@ int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, floa
   p.cnt = cnt;
   p.status = status;
   p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
-  const size_t smem = 1024 + (size_t)kStagesA * kStageBytes + 2 * kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
+  const size_t smem = 1024 + (size_t)kStagesA * (kStageBytes + kQBytes) + kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
                       (size_t)(2 * a.batch + 1) * 4;
   if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
       cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)

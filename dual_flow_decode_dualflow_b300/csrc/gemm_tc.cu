@@ -33,7 +33,8 @@
 namespace df {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;                 // most pipeline stages (barrier arrays are sized for it)
+constexpr int kStageBudget = 96 * 1024;    // stage bytes that still let two CTAs share an SM
 constexpr int kThreads = 128;
 constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per stage
 constexpr int kSplitMaxRows = 208;                    // padded activation rows a split CTA can hold
@@ -45,6 +46,7 @@ struct GemmParams {
   int kb_total;  // k / 64
   int n_tiles;
   int vec_ok;    // y / u rows allow 16-byte (fp32) or 8-byte (bf16) vector access
+  int stages;    // pipeline stages in use (2..kStages)
   int region;    // bytes of the data region (pipeline stages, later the partial tiles)
   int32_t* status;
 };
@@ -181,7 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_bytes = p.n_pad * 128;
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
+  const int nst = p.stages;
+  uint8_t* sB = smem + nst * kABytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.region);
   uint64_t* empty = full + kStages;
   uint64_t* done = empty + kStages;
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA producer: weights are streamed once (evict-first), activations stay L2-resident.
     const uint64_t pol_w = policy_evict_first();
     const uint64_t pol_x = policy_evict_last();
-    const int npre = nkb < kStages ? nkb : kStages;
+    const int npre = nkb < nst ? nkb : nst;
     // weights of the first stages do not depend on the preceding kernel: request them first
     for (int i = 0; i < npre; ++i) {
       mbar_arrive_expect_tx(&full[i], (uint32_t)(kABytes + b_bytes));
@@ -259,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < npre; ++i)
       tma_load_2d_hint(sB + i * b_bytes, &map_x, &full[i], (kb0 + i) * kGemmTileK, xrow, pol_x);
     for (int i = npre; i < nkb; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      const int s = i % nst;
+      const uint32_t ph = (uint32_t)(i / nst) & 1u;
       if (!mbar_wait(&empty[s], ph ^ 1u)) {
         set_status(p.status, DF_ERR_TIMEOUT);
         break;
@@ -275,8 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MMA issuer: 4 x (M=128, N=n_pad, K=16) per stage, accumulate in TMEM.
     const uint32_t idesc = idesc_bf16_f32(kGemmTileN, p.n_pad);
     for (int i = 0; i < nkb; ++i) {
-      const int s = i % kStages;
-      const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+      const int s = i % nst;
+      const uint32_t ph = (uint32_t)(i / nst) & 1u;
       if (!mbar_wait(&full[s], ph)) {
         set_status(p.status, DF_ERR_TIMEOUT);
         break;
@@ -330,11 +333,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       dst = acc_s + j * stage_stride + (f >> 6) * nl + hf % nl;
       stride = nfs;
     }
-    for (int c0 = 0; c0 < p.n_pad; c0 += 16) {
-      float v[16];
-      tmem_ld16(lane_base + (uint32_t)c0, v);
+    // up to four 16-column loads in flight per wait
+    for (int c0 = 0; c0 < p.n_pad; c0 += 64) {
+      uint32_t v[4][16];
+      const int nblk = (p.n_pad - c0) >= 64 ? 4 : (p.n_pad - c0) / 16;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) dst[(c0 + j) * stride] = v[j];
+      for (int q = 0; q < 4; ++q)
+        if (q < nblk) tmem_ld16_nowait(lane_base + (uint32_t)(c0 + 16 * q), v[q]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < nblk)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[(c0 + 16 * q + j) * stride] = __uint_as_float(v[q][j]);
     }
   }
   fence_proxy_async_smem();  // the staged slices are read by the bulk-copy engine
@@ -654,7 +665,10 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   // data region: the pipeline stages; after the main loop the partial tile (512 B per activation
   // row) or, when split, the staged slices plus the receive area (1 KB per row + bank pads). Then
   // the barriers, the TMEM address slot and the 256-float row-scale array.
-  const int pipe = kStages * (kABytes + p.n_pad * 128);
+  // as many stages (up to 4) as fit the budget that keeps two CTAs per SM
+  p.stages = kStageBudget / (kABytes + p.n_pad * 128);
+  p.stages = p.stages > kStages ? kStages : (p.stages < 2 ? 2 : p.stages);
+  const int pipe = p.stages * (kABytes + p.n_pad * 128);
   const int parts = p.splits > 1 ? 1024 * p.n_pad + 32 * p.splits : 512 * p.n_pad;
   p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
   const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 4;

@@ -171,6 +171,10 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t smem_addr) {
       : "r"(taddr)                                                                                             \
       : "memory")
 
+// Issues a 16-column TMEM load into r without waiting (pair with tmem_ld_wait before use).
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) { DF_TMEM_LD_X16(taddr, r); }
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // Lane (32*warp + t) of the warp reads 16 consecutive fp32 columns starting at `col`.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];

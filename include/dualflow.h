@@ -253,8 +253,9 @@ DF_API int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream);
  * head_dim / group / page-size limits as dualflow_init (DF_ERR_UNSUPPORTED otherwise).
  *   cfg     host; n_q_heads, n_kv_heads, head_dim, dtype, paged, page_size, max_batch, max_ctx,
  *           max_pages describe the cache layout exactly as for dualflow_init (other fields unused)
- *   q       device bf16 [2, batch, Hq, D]: both flows' queries, already coupled and rotated (the
- *           queries dualflow_decode_attention forms internally); flow 1 rows read only if aux_on
+ *   q       device bf16 [2, batch, Hq, D], 16-byte aligned: both flows' queries, already coupled
+ *           and rotated (the queries dualflow_decode_attention forms internally); flow 1 rows read
+ *           only if aux_on
  *   kv      host struct of device pointers, as for dualflow_decode_attention; layer selects k/v
  *   o       device bf16 [2, batch, Hq, D]: o_f = softmax(q_f K1^T / sqrt(D)) V1 over the cached
  *           positions 0..seq_len[b]-1; seq_len[b] == 0 gives o = 0; flow 1 written only if aux_on
