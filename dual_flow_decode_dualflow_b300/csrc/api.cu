@@ -371,6 +371,15 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
     g.ss_ld = ss_ld;
     g.pdl = pdl;
   };
+  // the projection that follows (weights, shape, epilogue): its first k-blocks are warmed in L2
+  auto prefetch = [&](GemmArgs& cur, const void* W, int n_out, int k, int epi) {
+    GemmArgs nx = gemm_args(ctx);
+    nx.W = W;
+    nx.n_out = n_out;
+    nx.k = k;
+    nx.epi = epi;
+    gemm_prefetch_next(ctx, cur, nx);
+  };
   for (int l = 0; l < c.n_layers; ++l) {
     GemmArgs g = gemm_args(ctx);
     g.x = ctx->x;
@@ -401,6 +410,7 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
     o.y = ctx->h;
     o.ldy = c.d_model;
     norm_output(o, w->g_mlp[l]);
+    if (c.n_experts == 0) prefetch(o, w->Wgu[l], c.ffn_hidden, c.d_model, EPI_SWIGLU);
     DF_TRY(L(DF_PROF_OPROJ, [&] { return launch_gemm_tc(ctx, o, s); }));
     ss_parts = o_parts;
     const void* g_next = l + 1 < c.n_layers ? w->g_attn[l + 1] : w->g_final;
@@ -422,6 +432,7 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
     gu.ldy = c.ffn_hidden;
     gu.vec = w->b[l];
     normed_input(gu);
+    prefetch(gu, w->Wd[l], c.d_model, c.ffn_hidden, EPI_COUPLE_ADD);
     DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_gemm_tc(ctx, gu, s); }));
     GemmArgs dn = gemm_args(ctx);
     dn.x = ctx->u;
@@ -435,6 +446,10 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
     dn.ldy = c.d_model;
     dn.vec = w->c[l];
     norm_output(dn, g_next);
+    if (l + 1 < c.n_layers)
+      prefetch(dn, w->Wqkv[l + 1], qkv_n, c.d_model, EPI_QKV);
+    else
+      prefetch(dn, w->W_lm, c.vocab, c.d_model, EPI_STORE_F32);
     DF_TRY(L(DF_PROF_DOWN, [&] { return launch_gemm_tc(ctx, dn, s); }));
     ss_parts = d_parts;
   }

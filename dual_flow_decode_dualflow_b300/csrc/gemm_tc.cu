@@ -48,6 +48,7 @@ struct GemmParams {
   int vec_ok;    // y / u rows allow 16-byte (fp32) or 8-byte (bf16) vector access
   int stages;    // pipeline stages in use (2..kStages)
   int region;    // bytes of the data region (pipeline stages, later the partial tiles)
+  int push_async;  // split-K partials pushed by 16-byte asynchronous stores (else staged + bulk copy)
   int32_t* status;
 };
 
@@ -125,12 +126,18 @@ __device__ __forceinline__ size_t cache_slot(const GemmArgs& a, int b, int hk, i
 }
 
 // Where a CTA finds the fp32 partial tiles of its output slice. S == 1: its own accumulator tile
-// acc[n][128]. S > 1: the S partials of its slice received from the cluster's CTAs, recv[r][n][2 nl]
-// (features lo0.. lo0+nl then 64+lo0.. 64+lo0+nl of every row n, from rank r).
+// acc[n][128]. S > 1: the S partials of its slice received from the cluster's CTAs, from rank r,
+// local feature fl (fl < nl: feature lo0 + fl; fl >= nl: its partner lo0 + 64 + fl - nl); row-major
+// recv[r][n][2nl] when staged and bulk-copied, feature-major recv[r][fl][n_pad + 4] when pushed by
+// asynchronous stores.
 struct RedSrc {
   const float* base;
-  int S, n_pad, nl;
+  int S, n_pad, nl, transposed;
 };
+
+__device__ __forceinline__ float4 col4(const float* e, int stride) {
+  return make_float4(e[0], e[stride], e[2 * stride], e[3 * stride]);
+}
 
 // Reduced accumulators of activation row n at the slice's quad qd: low features (lo) and their
 // partners 64 apart (hi), summed over the S partials in rank order.
@@ -141,14 +148,26 @@ __device__ __forceinline__ void reduce_pair(const RedSrc& r, int lo0, int n, int
     hi = *reinterpret_cast<const float4*>(e + 64);
     return;
   }
-  const int nfs = 2 * r.nl;
-  const float* e = r.base + n * nfs + 4 * qd;
-  const int rs = r.n_pad * nfs;
-  lo = *reinterpret_cast<const float4*>(e);
-  hi = *reinterpret_cast<const float4*>(e + r.nl);
+  if (!r.transposed) {
+    const int nfs = 2 * r.nl;
+    const float* e = r.base + n * nfs + 4 * qd;
+    const int rs = r.n_pad * nfs;
+    lo = *reinterpret_cast<const float4*>(e);
+    hi = *reinterpret_cast<const float4*>(e + r.nl);
+    for (int k = 1; k < r.S; ++k) {
+      lo = f4_add(lo, *reinterpret_cast<const float4*>(e + k * rs));
+      hi = f4_add(hi, *reinterpret_cast<const float4*>(e + k * rs + r.nl));
+    }
+    return;
+  }
+  const int fs = r.n_pad + 4;                   // feature row stride
+  const int rs = 2 * r.nl * fs;                 // one rank's slice
+  const float* e = r.base + (4 * qd) * fs + n;
+  lo = col4(e, fs);
+  hi = col4(e + r.nl * fs, fs);
   for (int k = 1; k < r.S; ++k) {
-    lo = f4_add(lo, *reinterpret_cast<const float4*>(e + k * rs));
-    hi = f4_add(hi, *reinterpret_cast<const float4*>(e + k * rs + r.nl));
+    lo = f4_add(lo, col4(e + k * rs, fs));
+    hi = f4_add(hi, col4(e + k * rs + r.nl * fs, fs));
   }
 }
 
@@ -178,7 +197,7 @@ __device__ __forceinline__ void store4(const GemmArgs& a, int vec_ok, int n, int
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap map_pf, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_bytes = p.n_pad * 128;
@@ -192,8 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
   float* rstd_s = reinterpret_cast<float*>(tmem_slot + 4);  // [256] 1 / rms of each activation row
   // After the main loop the pipeline bytes hold, for S == 1, the accumulator tile acc[n][128];
-  // for S > 1, the staged partial split into S slices [S][n_pad * 2nl + 8] (the 8-float pad
-  // spreads the slices over the shared-memory banks) followed by the receive area [S][n_pad][2nl].
+  // for S > 1 and staged partials, the partial split into S slices [S][n_pad * 2nl + 8] (the pad
+  // spreads the slices over the banks) followed by the receive area [S][n_pad][2nl]; for pushed
+  // partials, the receive area [S][2nl][n_pad + 4] only (see RedSrc).
   float* acc_s = reinterpret_cast<float*>(smem);
 
   const GemmArgs& a = p.a;
@@ -207,9 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   while ((int)ncols < p.n_pad) ncols <<= 1;
   const int S = p.splits;
   const int nl = 64 / S, lo0 = split * nl, nq = nl / 4, nfs = 2 * nl;
-  const int slice_floats = p.n_pad * nfs;          // one rank's partial of one slice
-  const int stage_stride = slice_floats + 8;       // staged slices, bank-spread
-  float* recv_s = acc_s + S * stage_stride;        // [S][n_pad][nfs]
+  const int fstride = p.n_pad + 4;                 // pushed: floats per feature row
+  const int slice_floats = p.push_async ? nfs * fstride : p.n_pad * nfs;  // one rank's slice partial
+  const int stage_stride = p.n_pad * nfs + 8;      // staged slices, bank-spread
+  float* recv_s = p.push_async ? acc_s : acc_s + S * stage_stride;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -220,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(recv_bar, 1);
     fence_mbar_init();
     // the S slices of this CTA's output arrive by bulk copy from the cluster's CTAs
-    if (S > 1) mbar_arrive_expect_tx(recv_bar, (uint32_t)(S * slice_floats * 4));
+    if (S > 1) mbar_arrive_expect_tx(recv_bar, (uint32_t)(S * nfs * p.n_pad * 4));
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_x);
   }
@@ -274,6 +295,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_2d_hint(sA + s * kABytes + kABytes / 2, &map_w, &full[s], kc, row1, pol_w);
       tma_load_2d_hint(sB + s * b_bytes, &map_x, &full[s], kc, xrow, pol_x);
     }
+    if (a.pf_W != nullptr && a.pf_depth > 0) {
+      // every tile of this launch is requested: warm L2 with the next launch's first k-blocks
+      const int ncur = gridDim.x * gridDim.y * gridDim.z;
+      const int cid = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+      const int nnext = a.pf_tiles * a.pf_splits, kbn = a.pf_k / kGemmTileK;
+      for (int q = (int)((long long)cid * nnext / ncur); q < (int)((long long)(cid + 1) * nnext / ncur); ++q) {
+        const int t = q / a.pf_splits, sp = q % a.pf_splits;
+        const int k0 = (int)((long long)sp * kbn / a.pf_splits), k1 = (int)((long long)(sp + 1) * kbn / a.pf_splits);
+        const int r0 = t * a.pf_tile_rows;
+        for (int kb = k0; kb < k1 && kb < k0 + a.pf_depth; ++kb) {
+          tma_prefetch_l2_2d(&map_pf, kb * kGemmTileK, r0);
+          tma_prefetch_l2_2d(&map_pf, kb * kGemmTileK, r0 + a.pf_half);
+        }
+      }
+    }
   } else if (warp == 1 && lane == 0) {
     // MMA issuer: 4 x (M=128, N=n_pad, K=16) per stage, accumulate in TMEM.
     const uint32_t idesc = idesc_bf16_f32(kGemmTileN, p.n_pad);
@@ -318,59 +354,74 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool acc_ok = mbar_wait(done, 0);
   tc_fence_after();
   if (!acc_ok) set_status(p.status, DF_ERR_TIMEOUT);
-  // this CTA's pipeline buffers are free: the cluster's CTAs may write into them once all arrive
-  if (S > 1) cluster_arrive();
-  {
-    const int f = threadIdx.x;  // TMEM lane == output feature within the tile
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    float* dst;
-    int stride;
-    if (S == 1) {
-      dst = acc_s + f;
-      stride = kGemmTileN;
+  const int tf = threadIdx.x;  // TMEM lane == output feature within the tile
+  const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+  const int hf = tf & 63, dst_rank = hf / nl;  // split-K: the rank that owns feature tf
+  const int fl = (tf >> 6) * nl + hf % nl;     // and its index there
+  float* dst = acc_s + tf;                      // S == 1: acc[n][128]
+  int dstride = kGemmTileN;
+  uint32_t adst = 0, abar = 0;
+  if (S > 1) {
+    // this CTA's pipeline buffers are free: the cluster's CTAs may write into them once all arrive
+    cluster_arrive();
+    if (p.push_async) {
+      cluster_wait();
+      adst = mapa_shared(smem_u32(recv_s + split * slice_floats + fl * fstride), (uint32_t)dst_rank);
+      abar = mapa_shared(smem_u32(recv_bar), (uint32_t)dst_rank);
     } else {
-      const int hf = f & 63, j = hf / nl;  // slice (destination rank) of feature f
-      dst = acc_s + j * stage_stride + (f >> 6) * nl + hf % nl;
-      stride = nfs;
+      dst = acc_s + dst_rank * stage_stride + fl;  // staged slice of rank dst_rank, row-major
+      dstride = nfs;
     }
-    // up to four 16-column loads in flight per wait
-    for (int c0 = 0; c0 < p.n_pad; c0 += 64) {
-      uint32_t v[4][16];
-      const int nblk = (p.n_pad - c0) >= 64 ? 4 : (p.n_pad - c0) / 16;
+  }
+  // four 16-column TMEM loads in flight per wait
+  for (int c0 = 0; c0 < p.n_pad; c0 += 64) {
+    uint32_t v[4][16];
+    const int nblk = (p.n_pad - c0) >= 64 ? 4 : (p.n_pad - c0) / 16;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q < nblk) tmem_ld16_nowait(lane_base + (uint32_t)(c0 + 16 * q), v[q]);
-      tmem_ld_wait();
+    for (int q = 0; q < 4; ++q)
+      if (q < nblk) tmem_ld16_nowait(lane_base + (uint32_t)(c0 + 16 * q), v[q]);
+    tmem_ld_wait();
+    if (S > 1 && p.push_async) {
+      // feature tf's column, straight into the owner's receive area (16-byte asynchronous stores)
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (q < nblk)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst[(c0 + 16 * q + j) * stride] = __uint_as_float(v[q][j]);
+          for (int jj = 0; jj < 16; jj += 4)
+            st_async_v4(adst + (uint32_t)((c0 + 16 * q + jj) * 4), __uint_as_float(v[q][jj]),
+                        __uint_as_float(v[q][jj + 1]), __uint_as_float(v[q][jj + 2]), __uint_as_float(v[q][jj + 3]),
+                        abar);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (q < nblk)
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dst[(c0 + 16 * q + j) * dstride] = __uint_as_float(v[q][j]);
     }
   }
-  fence_proxy_async_smem();  // the staged slices are read by the bulk-copy engine
+  if (S > 1 && !p.push_async) fence_proxy_async_smem();  // staged slices are read by the bulk-copy engine
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, ncols);
   griddep_wait();  // the epilogue reads and writes buffers of the preceding kernels
-
-  // ---- split-K reduction: every CTA pushes slice r of its partial into rank r's receive area
-  //      (one bulk copy each), then sums the S partials of its own slice in rank order, so the
-  //      result is deterministic and independent of which flows are present ----
   if (S > 1) {
-    cluster_wait();  // every CTA of the cluster has drained its pipeline
-    if (threadIdx.x == 0) {
-      const uint32_t src0 = smem_u32(acc_s), dst_local = smem_u32(recv_s + split * slice_floats);
-      const uint32_t bar_local = smem_u32(recv_bar);
-      for (int r = 0; r < S; ++r)
-        bulk_copy_to_cluster(mapa_shared(dst_local, (uint32_t)r), src0 + (uint32_t)(r * stage_stride * 4),
-                             (uint32_t)(slice_floats * 4), mapa_shared(bar_local, (uint32_t)r));
+    if (!p.push_async) {
+      // every CTA pushes staged slice r into rank r's receive area, one bulk copy each
+      cluster_wait();  // every CTA of the cluster has drained its pipeline
+      if (threadIdx.x == 0) {
+        const uint32_t src0 = smem_u32(acc_s), dst_local = smem_u32(recv_s + split * slice_floats);
+        const uint32_t bar_local = smem_u32(recv_bar);
+        for (int r = 0; r < S; ++r)
+          bulk_copy_to_cluster(mapa_shared(dst_local, (uint32_t)r), src0 + (uint32_t)(r * stage_stride * 4),
+                               (uint32_t)(slice_floats * 4), mapa_shared(bar_local, (uint32_t)r));
+      }
     }
     if (!mbar_wait(recv_bar, 0)) set_status(p.status, DF_ERR_TIMEOUT);
     cluster_arrive();  // this CTA has received everything sent to it (its own copies are done too)
   }
   RedSrc red;
   red.base = S == 1 ? acc_s : recv_s;
+  red.transposed = p.push_async;
   red.S = S;
   red.n_pad = p.n_pad;
   red.nl = nl;
@@ -585,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int EPI>
-int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, size_t smem, cudaStream_t s) {
+int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& mpf, const GemmParams& p, size_t smem,
+               cudaStream_t s) {
   auto kern = gemm_tc_kernel<EPI>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return DF_ERR_CUDA;
@@ -610,10 +662,22 @@ int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, kern, mw, mx, p) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, mw, mx, mpf, p) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
 }  // namespace
+
+void gemm_prefetch_next(const dualflow_ctx* ctx, GemmArgs& cur, const GemmArgs& next) {
+  const bool swiglu = next.epi == EPI_SWIGLU;
+  cur.pf_W = next.W;
+  cur.pf_k = next.k;
+  cur.pf_rows = swiglu ? 2 * next.n_out : next.n_out;
+  cur.pf_tiles = gemm_tiles(next.n_out, next.epi);
+  cur.pf_splits = gemm_splits(ctx, next.n_out, next.k, next.epi);
+  cur.pf_tile_rows = swiglu ? 64 : kGemmTileN;
+  cur.pf_half = swiglu ? next.n_out : 64;
+  cur.pf_depth = kStages;
+}
 
 int gemm_tiles(int n_out, int epi) {
   return (epi == EPI_SWIGLU || epi == EPI_MOE_GATEUP) ? n_out / 64 : (n_out + kGemmTileN - 1) / kGemmTileN;
@@ -621,9 +685,8 @@ int gemm_tiles(int n_out, int epi) {
 
 // Reduction splits (cluster size): the smallest power of two, at most 8, that gives every SM a
 // tile slice, with at least 2 k-blocks per CTA. Depends only on the weight shape and the context's
-// capacity, never on which flows are present. A split CTA holds its partial tile and the S
-// received slices at once (1 KB per padded activation row), so contexts with more than 208 rows
-// of capacity do not split.
+// capacity, never on which flows are present. A split CTA receives its slice of the S partials
+// (512 B per padded activation row); contexts with more than 208 rows of capacity do not split.
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups) {
   const int tiles = gemm_tiles(n_out, epi) * groups;
   const int kb = k / kGemmTileK;
@@ -662,6 +725,11 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   if (rc != DF_OK) return rc;
   rc = encode_map_2d_bf16(&mx, a.x, (uint64_t)a.k, x_rows, (uint64_t)a.k * 2, kGemmTileK, (uint32_t)p.n_pad);
   if (rc != DF_OK) return rc;
+  CUtensorMap mpf = mw;
+  if (a.pf_W != nullptr) {
+    rc = encode_map_2d_bf16(&mpf, a.pf_W, (uint64_t)a.pf_k, (uint64_t)a.pf_rows, (uint64_t)a.pf_k * 2, kGemmTileK, 64);
+    if (rc != DF_OK) return rc;
+  }
   // data region: the pipeline stages; after the main loop the partial tile (512 B per activation
   // row) or, when split, the staged slices plus the receive area (1 KB per row + bank pads). Then
   // the barriers, the TMEM address slot and the 256-float row-scale array.
@@ -669,19 +737,23 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   p.stages = kStageBudget / (kABytes + p.n_pad * 128);
   p.stages = p.stages > kStages ? kStages : (p.stages < 2 ? 2 : p.stages);
   const int pipe = p.stages * (kABytes + p.n_pad * 128);
-  const int parts = p.splits > 1 ? 1024 * p.n_pad + 32 * p.splits : 512 * p.n_pad;
+  // split-K partials: staged and bulk-copied when the staging fits in the pipeline bytes, else
+  // pushed from TMEM by asynchronous stores (no staging, so two CTAs still share an SM)
+  const int staged = 1024 * p.n_pad + 32 * p.splits;
+  p.push_async = (p.splits > 1 && staged > pipe) ? 1 : 0;
+  const int parts = p.splits == 1 ? 512 * p.n_pad : p.push_async ? 512 * (p.n_pad + 4) : staged;
   p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
   const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 4;
   switch (a.epi) {
-    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(mw, mx, p, smem, s);
-    case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(mw, mx, p, smem, s);
-    case EPI_ADD_F32: return launch_epi<EPI_ADD_F32>(mw, mx, p, smem, s);
-    case EPI_COUPLE_ADD: return launch_epi<EPI_COUPLE_ADD>(mw, mx, p, smem, s);
-    case EPI_QKV: return launch_epi<EPI_QKV>(mw, mx, p, smem, s);
-    case EPI_Q2: return launch_epi<EPI_Q2>(mw, mx, p, smem, s);
-    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(mw, mx, p, smem, s);
-    case EPI_MOE_GATEUP: return launch_epi<EPI_MOE_GATEUP>(mw, mx, p, smem, s);
-    case EPI_MOE_DOWN: return launch_epi<EPI_MOE_DOWN>(mw, mx, p, smem, s);
+    case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(mw, mx, mpf, p, smem, s);
+    case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(mw, mx, mpf, p, smem, s);
+    case EPI_ADD_F32: return launch_epi<EPI_ADD_F32>(mw, mx, mpf, p, smem, s);
+    case EPI_COUPLE_ADD: return launch_epi<EPI_COUPLE_ADD>(mw, mx, mpf, p, smem, s);
+    case EPI_QKV: return launch_epi<EPI_QKV>(mw, mx, mpf, p, smem, s);
+    case EPI_Q2: return launch_epi<EPI_Q2>(mw, mx, mpf, p, smem, s);
+    case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(mw, mx, mpf, p, smem, s);
+    case EPI_MOE_GATEUP: return launch_epi<EPI_MOE_GATEUP>(mw, mx, mpf, p, smem, s);
+    case EPI_MOE_DOWN: return launch_epi<EPI_MOE_DOWN>(mw, mx, mpf, p, smem, s);
     default: return DF_ERR_ARG;
   }
 }

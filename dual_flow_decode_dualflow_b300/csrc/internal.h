@@ -77,6 +77,11 @@ struct GemmArgs {
   int n_groups, w_group_rows, x_group_rows;
   size_t y_group_stride;
   const int32_t* sel_pos;
+  // L2 prefetch of the next projection's weights: once its last tiles are requested, each CTA asks
+  // L2 for the first pf_depth k-blocks of its share of the next launch's (tile, split) CTAs, so the
+  // next launch starts on L2-resident weights. pf_W = nullptr: none.
+  const void* pf_W;
+  int pf_k, pf_rows, pf_tiles, pf_splits, pf_tile_rows, pf_half, pf_depth;
 };
 
 struct AttnArgs {
@@ -153,6 +158,9 @@ int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 // Launchers (return dualflow_status).
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s);
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups = 1);
+int gemm_tiles(int n_out, int epi);
+// Fills cur's L2-prefetch fields from the (ungrouped) projection `next` that follows it.
+void gemm_prefetch_next(const dualflow_ctx* ctx, GemmArgs& cur, const GemmArgs& next);
 int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl = 0);
 // The same kernel with caller-chosen workspace: split partials (>= pairs + ctas slots of
 // kAttnPartFloats), per-pair merge counters (zero on entry), the status word, and a grid of `ctas`

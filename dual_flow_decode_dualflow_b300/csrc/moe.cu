@@ -15,8 +15,6 @@
 namespace df {
 namespace {
 
-__device__ __forceinline__ void set_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
-
 // Rank of lane e's logit among the E logits of lanes 0..E-1: the number of experts ordered before it
 // (larger logit, or equal logit and lower index). The experts of rank < k are the top-k, in rank
 // order. Every lane of the warp executes the shuffles; lanes >= E get rank >= E.
