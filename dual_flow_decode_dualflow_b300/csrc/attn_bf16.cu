@@ -46,7 +46,7 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
   if (*err) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) {
     if (*err) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       *err = 1;
