@@ -4,17 +4,21 @@
 // (primary rows then auxiliary rows, <= 256): the weight tile is the M = 128 operand, the stacked
 // activations are the N operand, so every weight byte is streamed from HBM once and serves both
 // flows ("Custos de Inferencia vs. Treinamento": grouping keeps the unique weights read unchanged).
-// Weight and activation tiles are staged by TMA (128-byte swizzle) through a 4-stage mbarrier
-// pipeline; one elected thread issues tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in TMEM).
-// Under programmatic dependent launch the weight tiles of the first stages are requested before
-// the kernel waits for its predecessor: weights never depend on it, activations do.
+// Weight and activation tiles are staged by TMA (128-byte swizzle) through a mbarrier pipeline of
+// up to 4 stages (as many as fit 96 KB, so that two CTAs share an SM); one elected thread issues
+// tcgen05.mma (kind::f16, bf16 in, fp32 accumulate in TMEM). Under programmatic dependent launch
+// the weight tiles of the first stages are requested before the kernel waits for its predecessor
+// (weights never depend on it, activations do), and the producer warms L2 with the first k-blocks
+// of the NEXT projection's weights once its own loads are issued.
 //
 // When the output has too few tiles to fill the GPU the reduction dimension is split across the S
-// CTAs of a thread-block cluster (S <= 8). Each CTA parks its fp32 partial tile in shared memory;
-// after a cluster barrier every CTA sums, over distributed shared memory and in rank order (so the
-// result is deterministic and independent of which flows are present), its own 1/S slice of the
-// tile's features -- feature i and its RoPE / gate-up partner i + 64 travel together, four at a
-// time -- and runs the epilogue on that slice:
+// CTAs of a thread-block cluster (S <= 8). Every CTA owns a 1/S slice of the tile's features --
+// feature i and its RoPE / gate-up partner i + 64 travel together, four at a time -- and receives
+// the other ranks' partials of that slice in its shared memory: either staged from TMEM and sent
+// by one bulk copy per destination, or, when staging would not fit in the pipeline's bytes, sent
+// straight from registers by 16-byte asynchronous remote stores. The owner sums the S partials in
+// rank order (deterministic, and independent of which flows are present) and runs the epilogue on
+// its slice:
 //   EPI_QKV      q1 = Wq.x1, q2 = Wq.x2 + a (*) q1 (before RoPE), RoPE(q1, q2, k1) at position
 //                seq_len[b], q stored bf16, primary k1/v1 appended to the cache at slot seq_len[b]
 //                ("Atencao de KV Compartilhada Assimetrica": the auxiliary flow writes no K/V)
@@ -22,6 +26,8 @@
 //   EPI_SWIGLU   u = silu(gate) (*) up for both flows, then u2 += b (*) u1 ("Acoplamento Leve")
 //   EPI_COUPLE_ADD  y2 += c (*) y1, then h += y (MLP output coupling and residual)
 //   EPI_ADD_F32 / EPI_STORE_F32 / EPI_STORE_BF16  residual update, logits, plain stores
+//   EPI_MOE_GATEUP / EPI_MOE_DOWN  one expert per grid.z: SWIGLU (with b where both flows chose the
+//                expert) or a plain fp32 store, for the rows whose routing selected that expert
 //
 // RMSNorm across kernels (decode step). RMSNorm(h) . W^T = (1/rms(h)) ((h (*) g) . W^T): a residual
 // epilogue that has just produced h also writes x_next = bf16(h (*) g_next) and, per row, the sum
