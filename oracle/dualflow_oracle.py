@@ -48,6 +48,9 @@ are silent, each one a choice of this implementation:
   R9 mixture head: alpha = 1/2 + 1/2 * sum_i p1_i^2 (collision probability mapped to [1/2, 1]).
   R10 an attention-only call on a sequence with nothing cached (L_b = 0) returns o = 0 (softmax
      over an empty set is undefined; the step itself always attends at least its own new entry).
+  R11 token choice after the mixture head: greedy = argmax of p_mix (ties to the lower index), or
+     inverse-transform sampling with a supplied uniform u in [0, 1): the smallest i whose
+     cumulative probability exceeds u (the last i with p_i > 0 when rounding leaves none).
 
 Precision: inputs arrive as the stored values widened to fp64. With mirror=True and a bf16
 workload the oracle rounds (to nearest bf16, ties to even) exactly where the GPU path stores
@@ -408,3 +411,13 @@ def mixture_head(logits1: np.ndarray, logits2: np.ndarray):
     alpha = 0.5 + 0.5 * float(np.sum(p1 * p1))
     pm = alpha * p1 + (1.0 - alpha) * p2
     return alpha, pm, int(np.argmax(pm))
+
+
+def sample_inverse_cdf(p: np.ndarray, u: float) -> int:
+    """Token drawn from the distribution p with the uniform u in [0, 1) (R11): the smallest i with
+    p_0 + ... + p_i > u; if rounding leaves every partial sum <= u, the last i with p_i > 0."""
+    p = np.asarray(p, F64)
+    above = np.nonzero(np.cumsum(p) > u)[0]
+    if len(above):
+        return int(above[0])
+    return int(np.nonzero(p > 0)[0][-1])

@@ -435,6 +435,26 @@ def pin_mixture_head(O):
         assert 0.5 <= a <= 1.0
 
 
+def pin_sampling(O):
+    """Inverse-transform sampling: hand-worked cases, closed forms, and the empirical frequencies
+    of a stratified grid of uniforms reproduce the distribution."""
+    p = np.array([0.1, 0.0, 0.3, 0.6])
+    for u, want in [(0.0, 0), (0.05, 0), (0.1, 2), (0.39, 2), (0.4, 3), (0.9999, 3)]:
+        assert O.sample_inverse_cdf(p, u) == want, (u, want)
+    assert O.sample_inverse_cdf(np.array([0.5, 0.5, 0.0]), 1.0) == 1  # no partial sum exceeds u
+    V = 37
+    for u in (0.013, 0.5 + 1e-9, 0.977):
+        assert O.sample_inverse_cdf(np.full(V, 1.0 / V), u) == int(np.floor(u * V))
+    one = np.zeros(V); one[11] = 1.0
+    assert all(O.sample_inverse_cdf(one, u) == 11 for u in (0.0, 0.3, 0.999))
+    rng = np.random.default_rng(17)
+    q = rng.dirichlet(np.ones(12))
+    N = 20000
+    counts = np.bincount([O.sample_inverse_cdf(q, (k + 0.5) / N) for k in range(N)], minlength=12)
+    assert np.all(np.abs(counts - N * q) <= 1.0 + 1e-9), (counts, N * q)
+
+
 ALL_PINS = [pin_round_bf16, pin_rmsnorm, pin_rope, pin_attention_closed_forms, pin_attention_gqa_vs_sdpa,
             pin_small_ops, pin_primary_is_standard_decoder, pin_flow_invariants, pin_coupling_special_cases, pin_query_coupling_source,
-            pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mirror_tracks_exact, pin_mixture_head]
+            pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mirror_tracks_exact, pin_mixture_head,
+            pin_sampling]

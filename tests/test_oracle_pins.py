@@ -54,6 +54,9 @@ MUTANTS = {
     "paged_wrong_page": ("ks = [np.asarray(self.K[int(self.table[b, j])], dtype=F64) for j in range(n)]",
                          "ks = [np.asarray(self.K[int(self.table[b, n - 1 - j])], dtype=F64) for j in range(n)]"),
     "final_norm_dropped": ('xf = _normed(h[f, i], glob["g_final"], hp, mirror)', "xf = h[f, i]"),
+    "sample_at_or_above": ("np.cumsum(p) > u", "np.cumsum(p) >= u"),
+    "sample_fallback_first": ("return int(np.nonzero(p > 0)[0][-1])", "return int(np.nonzero(p > 0)[0][0])"),
+    "mix_weights_swapped": ("pm = alpha * p1 + (1.0 - alpha) * p2", "pm = alpha * p2 + (1.0 - alpha) * p1"),
 }
 
 
