@@ -23,7 +23,7 @@ DF_EPI_STORE_F32, DF_EPI_STORE_BF16, DF_EPI_ADD_F32, DF_EPI_COUPLE_ADD = 0, 1, 2
 C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dualflow_decode_attention",
                "dualflow_stacked_linear", "dualflow_coupled_mlp", "dualflow_step", "dualflow_step_host",
                "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
-               "dualflow_decode_attention_noalloc", "dualflow_expert_ids")
+               "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head")
 DF_PROF_FAMILIES = 8
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
@@ -84,6 +84,7 @@ def load_library(path: str = LIB_PATH):
         "dualflow_decode_attention_noalloc": ([POINTER(dualflow_config), vp, POINTER(dualflow_kv), i32, i32, vp, i32,
                                                vp, vp], i32),
         "dualflow_expert_ids": ([vp, vp, i32, vp], i32),
+        "dualflow_mixture_head": ([vp, vp, i32, vp, vp, vp, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -203,6 +204,14 @@ def dualflow_decode_attention_noalloc(cfg: dualflow_config, q, kv: "dualflow_kv"
 def dualflow_expert_ids(ctx, ids, batch: int, stream=None) -> None:
     """Experts of every layer chosen by the last step: device int32 [n_layers, 2, batch, kmax]."""
     _check("dualflow_expert_ids", load_library().dualflow_expert_ids(ctx, _ptr(ids), batch, _stream(stream)))
+
+
+def dualflow_mixture_head(ctx, logits, batch: int, u=None, alpha=None, p_mix=None, token=None, stream=None) -> None:
+    """Mixture of both flows' next-token distributions and the token choice: logits device fp32
+    [2, batch, vocab]; u device fp32 [batch] (sampling) or None (argmax); outputs nullable."""
+    rc = load_library().dualflow_mixture_head(ctx, _ptr(logits), batch, _ptr(u), _ptr(alpha), _ptr(p_mix),
+                                              _ptr(token), _stream(stream))
+    _check("dualflow_mixture_head", rc)
 
 
 def dualflow_sync_status(ctx, stream=None) -> int:

@@ -755,6 +755,13 @@ int dualflow_expert_ids(dualflow_ctx* ctx, int32_t* ids, int32_t batch, dualflow
              : DF_ERR_CUDA;
 }
 
+int dualflow_mixture_head(dualflow_ctx* ctx, const float* logits, int32_t batch, const float* u, float* alpha,
+                          float* p_mix, int32_t* token, dualflow_stream stream) {
+  if (!ctx || !logits) return DF_ERR_ARG;
+  if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
+  return launch_mixture_head(logits, batch, ctx->cfg.vocab, u, alpha, p_mix, token, S(stream));
+}
+
 int dualflow_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
                   int32_t batch, float* logits, int32_t aux_on, dualflow_stream stream) {
   if (!ctx || !tokens || !logits) return DF_ERR_ARG;
@@ -855,6 +862,10 @@ int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream) {
   int32_t v = 0;
   if (cudaMemcpy(&v, ctx->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return DF_ERR_CUDA;
   if (v != 0 && cudaMemset(ctx->status, 0, sizeof(v)) != cudaSuccess) return DF_ERR_CUDA;
+  // a kernel that gave up on a wait may have left the attention's merge counters behind
+  if (v == DF_ERR_TIMEOUT && ctx->attn_cnt &&
+      cudaMemset(ctx->attn_cnt, 0, (size_t)ctx->cfg.max_batch * ctx->cfg.n_kv_heads * sizeof(int32_t)) != cudaSuccess)
+    return DF_ERR_CUDA;
   return v;
 }
 

@@ -182,6 +182,8 @@ int launch_moe_route(dualflow_ctx* ctx, const float* rlog, int batch, int aux_on
                      int pdl);
 int launch_moe_combine(dualflow_ctx* ctx, float* h, int batch, int aux_on, const void* c_vec, const void* g_next,
                        cudaStream_t s, int pdl);
+int launch_mixture_head(const float* logits, int batch, int vocab, const float* u, float* alpha, float* p_mix,
+                        int32_t* token, cudaStream_t s);
 int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s);
 int launch_rope_q1(dualflow_ctx* ctx, const void* q1, void* q, const int32_t* seq_len, int batch, cudaStream_t s);
 

@@ -1,0 +1,282 @@
+// Mixture head and token choice of the dual-flow decoder, fp32, sm_103a.
+//
+// "Objetivo de Mistura" (gist.science technical summary, "Mecanismos Chave"): the next-token
+// distribution mixes both flows' predictions with a weight that grows with the primary flow's
+// confidence and never drops below one half. This build's reading: p_f = softmax(logits_f),
+// alpha = 1/2 + 1/2 * sum_i p1_i^2 (the collision probability of p1 mapped to [1/2, 1]),
+// p_mix = alpha * p1 + (1 - alpha) * p2. The token is the argmax of p_mix (ties to the lower index)
+// or, given a uniform u in [0, 1), the smallest i whose cumulative p_mix exceeds u (inverse-transform
+// sampling; the last i with p_mix_i > 0 when rounding leaves none).
+//
+// One thread-block cluster per sequence; its S CTAs (S <= 8) split the vocabulary into contiguous
+// slices. Pass 1: each CTA reduces its slice of both flows' logits to an online-softmax triple
+// (max, sum of exp, sum of exp^2), exchanged over distributed shared memory and combined in rank
+// order, so every CTA holds the same (M1, Z1, Q1, M2, Z2) and alpha = 1/2 + Q1 / (2 Z1^2). Pass 2:
+// every thread owns a contiguous run of its CTA's slice, computes p_mix there (stored if asked),
+// its running argmax and its sum; block and cluster scans in fixed order give each run its start
+// on the cumulative axis, and the one run whose interval holds u walks its elements. All
+// reductions have a fixed order: the result does not depend on scheduling.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace df {
+namespace {
+
+constexpr int kMixThreads = 256;
+constexpr int kMixWarps = kMixThreads / 32;
+constexpr int kMixMaxCluster = 8;
+
+struct Soft {  // online softmax state of one flow: max, sum e^(l - m), sum e^(2 (l - m))
+  float m, s, q;
+};
+
+__device__ __forceinline__ Soft soft_add(Soft a, float l) {
+  if (l > a.m) {
+    const float f = expf(a.m - l);  // 0 when a.m = -inf
+    a.s = __fmaf_rn(a.s, f, 1.f);
+    a.q = __fmaf_rn(a.q, f * f, 1.f);
+    a.m = l;
+  } else {
+    const float e = expf(l - a.m);
+    a.s = __fadd_rn(a.s, e);
+    a.q = __fmaf_rn(e, e, a.q);
+  }
+  return a;
+}
+
+__device__ __forceinline__ Soft soft_merge(Soft a, Soft b) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -INFINITY) return a;
+  const float fa = expf(a.m - M), fb = expf(b.m - M);
+  Soft r;
+  r.m = M;
+  r.s = __fadd_rn(a.s * fa, b.s * fb);
+  r.q = __fadd_rn(a.q * (fa * fa), b.q * (fb * fb));
+  return r;
+}
+
+__device__ __forceinline__ Soft soft_shfl(Soft a, int off) {
+  Soft b;
+  b.m = __shfl_xor_sync(0xffffffffu, a.m, off);
+  b.s = __shfl_xor_sync(0xffffffffu, a.s, off);
+  b.q = __shfl_xor_sync(0xffffffffu, a.q, off);
+  return b;
+}
+
+// (value, index) argmax step: larger value wins, equal values go to the lower index.
+__device__ __forceinline__ void arg_merge(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+struct MixShared {
+  Soft soft[2][kMixWarps];  // per-warp partials, then [f][0] the CTA's
+  float best_v[kMixWarps];
+  int best_i[kMixWarps];
+  int last_pos[kMixWarps];
+  float warp_total[kMixWarps];
+  float run_start[kMixThreads];  // exclusive scan of the runs' sums of p_mix
+  // the CTA's results read by the other CTAs of the cluster
+  float cta_soft[2][3];
+  float cta_best_v;
+  int cta_best_i;
+  int cta_last_pos;
+  float cta_total;
+  int cta_pick;
+};
+
+// grid (S, B), cluster (S, 1, 1), 256 threads. logits [2][B][V] fp32.
+__global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* __restrict__ logits, int B, int V,
+                                                                   const float* __restrict__ u, float* alpha_out,
+                                                                   float* p_mix, int32_t* token_out) {
+  __shared__ MixShared sh;
+  const int S = gridDim.x, r = blockIdx.x, b = blockIdx.y;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int chunk = (V + S - 1) / S;
+  const int lo = r * chunk, hi = min(V, lo + chunk), n = max(0, hi - lo);
+  const float* l1 = logits + (size_t)b * V + lo;
+  const float* l2 = logits + ((size_t)B + b) * V + lo;
+
+  // ---- pass 1: online softmax triples of both flows over the slice ----
+  Soft s1 = {-INFINITY, 0.f, 0.f}, s2 = {-INFINITY, 0.f, 0.f};
+  for (int i = t; i < n; i += kMixThreads) {
+    s1 = soft_add(s1, __ldg(l1 + i));
+    s2 = soft_add(s2, __ldg(l2 + i));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    s1 = soft_merge(s1, soft_shfl(s1, off));
+    s2 = soft_merge(s2, soft_shfl(s2, off));
+  }
+  if (lane == 0) {
+    sh.soft[0][warp] = s1;
+    sh.soft[1][warp] = s2;
+  }
+  __syncthreads();
+  if (t < 2) {
+    Soft acc = sh.soft[t][0];
+    for (int w = 1; w < kMixWarps; ++w) acc = soft_merge(acc, sh.soft[t][w]);
+    sh.cta_soft[t][0] = acc.m;
+    sh.cta_soft[t][1] = acc.s;
+    sh.cta_soft[t][2] = acc.q;
+  }
+  cluster_sync();
+  // every CTA combines the S triples in rank order (identical result in every CTA)
+  Soft g1 = {-INFINITY, 0.f, 0.f}, g2 = {-INFINITY, 0.f, 0.f};
+  const uint32_t soft_addr = smem_u32(&sh.cta_soft[0][0]);
+  for (int k = 0; k < S; ++k) {
+    const uint32_t ra = mapa_shared(soft_addr, (uint32_t)k);
+    const Soft a1 = {ld_dsmem_f32(ra), ld_dsmem_f32(ra + 4), ld_dsmem_f32(ra + 8)};
+    const Soft a2 = {ld_dsmem_f32(ra + 12), ld_dsmem_f32(ra + 16), ld_dsmem_f32(ra + 20)};
+    g1 = soft_merge(g1, a1);
+    g2 = soft_merge(g2, a2);
+  }
+  const float iz1 = 1.f / g1.s, iz2 = 1.f / g2.s;
+  const float alpha = __fmaf_rn(0.5f, g1.q * (iz1 * iz1), 0.5f);
+  const float beta = 1.f - alpha;
+
+  // ---- pass 2: p_mix over this thread's contiguous run ----
+  const int per = (n + kMixThreads - 1) / kMixThreads;
+  const int i0 = min(n, t * per), i1 = min(n, i0 + per);
+  float run = 0.f, bv = -INFINITY;
+  int bi = 0x7fffffff, lastpos = -1;
+  for (int i = i0; i < i1; ++i) {
+    const float p1 = expf(__ldg(l1 + i) - g1.m) * iz1;
+    const float p2 = expf(__ldg(l2 + i) - g2.m) * iz2;
+    const float pm = __fmaf_rn(alpha, p1, beta * p2);
+    if (p_mix) p_mix[(size_t)b * V + lo + i] = pm;
+    if (pm > bv) {
+      bv = pm;
+      bi = lo + i;
+    }
+    if (pm > 0.f) lastpos = lo + i;
+    run = __fadd_rn(run, pm);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    arg_merge(bv, bi, __shfl_xor_sync(0xffffffffu, bv, off), __shfl_xor_sync(0xffffffffu, bi, off));
+    lastpos = max(lastpos, __shfl_xor_sync(0xffffffffu, lastpos, off));
+  }
+  // scan of the runs' sums in thread order: a fixed shuffle tree inside each warp, then the warps'
+  // totals in order
+  float incl = run;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl = __fadd_rn(y, incl);
+  }
+  float excl_w = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl_w = 0.f;
+  if (lane == 31) sh.warp_total[warp] = incl;
+  if (lane == 0) {
+    sh.best_v[warp] = bv;
+    sh.best_i[warp] = bi;
+    sh.last_pos[warp] = lastpos;
+  }
+  __syncthreads();
+  if (t == 0) {
+    float v = sh.best_v[0];
+    int ix = sh.best_i[0], lp = sh.last_pos[0];
+    for (int w = 1; w < kMixWarps; ++w) {
+      arg_merge(v, ix, sh.best_v[w], sh.best_i[w]);
+      lp = max(lp, sh.last_pos[w]);
+    }
+    float acc = 0.f;
+    for (int w = 0; w < kMixWarps; ++w) {
+      const float x = sh.warp_total[w];
+      sh.warp_total[w] = acc;  // now the warp's exclusive offset
+      acc = __fadd_rn(acc, x);
+    }
+    sh.cta_best_v = v;
+    sh.cta_best_i = ix;
+    sh.cta_last_pos = lp;
+    sh.cta_total = acc;
+    sh.cta_pick = 0x7fffffff;
+  }
+  __syncthreads();
+  sh.run_start[t] = __fadd_rn(sh.warp_total[warp], excl_w);  // this run's start within the CTA's slice
+  cluster_sync();
+  // cluster view, in rank order: argmax, last positive index, this CTA's offset on the cumulative axis
+  float gv = -INFINITY, offset = 0.f, total = 0.f;
+  int gi = 0x7fffffff, glast = -1;
+  {
+    const uint32_t bv_addr = smem_u32(&sh.cta_best_v), bi_addr = smem_u32(&sh.cta_best_i);
+    const uint32_t lp_addr = smem_u32(&sh.cta_last_pos), tot_addr = smem_u32(&sh.cta_total);
+    for (int k = 0; k < S; ++k) {
+      arg_merge(gv, gi, ld_dsmem_f32(mapa_shared(bv_addr, (uint32_t)k)),
+                (int)ld_dsmem_u32(mapa_shared(bi_addr, (uint32_t)k)));
+      glast = max(glast, (int)ld_dsmem_u32(mapa_shared(lp_addr, (uint32_t)k)));
+      const float tk = ld_dsmem_f32(mapa_shared(tot_addr, (uint32_t)k));
+      if (k == r) offset = total;
+      total = __fadd_rn(total, tk);
+    }
+  }
+  int pick = -1;
+  if (u != nullptr) {
+    // run r covers [e_r, e_r+1) with e_r = fl(offset + start of r); the next CTA's first run starts at
+    // fl(offset + total), this CTA's last boundary. Consecutive intervals share their boundary, so
+    // every u in [0, total) lies in some run's interval; where rounding makes two overlap, the
+    // lower index wins.
+    const float uu = __ldg(u + b);
+    const float start = __fadd_rn(offset, sh.run_start[t]);
+    const float end = __fadd_rn(offset, (t + 1 < kMixThreads) ? sh.run_start[t + 1] : sh.cta_total);
+    if (i1 > i0 && start <= uu && uu < end) {
+      float c = start;
+      int lastp = -1;
+      for (int i = i0; i < i1; ++i) {
+        const float p1 = expf(__ldg(l1 + i) - g1.m) * iz1;
+        const float p2 = expf(__ldg(l2 + i) - g2.m) * iz2;
+        const float pm = __fmaf_rn(alpha, p1, beta * p2);
+        if (pm > 0.f) lastp = lo + i;
+        c = __fadd_rn(c, pm);
+        if (c > uu) {
+          pick = lo + i;
+          break;
+        }
+      }
+      if (pick < 0) pick = lastp >= 0 ? lastp : lo + i1 - 1;  // rounding ended the walk at or below u
+      atomicMin(&sh.cta_pick, pick);
+    }
+  }
+  cluster_sync();
+  if (r == 0 && t == 0) {
+    if (alpha_out) alpha_out[b] = alpha;
+    if (token_out) {
+      int tok = gi;
+      if (u != nullptr) {
+        int p = 0x7fffffff;
+        const uint32_t pk_addr = smem_u32(&sh.cta_pick);
+        for (int k = 0; k < S; ++k) p = min(p, (int)ld_dsmem_u32(mapa_shared(pk_addr, (uint32_t)k)));
+        tok = (p != 0x7fffffff) ? p : glast;
+      }
+      token_out[b] = tok;
+    }
+  }
+  cluster_sync();  // no CTA leaves while its shared memory may still be read
+}
+
+}  // namespace
+
+int launch_mixture_head(const float* logits, int batch, int vocab, const float* u, float* alpha, float* p_mix,
+                        int32_t* token, cudaStream_t s) {
+  int S = (vocab + 4095) / 4096;
+  S = S < 1 ? 1 : (S > kMixMaxCluster ? kMixMaxCluster : S);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(S, batch, 1);
+  lc.blockDim = dim3(kMixThreads, 1, 1);
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = S;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, mixture_head_kernel, logits, batch, vocab, u, alpha, p_mix, token) == cudaSuccess
+             ? DF_OK
+             : DF_ERR_CUDA;
+}
+
+}  // namespace df

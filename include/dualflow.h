@@ -190,6 +190,24 @@ DF_API int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weig
  * step ran with aux_on = 0). batch must equal the step's batch. Asynchronous on `stream`. */
 DF_API int dualflow_expert_ids(dualflow_ctx* ctx, int32_t* ids, int32_t batch, dualflow_stream stream);
 
+/* Mixture head and token choice ("Objetivo de Mistura", gist.science technical summary, "Mecanismos
+ * Chave": the two flows' next-token distributions are mixed with a weight on the primary that
+ * grows with its confidence and is at least one half). Reading of this library:
+ *   p_f = softmax(logits_f), alpha = 1/2 + 1/2 * sum_i p1_i^2, p_mix = alpha p1 + (1 - alpha) p2;
+ *   token = argmax_i p_mix_i (ties to the lower index) when u is NULL, else the smallest i with
+ *   p_mix_0 + ... + p_mix_i > u[b] (inverse-transform sampling; the last i with p_mix_i > 0 if
+ *   rounding leaves no partial sum above u[b]).
+ *   logits  device fp32 [2, batch, vocab] (flow-major, as written by dualflow_step), finite
+ *   u       device fp32 [batch] uniforms in [0, 1), or NULL for greedy choice
+ *   alpha   device fp32 [batch] or NULL;  p_mix  device fp32 [batch, vocab] or NULL
+ *   token   device int32 [batch] or NULL
+ * vocab is the context's. One launch on `stream`, nothing allocated, graph-capturable; fp32
+ * arithmetic with every reduction in a fixed order (the outputs do not depend on scheduling).
+ * Returns DF_ERR_ARG for a NULL context or logits, DF_ERR_SHAPE for batch outside
+ * 1..max_batch; non-finite logits give unspecified (but in-bounds) tokens. */
+DF_API int dualflow_mixture_head(dualflow_ctx* ctx, const float* logits, int32_t batch, const float* u, float* alpha,
+                                 float* p_mix, int32_t* token, dualflow_stream stream);
+
 /* One whole decode step of both flows: embeddings E1[tok], E2[tok] -> n_layers x {RMSNorm,
  * QKV with query coupling, RoPE and primary-only KV append, shared-KV attention, O projection,
  * coupled MLP} -> final RMSNorm -> shared LM head.
@@ -234,7 +252,10 @@ DF_API int dualflow_set_profiling(dualflow_ctx* ctx, int32_t enabled);
 DF_API int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches, int32_t n_families);
 
 /* Synchronizes `stream`, then returns and clears the device status word: DF_OK, or the first
- * DF_ERR_DEVICE_BOUNDS / DF_ERR_TIMEOUT latched by a kernel since the last call. */
+ * DF_ERR_DEVICE_BOUNDS / DF_ERR_TIMEOUT latched by a kernel since the last call. After
+ * DF_ERR_TIMEOUT it also clears the attention kernel's merge counters, which a kernel that stopped
+ * early may have left behind, so the context is usable again (the outputs of the failed calls are
+ * not). */
 DF_API int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream);
 
 /* Largest batch * n_kv_heads that dualflow_decode_attention_noalloc accepts. */
