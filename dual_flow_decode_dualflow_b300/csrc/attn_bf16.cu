@@ -46,7 +46,7 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
   if (*err) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) {
+  while (!mbar_try_wait(bar, parity)) {
     if (*err) return false;
     if (globaltimer() - t0 > kWaitLimitNs) {
       *err = 1;
@@ -141,8 +141,22 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
   griddep_launch_dependents();
   const long long T = sched[B];
   // Cut the T tiles over C = min(grid, T) CTAs so that every participating CTA owns at least one
-  // tile (the partial-merge counts rely on it); CTAs beyond C only zero empty sequences.
-  const int C = (int)(T < (long long)gridDim.x ? T : (long long)gridDim.x);
+  // tile (the partial-merge counts rely on it); CTAs beyond C only zero empty sequences. When every
+  // pair has the same number of tiles and the grid holds k >= 1 CTAs per pair, C = pairs * k: the
+  // cuts fall on pair boundaries, every CTA works on one pair, and no CTA pays for a pair change.
+  int C = (int)(T < (long long)gridDim.x ? T : (long long)gridDim.x);
+  {
+    const int per = B > 0 ? sched[1] / Hkv : 0;  // tiles of one pair of sequence 0
+    const int pairs = B * Hkv;
+    if (per > 0 && pairs <= (int)gridDim.x && T == (long long)pairs * per) {
+      bool uniform = true;
+      for (int b = 1; b < B && uniform; ++b) uniform = (sched[b + 1] - sched[b] == per * Hkv);
+      if (uniform) {
+        const int k = min((int)gridDim.x / pairs, per);
+        C = pairs * k;
+      }
+    }
+  }
   const long long t0 = (c < C) ? T * c / C : 0, t1 = (c < C) ? T * (c + 1) / C : 0;
 
   if (warp == kConsumers) {

@@ -52,27 +52,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait that may suspend the thread (up to `hint_ns`) until the phase completes, instead of
-// returning at once: waiting warps then leave the issue slots to the working ones.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
-constexpr uint32_t kSuspendHintNs = 100000;  // a waiting thread sleeps up to 100 us per try
-
 // Waits for the phase with the given parity to complete; false when the limit expired.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) {
+  while (!mbar_try_wait(bar, parity)) {
     if (globaltimer() - t0 > kWaitLimitNs) return false;
   }
   return true;
