@@ -51,6 +51,10 @@ are silent, each one a choice of this implementation:
   R11 token choice after the mixture head: greedy = argmax of p_mix (ties to the lower index), or
      inverse-transform sampling with a supplied uniform u in [0, 1): the smallest i whose
      cumulative probability exceeds u (the last i with p_i > 0 when rounding leaves none).
+  R12 generation loop: each decode step appends the primary's k1/v1 at position seq_len[b] (the
+     entry the step attended), seq_len[b] grows by one, and the token chosen from that step's
+     mixture (R11) is the next step's input. With the auxiliary flow off the choice is made from
+     the primary's distribution softmax(logits_1) alone.
 
 Precision: inputs arrive as the stored values widened to fp64. With mirror=True and a bf16
 workload the oracle rounds (to nearest bf16, ties to even) exactly where the GPU path stores
@@ -411,6 +415,61 @@ def mixture_head(logits1: np.ndarray, logits2: np.ndarray):
     alpha = 0.5 + 0.5 * float(np.sum(p1 * p1))
     pm = alpha * p1 + (1.0 - alpha) * p2
     return alpha, pm, int(np.argmax(pm))
+
+
+def choose_token(logits1: np.ndarray, logits2: np.ndarray | None, u: float | None = None) -> int:
+    """The next token from one sequence's logits (R11, R12): from the mixture of both flows, or from
+    the primary's distribution alone when logits2 is None; argmax, or a sample with uniform u."""
+    if logits2 is None:
+        p = softmax(np.asarray(logits1, F64))
+    else:
+        _, p, _ = mixture_head(logits1, logits2)
+    return int(np.argmax(p)) if u is None else sample_inverse_cdf(p, u)
+
+
+def append_entry(cache, b: int, L: int, k: np.ndarray, v: np.ndarray) -> None:
+    """Writes the primary's key/value [Hkv, D] at position L of sequence b (the cache arrays are
+    written in place; a paged cache must map position L to a page)."""
+    if isinstance(cache, PagedCache):
+        pid = int(cache.table[b, L // cache.page_size])
+        cache.K[pid][:, L % cache.page_size, :] = k
+        cache.V[pid][:, L % cache.page_size, :] = v
+    else:
+        cache.K[b][:, L, :] = k
+        cache.V[b][:, L, :] = v
+
+
+def generate(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequence, tokens: np.ndarray,
+             seq_len: np.ndarray, n_steps: int, u: np.ndarray | None = None, aux_on: bool = True,
+             mirror: bool = True, token_override: Callable | None = None,
+             ids_override: Callable | None = None) -> dict:
+    """The decode loop (R12): n_steps decode steps of every sequence; after step t the appended
+    entries join the caches, seq_len grows by one, and token[t, b] (R11; u[t, b] when sampling)
+    feeds step t + 1. caches are written in place. token_override(t, b, token) may replace a
+    choice (a caller resolving a near tie the way another implementation took it).
+
+    Returns tokens [n_steps, B], logits [n_steps, 2, B, V] and the final seq_len."""
+    tokens = np.array(tokens, dtype=np.int64)
+    L = np.array(seq_len, dtype=np.int64)
+    B = len(tokens)
+    out_tok = np.zeros((n_steps, B), dtype=np.int64)
+    out_logits = np.full((n_steps, 2, B, hp.vocab), np.nan)
+    for t in range(n_steps):
+        ov = (lambda l, b, t=t: ids_override(t, l, b)) if ids_override is not None else None
+        r = decode_step(hp, glob, layers, caches, tokens, L, aux_on=aux_on, mirror=mirror, ids_override=ov)
+        out_logits[t] = r["logits"]
+        for layer in range(len(layers)):
+            for b in range(B):
+                append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])
+        for b in range(B):
+            tok = choose_token(r["logits"][0, b], r["logits"][1, b] if aux_on else None,
+                               None if u is None else float(u[t, b]))
+            if token_override is not None:
+                tok = int(token_override(t, b, tok))
+            out_tok[t, b] = tok
+        L = L + 1
+        tokens = out_tok[t].copy()
+    return dict(tokens=out_tok, logits=out_logits, seq_len=L)
 
 
 def sample_inverse_cdf(p: np.ndarray, u: float) -> int:

@@ -454,7 +454,99 @@ def pin_sampling(O):
     assert np.all(np.abs(counts - N * q) <= 1.0 + 1e-9), (counts, N * q)
 
 
+def _torch_decode_one(hp, glob, layers, tok, L, Kl, Vl, Wq_scale=None):
+    """One sequence's decode step with a textbook decoder from torch calls (fp64) over explicit
+    cache tensors Kl[l], Vl[l] ([Hkv, L, D]); returns the logits and each layer's new (k, v)."""
+    t = lambda a: torch.from_numpy(np.asarray(a, F64))  # noqa: E731
+    Hq, Hkv, D, F = hp.n_q_heads, hp.n_kv_heads, hp.head_dim, hp.ffn_hidden
+    h = t(glob["E1"][tok])
+    new = []
+    for li, P in enumerate(layers):
+        x = TF.rms_norm(h, (hp.d_model,), weight=t(P["g_attn"]), eps=hp.rms_eps)
+        W = t(P["Wqkv"])
+        Wq, Wk, Wv = W[: Hq * D], W[Hq * D: (Hq + Hkv) * D], W[(Hq + Hkv) * D:]
+        if Wq_scale is not None:
+            Wq = Wq * t(Wq_scale)[:, None]
+        q = _torch_rope(TF.linear(x, Wq).view(Hq, D), L, hp.rope_base)
+        k = _torch_rope(TF.linear(x, Wk).view(Hkv, D), L, hp.rope_base)
+        v = TF.linear(x, Wv).view(Hkv, D)
+        Kc = torch.cat([Kl[li], k[:, None]], 1)
+        Vc = torch.cat([Vl[li], v[:, None]], 1)
+        o = TF.scaled_dot_product_attention(q[None, :, None], Kc[None], Vc[None], enable_gqa=True)[0, :, 0]
+        h = h + TF.linear(o.reshape(-1), t(P["Wo"]))
+        x = TF.rms_norm(h, (hp.d_model,), weight=t(P["g_mlp"]), eps=hp.rms_eps)
+        h = h + TF.linear(TF.silu(TF.linear(x, t(P["Wgu"][:F]))) * TF.linear(x, t(P["Wgu"][F:])), t(P["Wd"]))
+        new.append((k, v))
+    x = TF.rms_norm(h, (hp.d_model,), weight=t(glob["g_final"]), eps=hp.rms_eps)
+    return TF.linear(x, t(glob["W_lm"])), new
+
+
+def torch_generate(hp, glob, layers, caches, tokens, seq_len, n_steps, u=None, aux_Wq_scale=None):
+    """Generation with torch calls and torch-side KV lists: the primary decoder's distribution, or
+    (aux_Wq_scale given) its mixture with a second decoder whose query rows are scaled, attending
+    the primary's cache; next token by torch.argmax or by torch.searchsorted of the cumulative sum."""
+    B, nL = len(tokens), len(layers)
+    Kl = [[torch.from_numpy(np.asarray(caches[li].seq(b, int(seq_len[b]))[0], F64)) for li in range(nL)] for b in range(B)]
+    Vl = [[torch.from_numpy(np.asarray(caches[li].seq(b, int(seq_len[b]))[1], F64)) for li in range(nL)] for b in range(B)]
+    toks = [int(x) for x in tokens]
+    out = np.zeros((n_steps, B), dtype=np.int64)
+    for st in range(n_steps):
+        for b in range(B):
+            L = int(seq_len[b]) + st
+            l1, new = _torch_decode_one(hp, glob, layers, toks[b], L, Kl[b], Vl[b])
+            p = torch.softmax(l1, 0)
+            if aux_Wq_scale is not None:
+                l2, _ = _torch_decode_one(hp, glob, layers, toks[b], L, Kl[b], Vl[b], Wq_scale=aux_Wq_scale)
+                alpha = 0.5 + 0.5 * torch.dot(p, p)
+                p = alpha * p + (1 - alpha) * torch.softmax(l2, 0)
+            if u is None:
+                out[st, b] = int(torch.argmax(p))
+            else:
+                out[st, b] = int(torch.searchsorted(torch.cumsum(p, 0), torch.tensor([float(u[st, b])], dtype=torch.float64),
+                                                    right=True)[0])
+            for li, (k, v) in enumerate(new):
+                Kl[b][li] = torch.cat([Kl[b][li], k[:, None]], 1)
+                Vl[b][li] = torch.cat([Vl[b][li], v[:, None]], 1)
+        toks = [int(x) for x in out[st]]
+    return out
+
+
+def _writable_caches(O, caches):
+    return [O.DenseCache(K=np.array(c.K, copy=True), V=np.array(c.V, copy=True)) for c in caches]
+
+
+def pin_generate(O):
+    """The decode loop against torch-built generators: greedy and sampled generation of tied,
+    uncoupled flows (the mixture is the primary's distribution); the mixture of a one-layer model
+    whose auxiliary flow differs only by query coupling a (a second decoder with scaled query rows
+    sharing the primary's cache); and primary-only generation with coupling on."""
+    hp = tiny_hp(O, vocab=11)
+    n = 4
+    glob, layers, caches, tokens, L = tiny_model(O, hp, n_layers=2, seed=21, couple=False, tie_emb=True)
+    ref = torch_generate(hp, glob, layers, caches, tokens, L, n)
+    got = O.generate(hp, glob, layers, _writable_caches(O, caches), tokens, L, n, mirror=False)
+    assert np.array_equal(got["tokens"], ref), (got["tokens"], ref)
+    assert np.array_equal(got["seq_len"], L + n)
+    u = np.random.default_rng(22).uniform(size=(n, len(tokens)))
+    ref = torch_generate(hp, glob, layers, caches, tokens, L, n, u=u)
+    got = O.generate(hp, glob, layers, _writable_caches(O, caches), tokens, L, n, u=u, mirror=False)
+    assert np.array_equal(got["tokens"], ref), (got["tokens"], ref)
+    # the mixture matters: a one-layer model, E2 = E1, coupling a only
+    glob1, layers1, caches1, tokens1, L1 = tiny_model(O, hp, n_layers=1, seed=23, couple=False, tie_emb=True,
+                                                      batch=2)
+    a = np.random.default_rng(24).normal(size=layers1[0]["a"].shape) * 1.5
+    layers1 = [dict(layers1[0], a=a)]
+    ref = torch_generate(hp, glob1, layers1, caches1, tokens1, L1, n, aux_Wq_scale=1 + a)
+    got = O.generate(hp, glob1, layers1, _writable_caches(O, caches1), tokens1, L1, n, mirror=False)
+    assert np.array_equal(got["tokens"], ref), (got["tokens"], ref)
+    prim = torch_generate(hp, glob1, layers1, caches1, tokens1, L1, n)
+    assert not np.array_equal(prim, ref), "the mixture never changes a choice here: the pin is blind"
+    # auxiliary flow off: the primary's own choice, coupling or not
+    got = O.generate(hp, glob1, layers1, _writable_caches(O, caches1), tokens1, L1, n, aux_on=False, mirror=False)
+    assert np.array_equal(got["tokens"], prim)
+
+
 ALL_PINS = [pin_round_bf16, pin_rmsnorm, pin_rope, pin_attention_closed_forms, pin_attention_gqa_vs_sdpa,
             pin_small_ops, pin_primary_is_standard_decoder, pin_flow_invariants, pin_coupling_special_cases, pin_query_coupling_source,
             pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mirror_tracks_exact, pin_mixture_head,
-            pin_sampling]
+            pin_sampling, pin_generate]

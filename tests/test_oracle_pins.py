@@ -57,6 +57,10 @@ MUTANTS = {
     "sample_at_or_above": ("np.cumsum(p) > u", "np.cumsum(p) >= u"),
     "sample_fallback_first": ("return int(np.nonzero(p > 0)[0][-1])", "return int(np.nonzero(p > 0)[0][0])"),
     "mix_weights_swapped": ("pm = alpha * p1 + (1.0 - alpha) * p2", "pm = alpha * p2 + (1.0 - alpha) * p1"),
+    "generate_no_append": ('append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])',
+                           "pass"),
+    "generate_no_increment": ("        L = L + 1\n        tokens = out_tok[t].copy()", "        tokens = out_tok[t].copy()"),
+    "generate_primary_choice": ("    if logits2 is None:\n        p = softmax", "    if True:\n        p = softmax"),
 }
 
 
