@@ -23,7 +23,8 @@ DF_EPI_STORE_F32, DF_EPI_STORE_BF16, DF_EPI_ADD_F32, DF_EPI_COUPLE_ADD = 0, 1, 2
 C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dualflow_decode_attention",
                "dualflow_stacked_linear", "dualflow_coupled_mlp", "dualflow_step", "dualflow_step_host",
                "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
-               "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head")
+               "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head",
+               "dualflow_generate")
 DF_PROF_FAMILIES = 8
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
@@ -85,6 +86,8 @@ def load_library(path: str = LIB_PATH):
                                                vp, vp], i32),
         "dualflow_expert_ids": ([vp, vp, i32, vp], i32),
         "dualflow_mixture_head": ([vp, vp, i32, vp, vp, vp, vp, vp], i32),
+        "dualflow_generate": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, vp, vp, vp, vp,
+                               i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -212,6 +215,16 @@ def dualflow_mixture_head(ctx, logits, batch: int, u=None, alpha=None, p_mix=Non
     rc = load_library().dualflow_mixture_head(ctx, _ptr(logits), batch, _ptr(u), _ptr(alpha), _ptr(p_mix),
                                               _ptr(token), _stream(stream))
     _check("dualflow_mixture_head", rc)
+
+
+def dualflow_generate(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens, batch: int, n_steps: int, tokens_out,
+                      logits, u=None, logits_all=None, free_pages=None, n_free=None, aux_on: int = 1,
+                      stream=None) -> None:
+    """The decode loop: n_steps steps, each step's chosen token feeding the next (see the header)."""
+    rc = load_library().dualflow_generate(ctx, ctypes.byref(w), ctypes.byref(kv), _ptr(tokens), batch, n_steps, _ptr(u),
+                                          _ptr(tokens_out), _ptr(logits), _ptr(logits_all), _ptr(free_pages),
+                                          _ptr(n_free), aux_on, _stream(stream))
+    _check("dualflow_generate", rc)
 
 
 def dualflow_sync_status(ctx, stream=None) -> int:

@@ -583,6 +583,7 @@ int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
       return fail(DF_ERR_CUDA);
   }
   if (dalloc(&ctx->status, sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->gen_tokens, (size_t)c.max_batch * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
   cudaMemset(ctx->status, 0, sizeof(int32_t));
   // decode attention: persistent grid of 2 CTAs per SM; partial slots = pairs + CTAs
   ctx->attn_ctas = 2 * ctx->num_sms;
@@ -635,7 +636,7 @@ int dualflow_free(dualflow_ctx* ctx) {
   }
   void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
                   ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss,
-                  ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids};
+                  ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids, ctx->gen_tokens};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete ctx;
@@ -759,7 +760,35 @@ int dualflow_mixture_head(dualflow_ctx* ctx, const float* logits, int32_t batch,
                           float* p_mix, int32_t* token, dualflow_stream stream) {
   if (!ctx || !logits) return DF_ERR_ARG;
   if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
-  return launch_mixture_head(logits, batch, ctx->cfg.vocab, u, alpha, p_mix, token, S(stream));
+  return launch_mixture_head(logits, batch, ctx->cfg.vocab, u, alpha, p_mix, token, nullptr, 1, S(stream));
+}
+
+int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
+                      int32_t batch, int32_t n_steps, const float* u, int32_t* tokens_out, float* logits,
+                      float* logits_all, int32_t* free_pages, int32_t* n_free, int32_t aux_on,
+                      dualflow_stream stream) {
+  if (!ctx || !tokens || !tokens_out || !logits || !kv || !kv->seq_len) return DF_ERR_ARG;
+  if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
+  if (batch <= 0 || batch > ctx->cfg.max_batch || n_steps < 0) return DF_ERR_SHAPE;
+  if (n_steps == 0) return DF_OK;
+  const dualflow_config& c = ctx->cfg;
+  cudaStream_t s = S(stream);
+  if (cudaMemcpyAsync(ctx->gen_tokens, tokens, (size_t)batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
+      cudaSuccess)
+    return DF_ERR_CUDA;
+  const size_t per_step = (size_t)2 * batch * c.vocab;
+  // the step reads the loop's own token buffer, so every step replays the same captured graph
+  for (int t = 0; t < n_steps; ++t) {
+    DF_TRY(dualflow_step(ctx, w, kv, ctx->gen_tokens, batch, logits, aux_on, stream));
+    if (logits_all && cudaMemcpyAsync(logits_all + (size_t)t * per_step, logits, per_step * sizeof(float),
+                                      cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return DF_ERR_CUDA;
+    DF_TRY(launch_mixture_head(logits, batch, c.vocab, u ? u + (size_t)t * batch : nullptr, nullptr, nullptr,
+                               tokens_out + (size_t)t * batch, ctx->gen_tokens, aux_on, s));
+    DF_TRY(launch_gen_advance(c, const_cast<int32_t*>(kv->seq_len), batch, const_cast<int32_t*>(kv->page_table),
+                              free_pages, n_free, ctx->status, s));
+  }
+  return DF_OK;
 }
 
 int dualflow_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,

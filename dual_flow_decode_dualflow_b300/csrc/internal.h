@@ -135,6 +135,7 @@ struct dualflow_ctx {
   void* moe_u = nullptr;           // [E][2 * max_batch][F] bf16
   float* moe_y = nullptr;          // [E][2 * max_batch][d]
   int32_t* moe_ids = nullptr;      // [n_layers][2][max_batch][kmax] experts chosen by the last step
+  int32_t* gen_tokens = nullptr;   // [max_batch] input tokens of the generation loop's next step
   int ss_ld = 0;                   // ceil(d / 128) tiles x 8 splits
   int32_t* tokens_dev = nullptr;   // dualflow_step_host staging
   float* logits_dev = nullptr;
@@ -183,7 +184,9 @@ int launch_moe_route(dualflow_ctx* ctx, const float* rlog, int batch, int aux_on
 int launch_moe_combine(dualflow_ctx* ctx, float* h, int batch, int aux_on, const void* c_vec, const void* g_next,
                        cudaStream_t s, int pdl);
 int launch_mixture_head(const float* logits, int batch, int vocab, const float* u, float* alpha, float* p_mix,
-                        int32_t* token, cudaStream_t s);
+                        int32_t* token, int32_t* token2, int aux_on, cudaStream_t s);
+int launch_gen_advance(const dualflow_config& c, int32_t* seq_len, int batch, int32_t* table, int32_t* free_pages,
+                       int32_t* n_free, int32_t* status, cudaStream_t s);
 int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s);
 int launch_rope_q1(dualflow_ctx* ctx, const void* q1, void* q, const int32_t* seq_len, int batch, cudaStream_t s);
 

@@ -87,10 +87,13 @@ struct MixShared {
   int cta_pick;
 };
 
-// grid (S, B), cluster (S, 1, 1), 256 threads. logits [2][B][V] fp32.
+// grid (S, B), cluster (S, 1, 1), 256 threads. logits [2][B][V] fp32. primary_only: the choice is
+// made from softmax(logits_1) alone (alpha = 1; the auxiliary logits are not read). token2: a second
+// copy of the chosen tokens (the next decode step's input), or null.
 __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* __restrict__ logits, int B, int V,
                                                                    const float* __restrict__ u, float* alpha_out,
-                                                                   float* p_mix, int32_t* token_out) {
+                                                                   float* p_mix, int32_t* token_out, int32_t* token2,
+                                                                   int primary_only) {
   __shared__ MixShared sh;
   const int S = gridDim.x, r = blockIdx.x, b = blockIdx.y;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -103,7 +106,7 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
   Soft s1 = {-INFINITY, 0.f, 0.f}, s2 = {-INFINITY, 0.f, 0.f};
   for (int i = t; i < n; i += kMixThreads) {
     s1 = soft_add(s1, __ldg(l1 + i));
-    s2 = soft_add(s2, __ldg(l2 + i));
+    if (!primary_only) s2 = soft_add(s2, __ldg(l2 + i));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -133,8 +136,8 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
     g1 = soft_merge(g1, a1);
     g2 = soft_merge(g2, a2);
   }
-  const float iz1 = 1.f / g1.s, iz2 = 1.f / g2.s;
-  const float alpha = __fmaf_rn(0.5f, g1.q * (iz1 * iz1), 0.5f);
+  const float iz1 = 1.f / g1.s, iz2 = primary_only ? 0.f : 1.f / g2.s;
+  const float alpha = primary_only ? 1.f : __fmaf_rn(0.5f, g1.q * (iz1 * iz1), 0.5f);
   const float beta = 1.f - alpha;
 
   // ---- pass 2: p_mix over this thread's contiguous run ----
@@ -144,7 +147,7 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
   int bi = 0x7fffffff, lastpos = -1;
   for (int i = i0; i < i1; ++i) {
     const float p1 = expf(__ldg(l1 + i) - g1.m) * iz1;
-    const float p2 = expf(__ldg(l2 + i) - g2.m) * iz2;
+    const float p2 = primary_only ? 0.f : expf(__ldg(l2 + i) - g2.m) * iz2;
     const float pm = __fmaf_rn(alpha, p1, beta * p2);
     if (p_mix) p_mix[(size_t)b * V + lo + i] = pm;
     if (pm > bv) {
@@ -227,7 +230,7 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
       int lastp = -1;
       for (int i = i0; i < i1; ++i) {
         const float p1 = expf(__ldg(l1 + i) - g1.m) * iz1;
-        const float p2 = expf(__ldg(l2 + i) - g2.m) * iz2;
+        const float p2 = primary_only ? 0.f : expf(__ldg(l2 + i) - g2.m) * iz2;
         const float pm = __fmaf_rn(alpha, p1, beta * p2);
         if (pm > 0.f) lastp = lo + i;
         c = __fadd_rn(c, pm);
@@ -252,15 +255,61 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
         tok = (p != 0x7fffffff) ? p : glast;
       }
       token_out[b] = tok;
+      if (token2) token2[b] = tok;
     }
   }
   cluster_sync();  // no CTA leaves while its shared memory may still be read
 }
 
+// After a decode step of the generation loop: every sequence's length grows by one (its new entry
+// is in the cache), and a paged sequence whose next slot opens a page gets one from the free list,
+// taken from the top in sequence order. One thread: the page assignment does not depend on
+// scheduling. A length that would reach max_ctx, a page slot beyond the table, or an empty free
+// list latches DF_ERR_DEVICE_BOUNDS and leaves that sequence as it is.
+__global__ void gen_advance_kernel(int32_t* seq_len, int B, int max_ctx, int paged, int page_size, int32_t* table,
+                                   int pages_per_seq, int max_pages, int32_t* free_pages, int32_t* n_free,
+                                   int32_t* status) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  for (int b = 0; b < B; ++b) {
+    const int L = seq_len[b] + 1;  // the next step writes slot L
+    if (L < 1 || L >= max_ctx) {
+      atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    if (paged && L % page_size == 0) {
+      const int j = L / page_size;
+      int32_t* slot = table + (size_t)b * pages_per_seq + j;
+      if (j >= pages_per_seq) {
+        atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      if (*slot < 0) {
+        const int nf = n_free ? *n_free : 0;
+        const int pid = (free_pages && nf > 0) ? free_pages[nf - 1] : -1;
+        if (pid < 0 || pid >= max_pages) {
+          atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+          continue;
+        }
+        *slot = pid;
+        *n_free = nf - 1;
+      }
+    }
+    seq_len[b] = L;
+  }
+}
+
 }  // namespace
 
+int launch_gen_advance(const dualflow_config& c, int32_t* seq_len, int batch, int32_t* table, int32_t* free_pages,
+                       int32_t* n_free, int32_t* status, cudaStream_t s) {
+  const int pps = c.paged ? (c.max_ctx + c.page_size - 1) / c.page_size : 0;
+  gen_advance_kernel<<<1, 32, 0, s>>>(seq_len, batch, c.max_ctx, c.paged, c.page_size, table, pps, c.max_pages,
+                                      free_pages, n_free, status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
 int launch_mixture_head(const float* logits, int batch, int vocab, const float* u, float* alpha, float* p_mix,
-                        int32_t* token, cudaStream_t s) {
+                        int32_t* token, int32_t* token2, int aux_on, cudaStream_t s) {
   int S = (vocab + 4095) / 4096;
   S = S < 1 ? 1 : (S > kMixMaxCluster ? kMixMaxCluster : S);
   cudaLaunchConfig_t lc = {};
@@ -274,7 +323,8 @@ int launch_mixture_head(const float* logits, int batch, int vocab, const float* 
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, mixture_head_kernel, logits, batch, vocab, u, alpha, p_mix, token) == cudaSuccess
+  return cudaLaunchKernelEx(&lc, mixture_head_kernel, logits, batch, vocab, u, alpha, p_mix, token, token2,
+                            aux_on ? 0 : 1) == cudaSuccess
              ? DF_OK
              : DF_ERR_CUDA;
 }

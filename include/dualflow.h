@@ -208,6 +208,29 @@ DF_API int dualflow_expert_ids(dualflow_ctx* ctx, int32_t* ids, int32_t batch, d
 DF_API int dualflow_mixture_head(dualflow_ctx* ctx, const float* logits, int32_t batch, const float* u, float* alpha,
                                  float* p_mix, int32_t* token, dualflow_stream stream);
 
+/* The decode loop: n_steps decode steps in which each step's chosen token is the next step's input
+ * (the technical summary's decode phase, "Custos de Inferencia vs. Treinamento": the auxiliary flow
+ * is on at every generated token). Step t runs dualflow_step on the loop's token buffer, then the
+ * mixture head and token choice of dualflow_mixture_head (from the primary's distribution alone
+ * when aux_on = 0), then advances the cache: seq_len[b] += 1 and, for a paged cache, when the next
+ * slot seq_len[b] opens a logical page whose table entry is -1, the top entry of the free-page
+ * list is popped into the table (sequences in order b = 0, 1, ...). Everything stays on the GPU.
+ *   tokens      device int32 [batch]: the first step's input tokens
+ *   u           device fp32 [n_steps, batch] uniforms in [0, 1) (sampling), or NULL (argmax)
+ *   tokens_out  device int32 [n_steps, batch]: token chosen after each step
+ *   logits      device fp32 [2, batch, vocab]: workspace, holds the last step's logits on return
+ *   logits_all  device fp32 [n_steps, 2, batch, vocab] or NULL: every step's logits
+ *   free_pages  device int32 [*n_free], n_free device int32 (paged caches; NULL: no new pages)
+ * kv->seq_len (device) is advanced in place by n_steps and kv->page_table written as above; the
+ * first step's slot must already be mapped, as for dualflow_step. Asynchronous on `stream`;
+ * nothing is allocated. A length reaching max_ctx, a page slot beyond the table or an empty free
+ * list latches DF_ERR_DEVICE_BOUNDS and that sequence stops advancing (its later steps overwrite
+ * the same slot). Host errors as for dualflow_step; n_steps < 0 is DF_ERR_SHAPE, 0 does nothing. */
+DF_API int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+                             const int32_t* tokens, int32_t batch, int32_t n_steps, const float* u,
+                             int32_t* tokens_out, float* logits, float* logits_all, int32_t* free_pages,
+                             int32_t* n_free, int32_t aux_on, dualflow_stream stream);
+
 /* One whole decode step of both flows: embeddings E1[tok], E2[tok] -> n_layers x {RMSNorm,
  * QKV with query coupling, RoPE and primary-only KV append, shared-KV attention, O projection,
  * coupled MLP} -> final RMSNorm -> shared LM head.

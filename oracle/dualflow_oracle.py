@@ -417,14 +417,14 @@ def mixture_head(logits1: np.ndarray, logits2: np.ndarray):
     return alpha, pm, int(np.argmax(pm))
 
 
-def choose_token(logits1: np.ndarray, logits2: np.ndarray | None, u: float | None = None) -> int:
-    """The next token from one sequence's logits (R11, R12): from the mixture of both flows, or from
-    the primary's distribution alone when logits2 is None; argmax, or a sample with uniform u."""
+def choice_distribution(logits1: np.ndarray, logits2: np.ndarray | None) -> np.ndarray:
+    """The distribution the next token is chosen from (R11, R12): the mixture of both flows, or the
+    primary's softmax alone when logits2 is None."""
     if logits2 is None:
         p = softmax(np.asarray(logits1, F64))
     else:
         _, p, _ = mixture_head(logits1, logits2)
-    return int(np.argmax(p)) if u is None else sample_inverse_cdf(p, u)
+    return p
 
 
 def append_entry(cache, b: int, L: int, k: np.ndarray, v: np.ndarray) -> None:
@@ -445,8 +445,9 @@ def generate(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequence, 
              ids_override: Callable | None = None) -> dict:
     """The decode loop (R12): n_steps decode steps of every sequence; after step t the appended
     entries join the caches, seq_len grows by one, and token[t, b] (R11; u[t, b] when sampling)
-    feeds step t + 1. caches are written in place. token_override(t, b, token) may replace a
-    choice (a caller resolving a near tie the way another implementation took it).
+    feeds step t + 1. caches are written in place. token_override(t, b, token, p) may replace a
+    choice made from distribution p (a caller resolving a near tie the way another implementation
+    took it).
 
     Returns tokens [n_steps, B], logits [n_steps, 2, B, V] and the final seq_len."""
     tokens = np.array(tokens, dtype=np.int64)
@@ -462,10 +463,10 @@ def generate(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequence, 
             for b in range(B):
                 append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])
         for b in range(B):
-            tok = choose_token(r["logits"][0, b], r["logits"][1, b] if aux_on else None,
-                               None if u is None else float(u[t, b]))
+            p = choice_distribution(r["logits"][0, b], r["logits"][1, b] if aux_on else None)
+            tok = int(np.argmax(p)) if u is None else sample_inverse_cdf(p, float(u[t, b]))
             if token_override is not None:
-                tok = int(token_override(t, b, tok))
+                tok = int(token_override(t, b, tok, p))
             out_tok[t, b] = tok
         L = L + 1
         tokens = out_tok[t].copy()
