@@ -503,6 +503,33 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         t = torch.tensor([e2e_s], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t.item())
+
+    # the decode loop: dualflow_generate (step, mixture head, greedy choice, length advance) for
+    # gen_n tokens; the lengths are restored before each repetition so the context stays the
+    # workload's
+    gen_n, gen_reps = 16, 3
+    gen = None
+    if w.max_ctx - 1 - int(run.seq_len_np.max()) >= gen_n:
+        seq0 = run.seq_len.clone()
+        tok_out = torch.empty((gen_n, w.batch), dtype=torch.int32, device=dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            for r in range(2 + gen_reps):
+                if r == 2:
+                    g0.record(stream)
+                run.seq_len.copy_(seq0)
+                dfl.dualflow_generate(run.ctx, run.weights, run.kv, run.tokens, w.batch, gen_n, tok_out, run.logits,
+                                      stream=stream)
+            g1.record(stream)
+            run.seq_len.copy_(seq0)
+        g1.synchronize()
+        gen_ms = g0.elapsed_time(g1) / (gen_reps * gen_n)
+        st = dfl.dualflow_sync_status(run.ctx)
+        if st != 0:
+            raise RuntimeError(f"device status after the decode loop: {dfl.dualflow_status_string(st)}")
+        gen = {"api": "dualflow_generate (greedy choice from the mixture head, in-loop length advance)",
+               "tokens_per_loop": gen_n, "ms_per_token_step": gen_ms,
+               "tokens_per_s": world * w.batch / (gen_ms * 1e-3)}
     run.close()
     if rank != 0:
         return None
@@ -543,6 +570,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         "e2e": {"value": world * w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(tok.numel() * 4),
                 "d2h_bytes_per_step": int(out.numel() * 4),
                 "api": "dualflow_step_host (pinned host tokens in, host logits out, stream sync per step)"},
+        "generate": gen,
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,
         "clocks": sampler.summary(),
