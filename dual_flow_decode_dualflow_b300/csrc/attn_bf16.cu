@@ -12,7 +12,10 @@
 // (running max via warp shuffles), merged at the end of a segment.
 //
 // Work split (flash-decoding): all (b, g, tile) triples are laid end to end and cut into equal
-// contiguous ranges, one per CTA, so ragged lengths balance across the GPU. A pair cut across
+// contiguous ranges, one per CTA, so ragged lengths balance across the GPU. When every pair has the
+// same length and the grid holds k >= 1 CTAs per pair, each pair goes to k CTAs instead, CTA j
+// taking the pair's tiles j, j + k, j + 2k, ...: no CTA changes pair, and the pair's CTAs stream
+// through its cache rows side by side. A pair cut across
 // several CTAs writes per-CTA partials (O, max, sum); the last CTA to arrive (atomic counter, no
 // waiting) merges them in CTA order, with all four consumer warps, so the result does not depend
 // on arrival order. The query rows of a pair reach shared memory by bulk copy with the pair's
@@ -57,9 +60,10 @@ __device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, vol
   return true;
 }
 
-// Walks the (b, g, tile) sequence in order.
+// Walks a CTA's (b, g, tile) sequence: consecutive tiles of the global order (stride 0), or every
+// stride-th tile of one pair.
 struct Walker {
-  int b, g, j, tiles_b;
+  int b, g, j, tiles_b, stride;
 };
 
 __device__ __forceinline__ int tiles_of(const int* sched, int b, int Hkv) { return (sched[b + 1] - sched[b]) / Hkv; }
@@ -75,6 +79,10 @@ __device__ __forceinline__ void walker_seek(Walker& w, const int* sched, int B, 
 }
 
 __device__ __forceinline__ void walker_next(Walker& w, const int* sched, int B, int Hkv) {
+  if (w.stride > 0) {
+    w.j += w.stride;
+    return;
+  }
   if (++w.j < w.tiles_b) return;
   w.j = 0;
   if (++w.g < Hkv) return;
@@ -145,6 +153,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
   // pair has the same number of tiles and the grid holds k >= 1 CTAs per pair, C = pairs * k: the
   // cuts fall on pair boundaries, every CTA works on one pair, and no CTA pays for a pair change.
   int C = (int)(T < (long long)gridDim.x ? T : (long long)gridDim.x);
+  int kpp = 0;  // > 0: kpp CTAs per pair, each taking every kpp-th tile of its pair
   {
     const int per = B > 0 ? sched[1] / Hkv : 0;  // tiles of one pair of sequence 0
     const int pairs = B * Hkv;
@@ -152,23 +161,39 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
       bool uniform = true;
       for (int b = 1; b < B && uniform; ++b) uniform = (sched[b + 1] - sched[b] == per * Hkv);
       if (uniform) {
-        const int k = min((int)gridDim.x / pairs, per);
-        C = pairs * k;
+        kpp = min((int)gridDim.x / pairs, per);
+        C = pairs * kpp;
       }
     }
   }
+  // This CTA's tiles. Contiguous: global tiles [t0, t1). Per pair: CTA c takes tiles j0, j0 + kpp,
+  // ... of pair c / kpp (j0 = c % kpp), so the pair's first tiles are every CTA's first tiles. The
+  // owners of a pair's partials are the same CTAs in both cases (owner_of below).
   const long long t0 = (c < C) ? T * c / C : 0, t1 = (c < C) ? T * (c + 1) / C : 0;
+  int n_my = (int)(t1 - t0);
+  Walker w0;
+  if (kpp > 0) {
+    const int pr = c / kpp, j0 = c % kpp, per = (c < C) ? tiles_of(sched, pr / Hkv, Hkv) : 0;
+    n_my = (c < C && j0 < per) ? (per - j0 + kpp - 1) / kpp : 0;
+    w0.b = pr / Hkv;
+    w0.g = pr % Hkv;
+    w0.j = j0;
+    w0.tiles_b = per;
+    w0.stride = kpp;
+  } else if (n_my > 0) {
+    walker_seek(w0, sched, B, Hkv, (int)t0);
+    w0.stride = 0;
+  }
 
   if (warp == kConsumers) {
     // ------------------------------ TMA producer ------------------------------
-    if (lane == 0 && t1 > t0) {
+    if (lane == 0 && n_my > 0) {
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
       const uint64_t pol = policy_evict_first();
       const int nf = a.aux_on ? 2 : 1;
       const uint32_t qbytes = (uint32_t)(nf * G * kHeadDim * 2);
-      Walker w;
-      walker_seek(w, sched, B, Hkv, (int)t0);
+      Walker w = w0;
       // Under programmatic dependent launch the first stages' tiles are requested before waiting
       // for the preceding kernel, unless they hold the slot that kernel appends (seq_len[b] when
       // extra = 1): the older cache positions are never written by it. The query rows of a
@@ -182,7 +207,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
                     reinterpret_cast<const __nv_bfloat16*>(a.q) + (((size_t)f * B + b) * Hq + g * G) * kHeadDim,
                     (uint32_t)(G * kHeadDim * 2), &full[s]);
       };
-      for (long long t = t0, i = 0; t < t1; ++t, ++i) {
+      for (int i = 0; i < n_my; ++i) {
         const int s = (int)(i % kStagesA);
         const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
         const int key0 = w.j * kAttnTileKeys;
@@ -194,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
           npend = 0;
         }
         if (!wait_or_fail(&empty[s], ph ^ 1u, err, P.status)) break;
-        const bool seg_start = (w.j == 0) || (t == t0);
+        const bool seg_start = (w.j == 0) || (i == 0);
         uint8_t* Kst = smem + s * kStageBytes;
         uint8_t* Vst = Kst + kTileBytes;
         if (!a.paged) {
@@ -263,7 +288,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
       for (int i = threadIdx.x; i < Hq * kHeadDim; i += kConsumers * 32)
         o[((size_t)f * B + b) * Hq * kHeadDim + i] = __float2bfloat16_rn(0.f);
   }
-  if (t1 <= t0) return;
+  if (n_my <= 0) return;
 
   const int kw = 16 * warp;
   const int qn = lane >> 2;          // query row this lane feeds into the B fragment
@@ -277,10 +302,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
   for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   uint32_t qb[8][2];
 
-  Walker w;
-  walker_seek(w, sched, B, Hkv, (int)t0);
+  Walker w = w0;
   bool new_seg = true;
-  for (long long t = t0, i = 0; t < t1; ++t, ++i) {
+  for (int i = 0; i < n_my; ++i) {
     const int Leff = lens[w.b];
     const int s = (int)(i % kStagesA);
     const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
@@ -384,7 +408,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
     if (lane == 0) mbar_arrive(&empty[s]);
 
     // ---- end of this CTA's segment of pair (b, g): merge warps, write result or partial ----
-    const bool seg_end = (w.j == w.tiles_b - 1) || (t == t1 - 1);
+    const bool seg_end = (w.j == w.tiles_b - 1) || (i == n_my - 1);
     if (seg_end) {
 #pragma unroll
       for (int off = 4; off < 32; off <<= 1) {
