@@ -41,6 +41,7 @@ namespace {
 
 constexpr int kStages = 4;                 // most pipeline stages (barrier arrays are sized for it)
 constexpr int kStageBudget = 96 * 1024;    // stage bytes that still let two CTAs share an SM
+constexpr int kStageBudget3 = 68 * 1024;   // ... three CTAs
 constexpr int kThreads = 128;
 constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per stage
 constexpr int kSplitMaxRows = 208;                    // padded activation rows a split CTA can hold
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* recv_bar = done + 1;                             // S > 1: the cluster's partials arrived
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
   float* rstd_s = reinterpret_cast<float*>(tmem_slot + 4);  // [256] 1 / rms of each activation row
+  int* sel_s = reinterpret_cast<int*>(rstd_s + kGemmMaxAct);  // [256] grouped: row selected this expert
   // After the main loop the pipeline bytes hold, for S == 1, the accumulator tile acc[n][128];
   // for S > 1 and staged partials, the partial split into S slices [S][n_pad * 2nl + 8] (the pad
   // spreads the slices over the banks) followed by the receive area [S][n_pad][2nl]; for pushed
@@ -335,10 +337,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(&empty[s]);
     }
     umma_commit(done);
-  } else if (warp >= 2 && a.ss_in != nullptr) {
-    // idle during the main loop: 1 / rms of every activation row, from the producer's partials
+  } else if (warp >= 2 && (a.ss_in != nullptr || a.sel_pos != nullptr)) {
+    // idle during the main loop: which rows selected this launch's expert (grouped launches) and
+    // 1 / rms of every activation row, from the producer's partials
     griddep_wait();
-    for (int n = threadIdx.x - 64; n < m; n += 64) {
+    if (a.sel_pos != nullptr)
+      for (int n = threadIdx.x - 64; n < m; n += 64) sel_s[n] = a.sel_pos[(size_t)n * a.n_groups + grp] >= 0;
+    for (int n = threadIdx.x - 64; a.ss_in != nullptr && n < m; n += 64) {
       const float* row = a.ss_in + (size_t)n * a.ss_ld;
       float ss = 0.f;
       int q = 0;
@@ -516,10 +521,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (EPI == EPI_MOE_GATEUP) {
         // expert grp: rows that selected it; the auxiliary row couples to the primary row only
         // when the primary selected the same expert
-        const int E = a.n_groups, j = tile * 64 + fa;
+        const int j = tile * 64 + fa;
         __nv_bfloat16* u = reinterpret_cast<__nv_bfloat16*>(a.y) + (size_t)grp * a.y_group_stride;
-        const bool s1 = a.sel_pos[(size_t)n * E + grp] >= 0;
-        const bool s2 = a.m_a > 0 && a.sel_pos[(size_t)(a.m_p + n) * E + grp] >= 0;
+        const bool s1 = sel_s[n] != 0;
+        const bool s2 = a.m_a > 0 && sel_s[a.m_p + n] != 0;
         const float4 u1 = f4_silu_mul(lo, hi);
         if (s1) st_bf16x4(u, (size_t)n * a.ldy + j, u1);
         if (s2) {
@@ -535,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           st_bf16x4(u, (size_t)(a.m_p + n) * a.ldy + j, u2);
         }
       } else if (EPI == EPI_MOE_DOWN) {
-        if (a.sel_pos[(size_t)n * a.n_groups + grp] >= 0) {
+        if (sel_s[n] != 0) {
           float* y = reinterpret_cast<float*>(a.y) + (size_t)grp * a.y_group_stride + (size_t)n * a.ldy;
           if (fg < a.n_out) *reinterpret_cast<float4*>(y + fg) = lo;
           if (fg + 64 < a.n_out) *reinterpret_cast<float4*>(y + fg + 64) = hi;
@@ -739,8 +744,14 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   // data region: the pipeline stages; after the main loop the partial tile (512 B per activation
   // row) or, when split, the staged slices plus the receive area (1 KB per row + bank pads). Then
   // the barriers, the TMEM address slot and the 256-float row-scale array.
-  // as many stages (up to 4) as fit the budget that keeps two CTAs per SM
-  p.stages = kStageBudget / (kABytes + p.n_pad * 128);
+  // as many stages (up to 4) as fit the budget that keeps two CTAs per SM; a grid of more than two
+  // CTAs per SM (grouped launches) keeps three per SM on fewer stages, so that it runs as one wave
+  const int ctas = p.n_tiles * p.splits * groups;
+  uint32_t tcols = 32;
+  while ((int)tcols < p.n_pad) tcols <<= 1;
+  const bool three = ctas > 2 * ctx->num_sms && ctas <= 3 * ctx->num_sms && 3 * tcols <= 512 &&
+                     2 * (kABytes + p.n_pad * 128) <= kStageBudget3 && 512 * p.n_pad <= kStageBudget3;
+  p.stages = (three ? kStageBudget3 : kStageBudget) / (kABytes + p.n_pad * 128);
   p.stages = p.stages > kStages ? kStages : (p.stages < 2 ? 2 : p.stages);
   const int pipe = p.stages * (kABytes + p.n_pad * 128);
   // split-K partials: staged and bulk-copied when the staging fits in the pipeline bytes, else
@@ -749,7 +760,7 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   p.push_async = (p.splits > 1 && staged > pipe) ? 1 : 0;
   const int parts = p.splits == 1 ? 512 * p.n_pad : p.push_async ? 512 * (p.n_pad + 4) : staged;
   p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
-  const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 4;
+  const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 8;
   switch (a.epi) {
     case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(mw, mx, mpf, p, smem, s);
     case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(mw, mx, mpf, p, smem, s);
