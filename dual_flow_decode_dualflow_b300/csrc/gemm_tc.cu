@@ -13,12 +13,13 @@
 //
 // When the output has too few tiles to fill the GPU the reduction dimension is split across the S
 // CTAs of a thread-block cluster (S <= 8). Every CTA owns a 1/S slice of the tile's features --
-// feature i and its RoPE / gate-up partner i + 64 travel together, four at a time -- and receives
-// the other ranks' partials of that slice in its shared memory: either staged from TMEM and sent
-// by one bulk copy per destination, or, when staging would not fit in the pipeline's bytes, sent
-// straight from registers by 16-byte asynchronous remote stores. The owner sums the S partials in
-// rank order (deterministic, and independent of which flows are present) and runs the epilogue on
-// its slice:
+// feature i and its RoPE / gate-up partner i + 64 travel together, four at a time. Each CTA stages
+// its partial tile from TMEM in its own shared memory and, after a cluster barrier, the owner of a
+// slice reads the S partials of it over distributed shared memory (16-byte loads, four ranks in
+// flight); when staging would not fit in the pipeline's bytes, the partials are instead pushed
+// straight from registers into the owners' shared memory by 16-byte asynchronous remote stores.
+// The owner sums the S partials in rank order (deterministic, and independent of which flows are
+// present) and runs the epilogue on its slice:
 //   EPI_QKV      q1 = Wq.x1, q2 = Wq.x2 + a (*) q1 (before RoPE), RoPE(q1, q2, k1) at position
 //                seq_len[b], q stored bf16, primary k1/v1 appended to the cache at slot seq_len[b]
 //                ("Atencao de KV Compartilhada Assimetrica": the auxiliary flow writes no K/V)
@@ -55,7 +56,8 @@ struct GemmParams {
   int vec_ok;    // y / u rows allow 16-byte (fp32) or 8-byte (bf16) vector access
   int stages;    // pipeline stages in use (2..kStages)
   int region;    // bytes of the data region (pipeline stages, later the partial tiles)
-  int push_async;  // split-K partials pushed by 16-byte asynchronous stores (else staged + bulk copy)
+  int push_async;  // split-K partials pushed by 16-byte asynchronous stores into the owners' areas
+  int pull;        // split-K partials staged locally and read by their owners over DSMEM
   int32_t* status;
 };
 
@@ -133,13 +135,14 @@ __device__ __forceinline__ size_t cache_slot(const GemmArgs& a, int b, int hk, i
 }
 
 // Where a CTA finds the fp32 partial tiles of its output slice. S == 1: its own accumulator tile
-// acc[n][128]. S > 1: the S partials of its slice received from the cluster's CTAs, from rank r,
-// local feature fl (fl < nl: feature lo0 + fl; fl >= nl: its partner lo0 + 64 + fl - nl); row-major
-// recv[r][n][2nl] when staged and bulk-copied, feature-major recv[r][fl][n_pad + 4] when pushed by
-// asynchronous stores.
+// acc[n][128]. S > 1, local feature fl of the slice (fl < nl: feature lo0 + fl; fl >= nl: its
+// partner lo0 + 64 + fl - nl): pulled, rank r's staged slice [n][2nl] row-major in rank r's shared
+// memory (rb[r]); pushed, this CTA's receive area recv[r][fl][n_pad + 4], feature-major.
 struct RedSrc {
   const float* base;
-  int S, n_pad, nl, transposed;
+  int S, n_pad, nl;
+  int remote;       // row-major slices read from the cluster's CTAs at rb[k] (shared::cluster addresses)
+  uint32_t rb[8];
 };
 
 __device__ __forceinline__ float4 col4(const float* e, int stride) {
@@ -155,15 +158,25 @@ __device__ __forceinline__ void reduce_pair(const RedSrc& r, int lo0, int n, int
     hi = *reinterpret_cast<const float4*>(e + 64);
     return;
   }
-  if (!r.transposed) {
-    const int nfs = 2 * r.nl;
-    const float* e = r.base + n * nfs + 4 * qd;
-    const int rs = r.n_pad * nfs;
-    lo = *reinterpret_cast<const float4*>(e);
-    hi = *reinterpret_cast<const float4*>(e + r.nl);
-    for (int k = 1; k < r.S; ++k) {
-      lo = f4_add(lo, *reinterpret_cast<const float4*>(e + k * rs));
-      hi = f4_add(hi, *reinterpret_cast<const float4*>(e + k * rs + r.nl));
+  if (r.remote) {
+    const uint32_t off = (uint32_t)((n * 2 * r.nl + 4 * qd) * 4), offh = off + (uint32_t)(r.nl * 4);
+    // four ranks' partials in flight at a time, summed in rank order
+#pragma unroll
+    for (int k0 = 0; k0 < 8; k0 += 4) {
+      if (k0 >= r.S) break;
+      float4 pl[4], ph[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k0 + k < r.S) {
+          pl[k] = ld_dsmem_f4(r.rb[k0 + k] + off);
+          ph[k] = ld_dsmem_f4(r.rb[k0 + k] + offh);
+        }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k0 + k < r.S) {
+          lo = (k0 + k == 0) ? pl[k] : f4_add(lo, pl[k]);
+          hi = (k0 + k == 0) ? ph[k] : f4_add(hi, ph[k]);
+        }
     }
     return;
   }
@@ -202,7 +215,7 @@ __device__ __forceinline__ void store4(const GemmArgs& a, int vec_ok, int n, int
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (see the stage budgets)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_pf, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -236,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int S = p.splits;
   const int nl = 64 / S, lo0 = split * nl, nq = nl / 4, nfs = 2 * nl;
   const int fstride = p.n_pad + 4;                 // pushed: floats per feature row
-  const int slice_floats = p.push_async ? nfs * fstride : p.n_pad * nfs;  // one rank's slice partial
-  const int stage_stride = p.n_pad * nfs + 8;      // staged slices, bank-spread
-  float* recv_s = p.push_async ? acc_s : acc_s + S * stage_stride;
+  const int slice_floats = nfs * fstride;          // pushed: one rank's slice partial
+  const int stage_stride = p.n_pad * nfs + 8;      // pulled: staged slices, bank-spread
+  float* recv_s = acc_s;                           // pushed: the receive area
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(recv_bar, 1);
     fence_mbar_init();
     // the S slices of this CTA's output arrive by bulk copy from the cluster's CTAs
-    if (S > 1) mbar_arrive_expect_tx(recv_bar, (uint32_t)(S * nfs * p.n_pad * 4));
+    if (S > 1 && p.push_async) mbar_arrive_expect_tx(recv_bar, (uint32_t)(S * nfs * p.n_pad * 4));
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_x);
   }
@@ -372,17 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* dst = acc_s + tf;                      // S == 1: acc[n][128]
   int dstride = kGemmTileN;
   uint32_t adst = 0, abar = 0;
-  if (S > 1) {
-    // this CTA's pipeline buffers are free: the cluster's CTAs may write into them once all arrive
+  if (S > 1 && p.push_async) {
+    // the owners' receive areas are their pipeline bytes: written once every CTA has drained its own
     cluster_arrive();
-    if (p.push_async) {
-      cluster_wait();
-      adst = mapa_shared(smem_u32(recv_s + split * slice_floats + fl * fstride), (uint32_t)dst_rank);
-      abar = mapa_shared(smem_u32(recv_bar), (uint32_t)dst_rank);
-    } else {
-      dst = acc_s + dst_rank * stage_stride + fl;  // staged slice of rank dst_rank, row-major
-      dstride = nfs;
-    }
+    cluster_wait();
+    adst = mapa_shared(smem_u32(recv_s + split * slice_floats + fl * fstride), (uint32_t)dst_rank);
+    abar = mapa_shared(smem_u32(recv_bar), (uint32_t)dst_rank);
+  } else if (S > 1) {
+    dst = acc_s + dst_rank * stage_stride + fl;  // pulled: the staged slice of rank dst_rank, row-major
+    dstride = nfs;
   }
   // four 16-column TMEM loads in flight per wait
   for (int c0 = 0; c0 < p.n_pad; c0 += 64) {
@@ -410,29 +421,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) dst[(c0 + 16 * q + j) * dstride] = __uint_as_float(v[q][j]);
     }
   }
-  if (S > 1 && !p.push_async) fence_proxy_async_smem();  // staged slices are read by the bulk-copy engine
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, ncols);
   griddep_wait();  // the epilogue reads and writes buffers of the preceding kernels
-  if (S > 1) {
-    if (!p.push_async) {
-      // every CTA pushes staged slice r into rank r's receive area, one bulk copy each
-      cluster_wait();  // every CTA of the cluster has drained its pipeline
-      if (threadIdx.x == 0) {
-        const uint32_t src0 = smem_u32(acc_s), dst_local = smem_u32(recv_s + split * slice_floats);
-        const uint32_t bar_local = smem_u32(recv_bar);
-        for (int r = 0; r < S; ++r)
-          bulk_copy_to_cluster(mapa_shared(dst_local, (uint32_t)r), src0 + (uint32_t)(r * stage_stride * 4),
-                               (uint32_t)(slice_floats * 4), mapa_shared(bar_local, (uint32_t)r));
-      }
-    }
+  if (S > 1 && p.pull) {
+    cluster_arrive();  // this CTA's partials are staged
+    cluster_wait();
+  } else if (S > 1) {
     if (!mbar_wait(recv_bar, 0)) set_status(p.status, DF_ERR_TIMEOUT);
-    cluster_arrive();  // this CTA has received everything sent to it (its own copies are done too)
+    cluster_arrive();  // this CTA has received everything pushed to it (its own pushes are done too)
   }
   RedSrc red;
   red.base = S == 1 ? acc_s : recv_s;
-  red.transposed = p.push_async;
+  red.remote = S > 1 && p.pull;
+#pragma unroll
+  for (int k = 0; k < 8; ++k)
+    red.rb[k] = (red.remote && k < S) ? mapa_shared(smem_u32(acc_s + split * stage_stride), (uint32_t)k) : 0u;
   red.S = S;
   red.n_pad = p.n_pad;
   red.nl = nl;
@@ -642,7 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  // no CTA may leave before every copy into or out of its shared memory has completed
+  // no CTA may leave before every copy into or out of its shared memory has completed (or every
+  // read of its staged partials)
+  if (S > 1 && p.pull) cluster_arrive();
   if (S > 1) cluster_wait();
 }
 
@@ -754,11 +761,12 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   p.stages = (three ? kStageBudget3 : kStageBudget) / (kABytes + p.n_pad * 128);
   p.stages = p.stages > kStages ? kStages : (p.stages < 2 ? 2 : p.stages);
   const int pipe = p.stages * (kABytes + p.n_pad * 128);
-  // split-K partials: staged and bulk-copied when the staging fits in the pipeline bytes, else
-  // pushed from TMEM by asynchronous stores (no staging, so two CTAs still share an SM)
-  const int staged = 1024 * p.n_pad + 32 * p.splits;
-  p.push_async = (p.splits > 1 && staged > pipe) ? 1 : 0;
-  const int parts = p.splits == 1 ? 512 * p.n_pad : p.push_async ? 512 * (p.n_pad + 4) : staged;
+  // split-K partials: staged in the CTA's own pipeline bytes and pulled by their owners when the
+  // staging fits, else pushed from TMEM by asynchronous stores into the owners' receive areas
+  const int staged_pull = 512 * p.n_pad + 32 * p.splits;  // the S staged slices
+  p.pull = p.splits > 1 && staged_pull <= pipe;
+  p.push_async = (p.splits > 1 && !p.pull) ? 1 : 0;
+  const int parts = p.splits == 1 ? 512 * p.n_pad : p.push_async ? 512 * (p.n_pad + 4) : staged_pull;
   p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
   const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 8;
   switch (a.epi) {

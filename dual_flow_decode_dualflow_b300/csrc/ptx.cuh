@@ -274,16 +274,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, floa
                : "memory");
 }
 
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from this CTA's shared
-// memory to shared memory of a CTA in the cluster (dst and its mbarrier given as shared::cluster
-// addresses, e.g. from mapa_shared); completion is counted in bytes on that mbarrier.
-__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "r"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 // Programmatic dependent launch: wait until the preceding kernel of the stream has completed and
 // its writes are visible (a no-op without the launch attribute); allow the next kernel to launch.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
