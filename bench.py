@@ -487,22 +487,40 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
                 fam_n = [a + b for a, b in zip(fam_n, n)]
     dfl.dualflow_set_profiling(run.ctx, 0)
 
-    # end to end through the host-buffer C-ABI call: tokens H2D, step, logits D2H, every step
+    # end to end through the host-buffer decode call a user makes: the step's input tokens copied in
+    # from pinned host memory, one decode step (step, mixture head, token choice, length advance),
+    # the chosen tokens copied back, stream synchronised, every step; the length is restored before
+    # each call so the context stays the workload's
     tok = torch.from_numpy(run.tokens_np.copy()).pin_memory()
-    out = torch.empty((2, w.batch, w.vocab), dtype=torch.float32).pin_memory()
+    tok_out = torch.empty((1, w.batch), dtype=torch.int32).pin_memory()
+    seq_keep = run.seq_len.clone()
+
+    def e2e_call():
+        with torch.cuda.stream(stream):
+            run.seq_len.copy_(seq_keep)
+        dfl.dualflow_generate_host(run.ctx, run.weights, run.kv, tok, w.batch, 1, tok_out, stream=stream)
+
     for _ in range(3):
-        dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
+        e2e_call()
     if dist:
         dist.barrier()
     e2e_steps = max(args.steps // 2, 3)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
-        dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
+        e2e_call()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
+    # the same with the full logits [2, B, V] copied back every step instead of the tokens
+    out = torch.empty((2, w.batch, w.vocab), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
+    e2e_logits_s = (time.perf_counter() - t0) / e2e_steps
     if dist:
-        t = torch.tensor([e2e_s], device=dev)
+        t = torch.tensor([e2e_s, e2e_logits_s], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+        e2e_s, e2e_logits_s = float(t[0].item()), float(t[1].item())
 
     # the decode loop: dualflow_generate (step, mixture head, greedy choice, length advance) for
     # gen_n tokens; the lengths are restored before each repetition so the context stays the
@@ -568,8 +586,12 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         "cpu_baseline": {"value": w.batch / cpu_s, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": world * w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(tok.numel() * 4),
-                "d2h_bytes_per_step": int(out.numel() * 4),
-                "api": "dualflow_step_host (pinned host tokens in, host logits out, stream sync per step)"},
+                "d2h_bytes_per_step": int(tok_out.numel() * 4),
+                "api": "dualflow_generate_host, one step per call (pinned host tokens in, the step's chosen "
+                       "tokens out, stream sync per step)"},
+        "e2e_logits": {"value": world * w.batch / e2e_logits_s, "unit": "tokens/s",
+                       "h2d_bytes_per_step": int(tok.numel() * 4), "d2h_bytes_per_step": int(out.numel() * 4),
+                       "api": "dualflow_step_host (pinned host tokens in, host logits [2, B, V] out, sync per step)"},
         "generate": gen,
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,

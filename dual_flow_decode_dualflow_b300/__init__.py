@@ -24,7 +24,7 @@ C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dual
                "dualflow_stacked_linear", "dualflow_coupled_mlp", "dualflow_step", "dualflow_step_host",
                "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
                "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head",
-               "dualflow_generate")
+               "dualflow_generate", "dualflow_generate_host")
 DF_PROF_FAMILIES = 8
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
@@ -88,6 +88,8 @@ def load_library(path: str = LIB_PATH):
         "dualflow_mixture_head": ([vp, vp, i32, vp, vp, vp, vp, vp], i32),
         "dualflow_generate": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, vp, vp, vp, vp,
                                i32, vp], i32),
+        "dualflow_generate_host": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, i32, vp],
+                                   i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -225,6 +227,14 @@ def dualflow_generate(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens, bat
                                           _ptr(tokens_out), _ptr(logits), _ptr(logits_all), _ptr(free_pages),
                                           _ptr(n_free), aux_on, _stream(stream))
     _check("dualflow_generate", rc)
+
+
+def dualflow_generate_host(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens_host, batch: int, n_steps: int,
+                           tokens_out_host, u_host=None, aux_on: int = 1, stream=None) -> None:
+    """The decode loop with host token buffers (pinned CPU tensors): n_steps <= 256."""
+    rc = load_library().dualflow_generate_host(ctx, ctypes.byref(w), ctypes.byref(kv), _ptr(tokens_host), batch,
+                                               n_steps, _ptr(u_host), _ptr(tokens_out_host), aux_on, _stream(stream))
+    _check("dualflow_generate_host", rc)
 
 
 def dualflow_sync_status(ctx, stream=None) -> int:

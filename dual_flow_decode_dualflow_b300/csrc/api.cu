@@ -584,6 +584,10 @@ int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
   }
   if (dalloc(&ctx->status, sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
   if (dalloc(&ctx->gen_tokens, (size_t)c.max_batch * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->gen_out_dev, (size_t)kGenHostMaxSteps * c.max_batch * sizeof(int32_t)) != DF_OK)
+    return fail(DF_ERR_OOM);
+  if (dalloc(&ctx->gen_u_dev, (size_t)kGenHostMaxSteps * c.max_batch * sizeof(float)) != DF_OK)
+    return fail(DF_ERR_OOM);
   cudaMemset(ctx->status, 0, sizeof(int32_t));
   // decode attention: persistent grid of 2 CTAs per SM; partial slots = pairs + CTAs
   ctx->attn_ctas = 2 * ctx->num_sms;
@@ -636,7 +640,7 @@ int dualflow_free(dualflow_ctx* ctx) {
   }
   void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
                   ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss,
-                  ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids, ctx->gen_tokens};
+                  ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids, ctx->gen_tokens, ctx->gen_out_dev, ctx->gen_u_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete ctx;
@@ -842,6 +846,25 @@ int dualflow_step_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualf
   const size_t rows = aux_on ? 2 : 1;
   if (cudaMemcpyAsync(logits_host, ctx->logits_dev, rows * batch * ctx->cfg.vocab * sizeof(float),
                       cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DF_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int dualflow_generate_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+                           const int32_t* tokens_host, int32_t batch, int32_t n_steps, const float* u_host,
+                           int32_t* tokens_out_host, int32_t aux_on, dualflow_stream stream) {
+  if (!ctx || !tokens_host || !tokens_out_host) return DF_ERR_ARG;
+  if (batch <= 0 || batch > ctx->cfg.max_batch || n_steps < 0 || n_steps > kGenHostMaxSteps) return DF_ERR_SHAPE;
+  if (n_steps == 0) return DF_OK;
+  cudaStream_t s = S(stream);
+  const size_t nb = (size_t)batch * sizeof(int32_t), total = (size_t)n_steps * batch;
+  if (cudaMemcpyAsync(ctx->tokens_dev, tokens_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess) return DF_ERR_CUDA;
+  if (u_host && cudaMemcpyAsync(ctx->gen_u_dev, u_host, total * sizeof(float), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return DF_ERR_CUDA;
+  DF_TRY(dualflow_generate(ctx, w, kv, ctx->tokens_dev, batch, n_steps, u_host ? ctx->gen_u_dev : nullptr,
+                           ctx->gen_out_dev, ctx->logits_dev, nullptr, nullptr, nullptr, aux_on, stream));
+  if (cudaMemcpyAsync(tokens_out_host, ctx->gen_out_dev, total * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
     return DF_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

@@ -18,6 +18,7 @@ constexpr int kMaxGroupRows = 8;    // 2 flows x G query heads per KV head share
 constexpr int kAttnTileKeys = 64;   // keys per pipeline stage of the decode-attention kernel
 constexpr int kGemmTileN = 128;     // weight rows (output features) per tcgen05 tile
 constexpr int kGemmTileK = 64;      // reduction elements per pipeline stage (128-byte rows)
+constexpr int kGenHostMaxSteps = 256;  // steps of one dualflow_generate_host call
 constexpr int kGemmMaxAct = 256;    // activation rows (both flows) per tcgen05 tile
 
 // Partial result of one attention segment: 8 query rows x (D values + running max + sum).
@@ -136,6 +137,8 @@ struct dualflow_ctx {
   float* moe_y = nullptr;          // [E][2 * max_batch][d]
   int32_t* moe_ids = nullptr;      // [n_layers][2][max_batch][kmax] experts chosen by the last step
   int32_t* gen_tokens = nullptr;   // [max_batch] input tokens of the generation loop's next step
+  int32_t* gen_out_dev = nullptr;  // [kGenHostMaxSteps][max_batch] dualflow_generate_host staging
+  float* gen_u_dev = nullptr;      // [kGenHostMaxSteps][max_batch]
   int ss_ld = 0;                   // ceil(d / 128) tiles x 8 splits
   int32_t* tokens_dev = nullptr;   // dualflow_step_host staging
   float* logits_dev = nullptr;

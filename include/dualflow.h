@@ -231,6 +231,15 @@ DF_API int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const
                              int32_t* tokens_out, float* logits, float* logits_all, int32_t* free_pages,
                              int32_t* n_free, int32_t aux_on, dualflow_stream stream);
 
+/* dualflow_generate with HOST buffers, for contiguous caches: copies tokens_host [batch] (and
+ * u_host [n_steps, batch] if not NULL) to the device, runs n_steps of the decode loop (step, mixture
+ * head, token choice, length advance), copies the chosen tokens back to tokens_out_host
+ * [n_steps, batch] and synchronizes `stream`. 0 <= n_steps <= 256 (DF_ERR_SHAPE otherwise); the
+ * context's own buffers hold the logits. Pinned host memory gives asynchronous copies. */
+DF_API int dualflow_generate_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+                                  const int32_t* tokens_host, int32_t batch, int32_t n_steps, const float* u_host,
+                                  int32_t* tokens_out_host, int32_t aux_on, dualflow_stream stream);
+
 /* One whole decode step of both flows: embeddings E1[tok], E2[tok] -> n_layers x {RMSNorm,
  * QKV with query coupling, RoPE and primary-only KV append, shared-KV attention, O projection,
  * coupled MLP} -> final RMSNorm -> shared LM head.

@@ -202,3 +202,28 @@ def test_generate_stops_at_capacity(cuda_device):
         assert int(run.seq_len.max().item()) == w.max_ctx - 1
     finally:
         run.close()
+
+
+def test_generate_host_matches_device(cuda_device):
+    """The host-buffer decode call returns the tokens the device call chooses, bit for bit, and
+    advances the lengths the same way."""
+    w = CASES["dense_small_g4"][0]
+    n = 5
+    run = H.DeviceRun(w, cuda_device)
+    try:
+        u = _uniforms(n, w.batch, seed=9)
+        ref_tok, _ = _run_gpu(run, w, n, u)
+        assert run.status() == 0
+        run.seq_len.copy_(torch.from_numpy(run.seq_len_np))
+        tok_h = torch.from_numpy(run.tokens_np.copy()).pin_memory()
+        out_h = torch.full((n, w.batch), -7, dtype=torch.int32).pin_memory()
+        u_h = torch.from_numpy(u).pin_memory()
+        s = torch.cuda.Stream()
+        dfl.dualflow_generate_host(run.ctx, run.weights, run.kv, tok_h, w.batch, n, out_h, u_host=u_h, stream=s)
+        assert run.status() == 0
+        assert np.array_equal(out_h.numpy(), ref_tok)
+        assert np.array_equal(run.seq_len.cpu().numpy(), run.seq_len_np + n)
+        with pytest.raises(dfl.DualFlowError):
+            dfl.dualflow_generate_host(run.ctx, run.weights, run.kv, tok_h, w.batch, 257, out_h, stream=s)
+    finally:
+        run.close()
