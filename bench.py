@@ -608,6 +608,52 @@ class _Null:
         return False
 
 
+def sweep_topk_aux(w, ks, local_rank: int, steps: int = 20) -> list:
+    """Decode-budget sweep of the auxiliary flow's expert fan-out (cost side only): the MoE step
+    with topk_aux = k, timed with both flows and primary-only, and the distinct experts the
+    step's rows touched per layer (their weights are read once each)."""
+    import torch
+
+    import dual_flow_decode_dualflow_b300 as dfl
+    from tests import gpu_harness as H
+
+    dev = torch.device("cuda", local_rank)
+    out = []
+    for k in ks:
+        wk = w.replace(topk_aux=k)
+        run = H.DeviceRun(wk, dev)
+        stream = torch.cuda.Stream(device=dev)
+
+        def timed(aux_on):
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    run.step(aux_on=aux_on, stream=stream)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(steps):
+                    run.step(aux_on=aux_on, stream=stream)
+                e1.record(stream)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / steps
+
+        ms_prim = timed(0)
+        ms_dual = timed(1)
+        kmax = max(wk.topk_primary, k)
+        ids = torch.empty((wk.n_layers, 2, wk.batch, kmax), dtype=torch.int32, device=dev)
+        dfl.dualflow_expert_ids(run.ctx, ids, wk.batch, stream)
+        stream.synchronize()
+        st = dfl.dualflow_sync_status(run.ctx)
+        if st != 0:
+            raise RuntimeError(f"device status in the topk_aux sweep: {dfl.dualflow_status_string(st)}")
+        touched = [len(set(x for x in ids[l].flatten().tolist() if x >= 0)) for l in range(wk.n_layers)]
+        nb = step_bytes(wk, touched)
+        out.append({"topk_aux": k, "ms_per_step": ms_dual, "primary_only_ms": ms_prim,
+                    "dual_over_primary": ms_dual / ms_prim, "experts_touched_mean": sum(touched) / len(touched),
+                    "step_bytes": nb["total"], "hbm_gbs": nb["total"] / (ms_dual * 1e-3) / 1e9})
+        run.close()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -618,6 +664,8 @@ def main():
                     help="profiling captures only: run the workload with this many layers")
     ap.add_argument("--quick", action="store_true", help="profiling captures only: time the step, skip the rest")
     ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged"], default="dense")
+    ap.add_argument("--sweep-topk-aux", default="",
+                    help="MoE only: comma-separated auxiliary fan-outs to time as well (cost side of the decode budget)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     w = workload(args.workload)
@@ -639,6 +687,8 @@ def main():
         res = run_ours_attention(args, w, rank, world, local_rank)
     else:
         res = run_ours(args, w, rank, world, local_rank)
+        if res is not None and args.sweep_topk_aux and w.n_experts > 0:
+            res["topk_aux_sweep"] = sweep_topk_aux(w, [int(k) for k in args.sweep_topk_aux.split(",")], local_rank)
     if res is not None:
         print(json.dumps(res), flush=True)
     if world > 1:
