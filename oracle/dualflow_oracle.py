@@ -51,6 +51,11 @@ are silent, each one a choice of this implementation:
   R11 token choice after the mixture head: greedy = argmax of p_mix (ties to the lower index), or
      inverse-transform sampling with a supplied uniform u in [0, 1): the smallest i whose
      cumulative probability exceeds u (the last i with p_i > 0 when rounding leaves none).
+  R13 prefill: the primary flow alone processes a prompt's tokens in one pass, each position
+     attending every earlier cached position and itself, and writes their keys/values into the
+     cache; the auxiliary flow is turned on at the last prompt position, which the caller runs as
+     the first decode step. Computed here as one primary-only decode step per prompt position (the
+     plain definition: a causal pass computes exactly what a step at each position computes).
   R12 generation loop: each decode step appends the primary's k1/v1 at position seq_len[b] (the
      entry the step attended), seq_len[b] grows by one, and the token chosen from that step's
      mixture (R11) is the next step's input. With the auxiliary flow off the choice is made from
@@ -471,6 +476,25 @@ def generate(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequence, 
         L = L + 1
         tokens = out_tok[t].copy()
     return dict(tokens=out_tok, logits=out_logits, seq_len=L)
+
+
+def prefill(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequence, prompt: np.ndarray,
+            seq_len: np.ndarray, mirror: bool = True) -> dict:
+    """Primary-only prefill (R13) of prompt [B, n]: token t of sequence b sits at position
+    seq_len[b] + t; its key/value enter the cache there (caches written in place). Returns the
+    primary logits of every position [B, n, V] and the final seq_len."""
+    prompt = np.asarray(prompt, dtype=np.int64)
+    B, n = prompt.shape
+    L = np.array(seq_len, dtype=np.int64)
+    logits = np.zeros((B, n, hp.vocab))
+    for t in range(n):
+        r = decode_step(hp, glob, layers, caches, prompt[:, t], L, aux_on=False, mirror=mirror)
+        logits[:, t] = r["logits"][0]
+        for layer in range(len(layers)):
+            for b in range(B):
+                append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])
+        L = L + 1
+    return dict(logits=logits, seq_len=L)
 
 
 def sample_inverse_cdf(p: np.ndarray, u: float) -> int:

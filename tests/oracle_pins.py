@@ -511,6 +511,57 @@ def torch_generate(hp, glob, layers, caches, tokens, seq_len, n_steps, u=None, a
     return out
 
 
+def torch_prefill(hp, glob, layers, caches, prompt, seq_len):
+    """A causal prefill with torch calls: all of a sequence's prompt positions in one pass per layer,
+    scaled_dot_product_attention with a boolean mask (position L + i sees cached positions and
+    prompt positions up to itself); returns the logits of every position [B, n, V]."""
+    t = lambda a: torch.from_numpy(np.asarray(a, F64))  # noqa: E731
+    Hq, Hkv, D, F = hp.n_q_heads, hp.n_kv_heads, hp.head_dim, hp.ffn_hidden
+    B, n = prompt.shape
+    out = []
+    for b in range(B):
+        L = int(seq_len[b])
+        h = t(glob["E1"][prompt[b]])  # [n, d]
+        pos = torch.arange(L, L + n, dtype=torch.float64)
+        mask = torch.arange(L + n)[None, :] <= torch.arange(L, L + n)[:, None]  # [n, L + n]
+        for li, P in enumerate(layers):
+            x = TF.rms_norm(h, (hp.d_model,), weight=t(P["g_attn"]), eps=hp.rms_eps)
+            W = t(P["Wqkv"])
+            q = TF.linear(x, W[: Hq * D]).view(n, Hq, D)
+            k = TF.linear(x, W[Hq * D: (Hq + Hkv) * D]).view(n, Hkv, D)
+            v = TF.linear(x, W[(Hq + Hkv) * D:]).view(n, Hkv, D)
+            th = hp.rope_base ** (-2.0 * torch.arange(D // 2, dtype=torch.float64) / D)
+            ang = pos[:, None, None] * th  # [n, 1, D/2]
+            rot = lambda z: torch.cat([z[..., : D // 2] * torch.cos(ang) - z[..., D // 2:] * torch.sin(ang),  # noqa: E731
+                                       z[..., : D // 2] * torch.sin(ang) + z[..., D // 2:] * torch.cos(ang)], -1)
+            q, k = rot(q), rot(k)
+            Kc, Vc = caches[li].seq(b, L)
+            Kall = torch.cat([t(Kc), k.transpose(0, 1)], 1)  # [Hkv, L + n, D]
+            Vall = torch.cat([t(Vc), v.transpose(0, 1)], 1)
+            o = TF.scaled_dot_product_attention(q.transpose(0, 1)[None], Kall[None], Vall[None], attn_mask=mask,
+                                                enable_gqa=True)[0]  # [Hq, n, D]
+            h = h + TF.linear(o.transpose(0, 1).reshape(n, -1), t(P["Wo"]))
+            x = TF.rms_norm(h, (hp.d_model,), weight=t(P["g_mlp"]), eps=hp.rms_eps)
+            h = h + TF.linear(TF.silu(TF.linear(x, t(P["Wgu"][:F]))) * TF.linear(x, t(P["Wgu"][F:])), t(P["Wd"]))
+        x = TF.rms_norm(h, (hp.d_model,), weight=t(glob["g_final"]), eps=hp.rms_eps)
+        out.append(TF.linear(x, t(glob["W_lm"])).numpy())
+    return np.stack(out)
+
+
+def pin_prefill(O):
+    """Prefill (one primary-only decode step per prompt position) equals a torch causal pass over the
+    whole prompt at every position, with and without a cached prefix; decoding after it equals
+    decoding after the same tokens fed one by one."""
+    hp = tiny_hp(O)
+    glob, layers, caches, _, L = tiny_model(O, hp, n_layers=2, seed=31)
+    prompt = np.random.default_rng(32).integers(0, hp.vocab, size=(2, 4))
+    for start in (np.zeros(2, dtype=np.int64), L):
+        ref = torch_prefill(hp, glob, layers, caches, prompt, start)
+        got = O.prefill(hp, glob, layers, _writable_caches(O, caches), prompt, start, mirror=False)
+        close(got["logits"], ref, 1e-11, "prefill logits at every position")
+        assert np.array_equal(got["seq_len"], start + prompt.shape[1])
+
+
 def _writable_caches(O, caches):
     return [O.DenseCache(K=np.array(c.K, copy=True), V=np.array(c.V, copy=True)) for c in caches]
 
@@ -549,4 +600,4 @@ def pin_generate(O):
 ALL_PINS = [pin_round_bf16, pin_rmsnorm, pin_rope, pin_attention_closed_forms, pin_attention_gqa_vs_sdpa,
             pin_small_ops, pin_primary_is_standard_decoder, pin_flow_invariants, pin_coupling_special_cases, pin_query_coupling_source,
             pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mirror_tracks_exact, pin_mixture_head,
-            pin_sampling, pin_generate]
+            pin_sampling, pin_generate, pin_prefill]

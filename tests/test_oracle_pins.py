@@ -60,6 +60,8 @@ MUTANTS = {
     "generate_no_append": ('append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])',
                            "pass"),
     "generate_no_increment": ("        L = L + 1\n        tokens = out_tok[t].copy()", "        tokens = out_tok[t].copy()"),
+    "prefill_no_append": ('                append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])\n        L = L + 1\n    return dict(logits=logits',
+                          '                pass\n        L = L + 1\n    return dict(logits=logits'),
     "generate_primary_choice": ("    if logits2 is None:\n        p = softmax", "    if True:\n        p = softmax"),
 }
 
