@@ -24,7 +24,7 @@ C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dual
                "dualflow_stacked_linear", "dualflow_coupled_mlp", "dualflow_step", "dualflow_step_host",
                "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
                "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head",
-               "dualflow_generate", "dualflow_generate_host")
+               "dualflow_generate", "dualflow_generate_host", "dualflow_prefill_reserve", "dualflow_prefill")
 DF_PROF_FAMILIES = 8
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
@@ -88,6 +88,8 @@ def load_library(path: str = LIB_PATH):
         "dualflow_mixture_head": ([vp, vp, i32, vp, vp, vp, vp, vp], i32),
         "dualflow_generate": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, vp, vp, vp, vp,
                                i32, vp], i32),
+        "dualflow_prefill_reserve": ([vp, i32], i32),
+        "dualflow_prefill": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp], i32),
         "dualflow_generate_host": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, i32, vp],
                                    i32),
     }
@@ -235,6 +237,19 @@ def dualflow_generate_host(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens
     rc = load_library().dualflow_generate_host(ctx, ctypes.byref(w), ctypes.byref(kv), _ptr(tokens_host), batch,
                                                n_steps, _ptr(u_host), _ptr(tokens_out_host), aux_on, _stream(stream))
     _check("dualflow_generate_host", rc)
+
+
+def dualflow_prefill_reserve(ctx, max_rows: int) -> None:
+    """Allocates the prefill workspace for batch * prompt-token rows (cold call)."""
+    _check("dualflow_prefill_reserve", load_library().dualflow_prefill_reserve(ctx, max_rows))
+
+
+def dualflow_prefill(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens, batch: int, n_tok: int,
+                     stream=None) -> None:
+    """Primary-only prefill of tokens [batch, n_tok] at positions seq_len[b] + t (see the header)."""
+    rc = load_library().dualflow_prefill(ctx, ctypes.byref(w), ctypes.byref(kv), _ptr(tokens), batch, n_tok,
+                                         _stream(stream))
+    _check("dualflow_prefill", rc)
 
 
 def dualflow_sync_status(ctx, stream=None) -> int:

@@ -9,7 +9,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdualflow.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "attn_bf16.cu", "small_ops.cu", "attn_noalloc.cu", "moe.cu", "mixture.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "attn_bf16.cu", "small_ops.cu", "attn_noalloc.cu", "moe.cu", "mixture.cu", "attn_prefill.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]
 

@@ -640,7 +640,8 @@ int dualflow_free(dualflow_ctx* ctx) {
   }
   void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
                   ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss,
-                  ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids, ctx->gen_tokens, ctx->gen_out_dev, ctx->gen_u_dev};
+                  ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids, ctx->gen_tokens, ctx->gen_out_dev, ctx->gen_u_dev,
+                  ctx->pf_h,   ctx->pf_x,    ctx->pf_q,      ctx->pf_o,     ctx->pf_u,     ctx->pf_ss};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete ctx;
@@ -848,6 +849,151 @@ int dualflow_step_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualf
                       cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return DF_ERR_CUDA;
   return cudaStreamSynchronize(s) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows) {
+  if (!ctx || max_rows < 0) return DF_ERR_ARG;
+  const dualflow_config& c = ctx->cfg;
+  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0 || c.paged) return DF_ERR_UNSUPPORTED;
+  if (max_rows <= ctx->pf_rows) return DF_OK;
+  for (void* p : {(void*)ctx->pf_h, ctx->pf_x, ctx->pf_q, ctx->pf_o, ctx->pf_u, (void*)ctx->pf_ss})
+    if (p) cudaFree(p);
+  ctx->pf_h = nullptr;
+  ctx->pf_x = ctx->pf_q = ctx->pf_o = ctx->pf_u = nullptr;
+  ctx->pf_ss = nullptr;
+  ctx->pf_rows = 0;
+  const size_t R = (size_t)max_rows, qd = (size_t)c.n_q_heads * c.head_dim;
+  void* h = nullptr;
+  void* ss = nullptr;
+  if (dalloc(&h, R * c.d_model * 4) != DF_OK || dalloc(&ctx->pf_x, R * c.d_model * 2) != DF_OK ||
+      dalloc(&ctx->pf_q, R * qd * 2) != DF_OK || dalloc(&ctx->pf_o, R * qd * 2) != DF_OK ||
+      dalloc(&ctx->pf_u, R * c.ffn_hidden * 2) != DF_OK || dalloc(&ss, R * ctx->ss_ld * 4) != DF_OK) {
+    for (void* p : {h, ctx->pf_x, ctx->pf_q, ctx->pf_o, ctx->pf_u, ss})
+      if (p) cudaFree(p);
+    ctx->pf_x = ctx->pf_q = ctx->pf_o = ctx->pf_u = nullptr;
+    return DF_ERR_OOM;
+  }
+  ctx->pf_h = static_cast<float*>(h);
+  ctx->pf_ss = static_cast<float*>(ss);
+  ctx->pf_rows = max_rows;
+  return DF_OK;
+}
+
+int dualflow_prefill(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
+                     int32_t batch, int32_t n_tok, dualflow_stream stream) {
+  if (!ctx || !tokens) return DF_ERR_ARG;
+  const dualflow_config& c = ctx->cfg;
+  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0 || c.paged) return DF_ERR_UNSUPPORTED;
+  const int G = c.n_q_heads / c.n_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return DF_ERR_UNSUPPORTED;
+  if (batch <= 0 || batch > c.max_batch || n_tok < 0) return DF_ERR_SHAPE;
+  if (n_tok == 0) return DF_OK;
+  if ((long long)batch * n_tok > ctx->pf_rows) return DF_ERR_SHAPE;
+  DF_TRY(check_weights(ctx, w));
+  if (!kv || kv->n_layers != c.n_layers) return DF_ERR_ARG;
+  for (int l = 0; l < c.n_layers; ++l) DF_TRY(check_kv(ctx, kv, l));
+  cudaStream_t s = S(stream);
+  const int R = batch * n_tok;
+  const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
+  const int d_tiles = (c.d_model + kGemmTileN - 1) / kGemmTileN;
+  // the decode step's kernels on the prefill rows: the context's activation buffers point at the
+  // prefill workspace for the duration of the call
+  struct Swap {
+    dualflow_ctx* c;
+    float* h;
+    void *x, *q, *o, *u;
+    float* ss;
+    ~Swap() {
+      c->h = h;
+      c->x = x;
+      c->q = q;
+      c->o = o;
+      c->u = u;
+      c->ss = ss;
+    }
+  } keep{ctx, ctx->h, ctx->x, ctx->q, ctx->o, ctx->u, ctx->ss};
+  ctx->h = ctx->pf_h;
+  ctx->x = ctx->pf_x;
+  ctx->q = ctx->pf_q;
+  ctx->o = ctx->pf_o;
+  ctx->u = ctx->pf_u;
+  ctx->ss = ctx->pf_ss;
+  DF_TRY(launch_embed_prep(ctx, w->E1, w->E1, tokens, w->g_attn[0], R, 0, s));
+  int ss_parts = 1;
+  auto rows = [&](GemmArgs& g) {
+    g.m_p = R;
+    g.m_a = 0;
+    g.row_blocked = 1;
+    g.seq_rows = n_tok;
+  };
+  auto normed_input = [&](GemmArgs& g) {
+    g.ss_in = ctx->ss;
+    g.ss_parts = ss_parts;
+    g.ss_ld = ctx->ss_ld;
+    g.inv_d = 1.0f / (float)c.d_model;
+    g.eps = c.rms_eps;
+  };
+  auto norm_output = [&](GemmArgs& g, const void* g_next) {
+    g.g_next = g_next;
+    g.x_next = ctx->x;
+    g.ss_out = ctx->ss;
+    g.ss_ld = ctx->ss_ld;
+  };
+  for (int l = 0; l < c.n_layers; ++l) {
+    GemmArgs g = gemm_args(ctx);
+    g.x = ctx->x;
+    g.W = w->Wqkv[l];
+    g.n_out = qkv_n;
+    g.k = c.d_model;
+    rows(g);
+    g.epi = EPI_PREFILL_QKV;
+    g.q_out = ctx->q;
+    g.seq_len = kv->seq_len;
+    g.k_cache = kv->k[l];
+    g.v_cache = kv->v[l];
+    normed_input(g);
+    DF_TRY(launch_gemm_tc(ctx, g, s));
+    DF_TRY(launch_attention_prefill(c, ctx->q, ctx->o, kv->k[l], kv->v[l], kv->seq_len, batch, n_tok, ctx->status,
+                                    s));
+    GemmArgs o = gemm_args(ctx);
+    o.x = ctx->o;
+    o.W = w->Wo[l];
+    o.n_out = c.d_model;
+    o.k = qd;
+    rows(o);
+    o.epi = EPI_ADD_F32;
+    o.y = ctx->h;
+    o.ldy = c.d_model;
+    norm_output(o, w->g_mlp[l]);
+    DF_TRY(launch_gemm_tc(ctx, o, s));
+    ss_parts = d_tiles;
+    GemmArgs gu = gemm_args(ctx);
+    gu.x = ctx->x;
+    gu.W = w->Wgu[l];
+    gu.n_out = c.ffn_hidden;
+    gu.k = c.d_model;
+    rows(gu);
+    gu.epi = EPI_SWIGLU;
+    gu.y = ctx->u;
+    gu.ldy = c.ffn_hidden;
+    gu.vec = w->b[l];
+    normed_input(gu);
+    DF_TRY(launch_gemm_tc(ctx, gu, s));
+    GemmArgs dn = gemm_args(ctx);
+    dn.x = ctx->u;
+    dn.W = w->Wd[l];
+    dn.n_out = c.d_model;
+    dn.k = c.ffn_hidden;
+    rows(dn);
+    dn.epi = EPI_COUPLE_ADD;
+    dn.y = ctx->h;
+    dn.ldy = c.d_model;
+    dn.vec = w->c[l];
+    if (l + 1 < c.n_layers) norm_output(dn, w->g_attn[l + 1]);
+    DF_TRY(launch_gemm_tc(ctx, dn, s));
+    ss_parts = d_tiles;
+  }
+  return launch_seq_advance(const_cast<int32_t*>(kv->seq_len), batch, n_tok, s);
 }
 
 int dualflow_generate_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,

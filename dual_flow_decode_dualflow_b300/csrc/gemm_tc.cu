@@ -56,6 +56,7 @@ struct GemmParams {
   int vec_ok;    // y / u rows allow 16-byte (fp32) or 8-byte (bf16) vector access
   int stages;    // pipeline stages in use (2..kStages)
   int region;    // bytes of the data region (pipeline stages, later the partial tiles)
+  int row_blocks;  // > 1: grid y runs over blocks of 256 activation rows (splits == 1)
   int push_async;  // split-K partials pushed by 16-byte asynchronous stores into the owners' areas
   int pull;        // split-K partials staged locally and read by their owners over DSMEM
   int32_t* status;
@@ -237,9 +238,20 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
   // partials, the receive area [S][2nl][n_pad + 4] only (see RedSrc).
   float* acc_s = reinterpret_cast<float*>(smem);
 
-  const GemmArgs& a = p.a;
+  GemmArgs a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, split = blockIdx.y, grp = blockIdx.z;
+  const int tile = blockIdx.x, split = p.row_blocks > 1 ? 0 : blockIdx.y, grp = blockIdx.z;
+  const int rbase = p.row_blocks > 1 ? blockIdx.y * kGemmMaxAct : 0;  // first activation row of this CTA
+  if (p.row_blocks > 1) {
+    // this CTA's block of rows: the epilogue's row-indexed operands start at its first row
+    const size_t ye = (EPI == EPI_STORE_BF16 || EPI == EPI_SWIGLU) ? 2 : 4;
+    a.m_p = min(kGemmMaxAct, p.a.m_p - rbase);
+    a.row_base = rbase;
+    if (a.y) a.y = static_cast<uint8_t*>(a.y) + (size_t)rbase * a.ldy * ye;
+    if (a.x_next) a.x_next = static_cast<__nv_bfloat16*>(a.x_next) + (size_t)rbase * a.n_out;
+    if (a.ss_out) a.ss_out += (size_t)rbase * a.ss_ld;
+    if (a.ss_in) a.ss_in += (size_t)rbase * a.ss_ld;
+  }
   const int kb0 = (int)((long long)split * p.kb_total / p.splits);
   const int kb1 = (int)((long long)(split + 1) * p.kb_total / p.splits);
   const int nkb = kb1 - kb0;
@@ -286,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
   }
   row0 += grp * a.w_group_rows;       // this expert's weights (grouped launch)
   row1 += grp * a.w_group_rows;
-  const int xrow = grp * a.x_group_rows;
+  const int xrow = grp * a.x_group_rows + rbase;
 
   if (warp == 0 && lane == 0) {
     // TMA producer: weights are streamed once (evict-first), activations stay L2-resident.
@@ -611,6 +623,37 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
             }
           }
         }
+      } else if (EPI == EPI_PREFILL_QKV) {
+        // prompt token t of sequence b (activation row b * seq_rows + t) at position seq_len[b] + t
+        const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, grow = a.row_base + n;
+        const int b = grow / a.seq_rows, pos = a.seq_len[b] + grow % a.seq_rows;
+        if (pos < 0 || pos >= a.max_ctx) {
+          set_status(p.status, DF_ERR_DEVICE_BOUNDS);
+        } else {
+          const float2* cs = a.rope + (size_t)pos * 64 + fa;
+          float4 r_lo, r_hi;
+          if (tile < Hq) {
+            rope4(cs, lo, hi, r_lo, r_hi);
+            const size_t o1 = ((size_t)grow * Hq + tile) * kHeadDim;
+            st_bf16x4(a.q_out, o1 + fa, r_lo);
+            st_bf16x4(a.q_out, o1 + fa + 64, r_hi);
+          } else {
+            const bool is_k = tile < Hq + Hkv;
+            const int hk = is_k ? tile - Hq : tile - Hq - Hkv;
+            bool ok;
+            const size_t off = cache_slot(a, b, hk, pos, p.status, &ok);
+            if (ok) {
+              if (is_k) {
+                rope4(cs, lo, hi, r_lo, r_hi);
+              } else {
+                r_lo = lo;
+                r_hi = hi;
+              }
+              st_bf16x4(is_k ? a.k_cache : a.v_cache, off + fa, r_lo);
+              st_bf16x4(is_k ? a.k_cache : a.v_cache, off + fa + 64, r_hi);
+            }
+          }
+        }
       } else if (EPI == EPI_Q2) {
         const int Hq = a.n_q_heads, B = a.m_a, h = tile, b = n;
         const int pos = a.seq_len[b];
@@ -662,7 +705,7 @@ int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& 
   if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return DF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_tiles, p.splits, p.a.n_groups > 0 ? p.a.n_groups : 1);
+  cfg.gridDim = dim3(p.n_tiles, p.row_blocks > 1 ? p.row_blocks : p.splits, p.a.n_groups > 0 ? p.a.n_groups : 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -718,7 +761,12 @@ int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups) 
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   const int m = a.m_p + a.m_a;
   if (m <= 0) return DF_OK;
-  if (m > kGemmMaxAct || m > 2 * ctx->cfg.max_batch || a.k % kGemmTileK != 0 || a.k <= 0) return DF_ERR_SHAPE;
+  if (a.k % kGemmTileK != 0 || a.k <= 0) return DF_ERR_SHAPE;
+  if (a.row_blocked) {
+    if (a.m_a != 0 || a.n_groups > 0 || a.seq_rows <= 0) return DF_ERR_ARG;
+  } else if (m > kGemmMaxAct || m > 2 * ctx->cfg.max_batch) {
+    return DF_ERR_SHAPE;
+  }
   if ((a.epi == EPI_SWIGLU || a.epi == EPI_MOE_GATEUP) && a.n_out % 64 != 0) return DF_ERR_SHAPE;
   const int groups = a.n_groups > 0 ? a.n_groups : 1;
   if ((a.epi == EPI_MOE_GATEUP || a.epi == EPI_MOE_DOWN) && (!a.sel_pos || a.n_groups <= 0)) return DF_ERR_ARG;
@@ -726,10 +774,11 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   if (a.g_next != nullptr && (a.n_out % 64 != 0 || !a.x_next || !a.ss_out)) return DF_ERR_ARG;
   GemmParams p;
   p.a = a;
-  p.n_pad = ((m + 15) / 16) * 16;
+  p.n_pad = m >= kGemmMaxAct ? kGemmMaxAct : ((m + 15) / 16) * 16;
+  p.row_blocks = a.row_blocked ? (m + kGemmMaxAct - 1) / kGemmMaxAct : 1;
   p.kb_total = a.k / kGemmTileK;
   p.n_tiles = gemm_tiles(a.n_out, a.epi);
-  p.splits = gemm_splits(ctx, a.n_out, a.k, a.epi, groups);
+  p.splits = a.row_blocked ? 1 : gemm_splits(ctx, a.n_out, a.k, a.epi, groups);
   p.status = ctx->status;
   const uintptr_t align = (a.epi == EPI_STORE_BF16 || a.epi == EPI_SWIGLU || a.epi == EPI_MOE_GATEUP) ? 8 : 16;
   p.vec_ok = a.y != nullptr && (reinterpret_cast<uintptr_t>(a.y) % align == 0) && (a.ldy % 4 == 0) ? 1 : 0;
@@ -779,6 +828,7 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
     case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(mw, mx, mpf, p, smem, s);
     case EPI_MOE_GATEUP: return launch_epi<EPI_MOE_GATEUP>(mw, mx, mpf, p, smem, s);
     case EPI_MOE_DOWN: return launch_epi<EPI_MOE_DOWN>(mw, mx, mpf, p, smem, s);
+    case EPI_PREFILL_QKV: return launch_epi<EPI_PREFILL_QKV>(mw, mx, mpf, p, smem, s);
     default: return DF_ERR_ARG;
   }
 }

@@ -35,6 +35,7 @@ enum GemmEpi : int {
   EPI_SWIGLU = 6,     // u = silu(gate) (*) up, u2 += b (*) u1, bf16 store
   EPI_MOE_GATEUP = 7, // per expert: SWIGLU for the rows that selected it, u2 += b (*) u1 if both did
   EPI_MOE_DOWN = 8,   // per expert: fp32 store of the rows that selected it
+  EPI_PREFILL_QKV = 9, // prefill (primary only): RoPE at seq_len[b] + t, q store, K/V into the cache
 };
 
 struct GemmArgs {
@@ -83,6 +84,10 @@ struct GemmArgs {
   // next launch starts on L2-resident weights. pf_W = nullptr: none.
   const void* pf_W;
   int pf_k, pf_rows, pf_tiles, pf_splits, pf_tile_rows, pf_half, pf_depth;
+  // Prefill: more activation rows than one tile holds. The rows are cut into blocks of 256
+  // (grid y), each CTA offsets y / x_next / ss_in / ss_out by its block; row_base is the block's
+  // first row, seq_rows the prompt positions per sequence (row r = b * seq_rows + t). m_a = 0.
+  int row_blocked, seq_rows, row_base;
 };
 
 struct AttnArgs {
@@ -136,6 +141,14 @@ struct dualflow_ctx {
   void* moe_u = nullptr;           // [E][2 * max_batch][F] bf16
   float* moe_y = nullptr;          // [E][2 * max_batch][d]
   int32_t* moe_ids = nullptr;      // [n_layers][2][max_batch][kmax] experts chosen by the last step
+  // prefill workspace (dualflow_prefill_reserve): rows = prompt tokens of all sequences
+  int pf_rows = 0;
+  float* pf_h = nullptr;           // [pf_rows][d] residual
+  void* pf_x = nullptr;            // [pf_rows][d] bf16 norm operand
+  void* pf_q = nullptr;            // [pf_rows][Hq * D] bf16
+  void* pf_o = nullptr;            // [pf_rows][Hq * D] bf16
+  void* pf_u = nullptr;            // [pf_rows][F] bf16
+  float* pf_ss = nullptr;          // [pf_rows][ss_ld]
   int32_t* gen_tokens = nullptr;   // [max_batch] input tokens of the generation loop's next step
   int32_t* gen_out_dev = nullptr;  // [kGenHostMaxSteps][max_batch] dualflow_generate_host staging
   float* gen_u_dev = nullptr;      // [kGenHostMaxSteps][max_batch]
@@ -188,6 +201,10 @@ int launch_moe_combine(dualflow_ctx* ctx, float* h, int batch, int aux_on, const
                        cudaStream_t s, int pdl);
 int launch_mixture_head(const float* logits, int batch, int vocab, const float* u, float* alpha, float* p_mix,
                         int32_t* token, int32_t* token2, int aux_on, cudaStream_t s);
+int launch_attention_prefill(const dualflow_config& c, const void* q, void* o, const void* k_cache,
+                             const void* v_cache, const int32_t* seq_len, int batch, int n_tok, int32_t* status,
+                             cudaStream_t s);
+int launch_seq_advance(int32_t* seq_len, int batch, int n, cudaStream_t s);
 int launch_gen_advance(const dualflow_config& c, int32_t* seq_len, int batch, int32_t* table, int32_t* free_pages,
                        int32_t* n_free, int32_t* status, cudaStream_t s);
 int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s);

@@ -298,7 +298,19 @@ __global__ void gen_advance_kernel(int32_t* seq_len, int B, int max_ctx, int pag
   }
 }
 
+__global__ void seq_advance_kernel(int32_t* seq_len, int B, int n) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) seq_len[b] += n;
+}
+
 }  // namespace
+
+// After a prefill of n positions: every sequence's cached length grows by n (the bounds were
+// checked by the kernels that wrote the entries).
+int launch_seq_advance(int32_t* seq_len, int batch, int n, cudaStream_t s) {
+  seq_advance_kernel<<<(batch + 127) / 128, 128, 0, s>>>(seq_len, batch, n);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
 
 int launch_gen_advance(const dualflow_config& c, int32_t* seq_len, int batch, int32_t* table, int32_t* free_pages,
                        int32_t* n_free, int32_t* status, cudaStream_t s) {

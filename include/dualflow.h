@@ -231,6 +231,26 @@ DF_API int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const
                              int32_t* tokens_out, float* logits, float* logits_all, int32_t* free_pages,
                              int32_t* n_free, int32_t aux_on, dualflow_stream stream);
 
+/* Workspace for dualflow_prefill: room for max_rows = batch * prompt tokens activation rows
+ * (about (4 d + 4 Hq D + 2 F + 4 ss) bytes per row). Allocates (cold call, not for a hot loop);
+ * a smaller request than the current room does nothing. bf16 dense contiguous-cache contexts only
+ * (DF_ERR_UNSUPPORTED otherwise); DF_ERR_OOM leaves no prefill room. */
+DF_API int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows);
+
+/* Primary-only prefill ("Custos de Inferencia vs. Treinamento", gist.science technical summary: the
+ * auxiliary flow is off while a prompt is processed and on from the decode phase). tokens: device
+ * int32 [batch, n_tok] row-major, token t of sequence b at position seq_len[b] + t. In one pass per
+ * layer the primary flow's projections run on all batch * n_tok rows (tcgen05 tiles of 256 rows),
+ * the keys/values of every prompt position are written into the cache, and each position attends
+ * the cached positions 0 .. itself (causal). Then seq_len[b] += n_tok (device). No logits: the
+ * caller runs the prompt's last token as the first decode step (dualflow_step / dualflow_generate),
+ * where the auxiliary flow joins. Needs dualflow_prefill_reserve(ctx, >= batch * n_tok)
+ * (DF_ERR_SHAPE otherwise); bf16 dense contexts with contiguous caches and G = Hq / Hkv in
+ * {1, 2, 4} (DF_ERR_UNSUPPORTED otherwise). A position seq_len[b] + t >= max_ctx latches
+ * DF_ERR_DEVICE_BOUNDS. Asynchronous on `stream`, launched eagerly (no graph). */
+DF_API int dualflow_prefill(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+                            const int32_t* tokens, int32_t batch, int32_t n_tok, dualflow_stream stream);
+
 /* dualflow_generate with HOST buffers, for contiguous caches: copies tokens_host [batch] (and
  * u_host [n_steps, batch] if not NULL) to the device, runs n_steps of the decode loop (step, mixture
  * head, token choice, length advance), copies the chosen tokens back to tokens_out_host

@@ -1,0 +1,101 @@
+"""Primary-only prefill (dualflow_prefill) on the GPU against the oracle's prefill.
+
+The cache rows the prefill writes (positions seq_len[b] .. seq_len[b] + n - 1 of every layer) are
+compared with the oracle's at the bf16 bar, every other cache element must be unchanged bit for
+bit, the lengths must advance by n, and a decode step of both flows after the prefill must give
+the oracle's logits (which depend on every prefilled entry)."""
+import numpy as np
+import pytest
+import torch
+
+import dual_flow_decode_dualflow_b300 as dfl
+import oracle as O
+from dfsynth import workloads as W
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+SMALL = dict(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=1, ffn_hidden=512, vocab=1000, batch=3, ctx_len=0,
+             ctx_lo=5, ctx_hi=200, gain_sigma=0.1)
+# (workload, prompt tokens per sequence, cached lengths before the prefill or None for the workload's)
+CASES = {
+    "g4_b3_n9": (W.DENSE_24L_B32_L4096.replace(**SMALL), 9, None),
+    "g2_b2_n300_rowblocks": (W.DENSE_24L_B32_L4096.replace(**dict(SMALL, n_kv_heads=2, batch=2, ctx_lo=0, ctx_hi=600)),
+                             300, [0, 37]),
+    "g1_b2_n70": (W.DENSE_24L_B32_L4096.replace(**dict(SMALL, n_q_heads=2, n_kv_heads=2, batch=2, ctx_lo=0,
+                                                       ctx_hi=100)), 70, [3, 20]),
+}
+
+
+def _oracle_caches(w):
+    out = []
+    for l in range(w.n_layers):
+        K = H.host_f64(w, f"L{l}.K").reshape(w.cache_shape()).copy()
+        V = H.host_f64(w, f"L{l}.V").reshape(w.cache_shape()).copy()
+        out.append(O.DenseCache(K=K, V=V))
+    return out
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_prefill_parity(cuda_device, name):
+    w, n, lens = CASES[name]
+    run = H.DeviceRun(w, cuda_device)
+    try:
+        if lens is not None:
+            run.seq_len_np = np.array(lens, dtype=np.int32)
+            run.seq_len.copy_(torch.from_numpy(run.seq_len_np))
+        L = run.seq_len_np.astype(np.int64)
+        assert L.max() + n < w.max_ctx
+        prompt = np.random.default_rng(41).integers(0, w.vocab, size=(w.batch, n)).astype(np.int32)
+        before = {k: v.clone() for k, v in run.t.items() if k.endswith((".K", ".V"))}
+        dfl.dualflow_prefill_reserve(run.ctx, w.batch * n)
+        dfl.dualflow_prefill(run.ctx, run.weights, run.kv, torch.from_numpy(prompt).to(cuda_device), w.batch, n)
+        assert run.status() == 0
+        assert np.array_equal(run.seq_len.cpu().numpy(), L + n)
+
+        caches = _oracle_caches(w)
+        glob = {"E1": H.LazyRows(w, "E1"), "E2": H.LazyRows(w, "E2"), "W_lm": H.host_f64(w, "W_lm"),
+                "g_final": H.host_f64(w, "g_final")}
+        layers = H.LazyLayers(w)
+        O.prefill(H.hparams(w), glob, layers, caches, prompt, L, mirror=True)
+        for l in range(w.n_layers):
+            for kind in ("K", "V"):
+                t = run.t[f"L{l}.{kind}"]
+                ref = caches[l].K if kind == "K" else caches[l].V
+                exp = before[f"L{l}.{kind}"].clone()
+                for b in range(w.batch):
+                    got = H.to_f64(t[b, :, L[b]:L[b] + n, :])
+                    err = H.rel_err(got, ref[b][:, L[b]:L[b] + n, :])
+                    assert err <= TOL, f"layer {l} {kind} seq {b}: rel err {err:.3e}"
+                    exp[b, :, L[b]:L[b] + n, :] = t[b, :, L[b]:L[b] + n, :]
+                assert torch.equal(exp, t), f"layer {l} {kind}: cache changed outside the prompt's rows"
+
+        # the next token of every sequence as a decode step of both flows, after the prompt
+        nxt = np.random.default_rng(42).integers(0, w.vocab, size=w.batch).astype(np.int32)
+        run.tokens.copy_(torch.from_numpy(nxt))
+        run.tokens_np = nxt
+        run.step(aux_on=1)
+        assert run.status() == 0
+        ref = O.decode_step(H.hparams(w), glob, layers, caches, nxt, L + n, aux_on=True, mirror=True)
+        got = H.to_f64(run.logits)
+        for f in range(2):
+            err = H.rel_err(got[f], ref["logits"][f])
+            assert err <= TOL, f"decode after prefill, flow {f + 1}: rel err {err:.3e}"
+    finally:
+        run.close()
+
+
+def test_prefill_rejects_without_room(cuda_device):
+    w, n, _ = CASES["g4_b3_n9"]
+    run = H.DeviceRun(w, cuda_device)
+    try:
+        prompt = torch.zeros((w.batch, n), dtype=torch.int32, device=cuda_device)
+        with pytest.raises(dfl.DualFlowError):
+            dfl.dualflow_prefill(run.ctx, run.weights, run.kv, prompt, w.batch, n)  # nothing reserved
+        dfl.dualflow_prefill_reserve(run.ctx, w.batch * n - 1)
+        with pytest.raises(dfl.DualFlowError):
+            dfl.dualflow_prefill(run.ctx, run.weights, run.kv, prompt, w.batch, n)
+        assert np.array_equal(run.seq_len.cpu().numpy(), run.seq_len_np)  # nothing ran
+    finally:
+        run.close()
