@@ -50,7 +50,21 @@ def load_peaks() -> tuple[float, str]:
 def workload(name: str = "dense"):
     from dfsynth import workloads as W
     return {"dense": W.DENSE_24L_B32_L4096, "moe": W.MOE_16L_B64, "attn": W.ATTN_B8_L2048,
-            "paged": W.PAGED_RAGGED_B64}[name]
+            "paged": W.PAGED_RAGGED_B64, "prefill": W.DENSE_24L_B32_L4096}[name]
+
+
+PREFILL_TOKENS = 512  # prompt tokens per sequence of the prefill workload (from an empty cache)
+
+
+def prefill_flops(w, n_tok: int) -> float:
+    """Algorithmic FLOPs of the primary-only prefill of n_tok tokens per sequence from position 0:
+    2 per weight element per row for the four projections of every layer, and the causal attention
+    (2 x 2 x D per head per (query, attended key) pair)."""
+    qkv = (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim * w.d_model
+    layer = qkv + w.d_model * w.n_q_heads * w.head_dim + 3 * w.ffn_hidden * w.d_model
+    rows = w.batch * n_tok
+    pairs = w.batch * n_tok * (n_tok + 1) / 2
+    return w.n_layers * (2.0 * layer * rows + 4.0 * w.head_dim * w.n_q_heads * pairs)
 
 
 def step_bytes(w, experts_touched=None) -> dict:
@@ -173,6 +187,39 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class PrefillOracleSample:
+    """The CPU oracle's prefill on a bounded sample: one sequence, the first layer, the first
+    n_sample prompt tokens from an empty cache; scaled to the workload by sequences, tokens and
+    layers (the oracle's prefill runs one decode step per position, logits included)."""
+
+    def __init__(self, w, n_sample: int, n_tok: int):
+        import oracle as O
+        from tests import gpu_harness as H
+        self.O, self.w, self.n_sample, self.n_tok = O, w, n_sample, n_tok
+        ws = w.replace(n_layers=1, batch=1)
+        self.layers = [H.LazyLayers(ws)[0]]
+        self.glob = {"E1": H.LazyRows(ws, "E1"), "E2": H.LazyRows(ws, "E2"), "W_lm": H.host_f64(ws, "W_lm"),
+                     "g_final": H.host_f64(ws, "g_final")}
+        self.hp = H.hparams(ws)
+        self.prompt = np.random.default_rng(51).integers(0, w.vocab, size=(1, n_sample))
+
+    def time(self) -> float:
+        caches = [self.O.DenseCache(K=np.zeros((1, self.w.n_kv_heads, self.n_sample, self.w.head_dim)),
+                                    V=np.zeros((1, self.w.n_kv_heads, self.n_sample, self.w.head_dim)))]
+        t0 = time.perf_counter()
+        self.O.prefill(self.hp, self.glob, self.layers, caches, self.prompt, np.zeros(1, dtype=np.int64))
+        return time.perf_counter() - t0
+
+    def full(self, seconds: float) -> float:
+        # per position: one layer + the LM head of the oracle's step; scale to all layers + head
+        return seconds * self.w.batch * (self.n_tok / self.n_sample) * (self.w.n_layers + 1) / 2
+
+    def describe(self) -> str:
+        return (f"oracle (numpy fp64) prefill of {self.n_sample} prompt tokens of 1 of {self.w.batch} sequences x 1 of "
+                f"{self.w.n_layers} layers (+ the LM head its per-position steps compute), scaled to {self.n_tok} "
+                f"tokens x {self.w.batch} sequences x (layers + 1)")
+
+
 class OracleSample:
     """The CPU oracle on a bounded sample of the workload: the first `n_layers` layers and the
     sequences in `rows`, inputs drawn and widened beforehand. time_step() times one oracle decode
@@ -258,6 +305,23 @@ def run_reference(args, w) -> dict:
     rotating through the batch, over the first layer and the LM head; for an attention-only
     workload, one sequence's attention call)."""
     per = []
+    if args.workload == "prefill":
+        samp = PrefillOracleSample(w, 8, PREFILL_TOKENS)
+        for i in range(args.warmup + args.steps):
+            t = samp.time()
+            if i >= args.warmup:
+                per.append(samp.full(t))
+        s = statistics.median(per)
+        value = w.batch * PREFILL_TOKENS / s
+        unit = "prefill tokens/s"
+        return {"impl": "reference", "metric": "primary-only prefill tokens/s at 1 B300", "value": value, "unit": unit,
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": f"prefill_{w.name}", "batch": w.batch, "prompt_tokens": PREFILL_TOKENS,
+                           "layers": w.n_layers},
+                "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle",
+                                 "sample": samp.describe()},
+                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     if w.kind == "attention":
         lens = w.seq_lens()
         order = [int(b) for b in np.argsort(lens)[: max(1, min(8, w.batch))]]  # the shortest: bounded time
@@ -404,6 +468,103 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
                 "api": "dualflow_decode_attention with q1, h2 copied from pinned host memory and o copied back, "
                        "stream sync per step"},
         "gpu_launches": 2 * steps, "launches_per_step": 2,
+        "clocks": sampler.summary(),
+    }
+
+
+def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | None:
+    """Primary-only prefill of PREFILL_TOKENS tokens per sequence from an empty cache, on the dense
+    model (the positions are rewritten by every repetition)."""
+    import torch
+
+    import dual_flow_decode_dualflow_b300 as dfl
+    from tests import gpu_harness as H
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = torch.distributed if world > 1 else None
+    run = H.DeviceRun(w, dev)
+    stream = torch.cuda.Stream(device=dev)
+    n_tok = PREFILL_TOKENS
+    prompt_np = np.random.default_rng(52).integers(0, w.vocab, size=(w.batch, n_tok)).astype(np.int32)
+    prompt = torch.from_numpy(prompt_np).to(dev)
+    dfl.dualflow_prefill_reserve(run.ctx, w.batch * n_tok)
+    steps = max(min(args.steps, 10), 3)
+
+    def once(tokens):
+        with torch.cuda.stream(stream):
+            run.seq_len.zero_()
+            dfl.dualflow_prefill(run.ctx, run.weights, run.kv, tokens, w.batch, n_tok, stream)
+
+    for _ in range(args.warmup):
+        once(prompt)
+    stream.synchronize()
+    if dist:
+        dist.barrier()
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler:
+        sampler.mark(True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(steps):
+                once(prompt)
+            e1.record(stream)
+        e1.synchronize()
+        sampler.mark(False)
+    ms = e0.elapsed_time(e1) / steps
+    st = dfl.dualflow_sync_status(run.ctx)
+    if st != 0:
+        raise RuntimeError(f"device status after the prefill: {dfl.dualflow_status_string(st)}")
+    # end to end: the prompt copied from pinned host memory, the prefill, a synchronisation
+    prompt_h = torch.from_numpy(prompt_np).pin_memory()
+    prompt_d = torch.empty_like(prompt)
+    e2e = []
+    for i in range(3 + steps):
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            prompt_d.copy_(prompt_h, non_blocking=True)
+        once(prompt_d)
+        stream.synchronize()
+        if i >= 3:
+            e2e.append(time.perf_counter() - t0)
+    e2e_s = statistics.median(e2e)
+    if dist:
+        t = torch.tensor([ms, e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_s = float(t[0].item()), float(t[1].item())
+    run.close()
+    if rank != 0:
+        return None
+    flops = prefill_flops(w, n_tok)
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops_sustained"]), "measured sustained bf16 (cuBLAS 8192^3 loop)"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1400.0, "fallback sustained bf16"
+    tflops = flops / (ms * 1e-3) / 1e12
+    samp = PrefillOracleSample(w, 8, n_tok)
+    cpu_s = samp.full(samp.time())
+    tokens = world * w.batch * n_tok
+    return {
+        "metric": "primary-only prefill tokens/s at 1 B300", "value": tokens / (ms * 1e-3), "unit": "prefill tokens/s",
+        "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
+        "data": "synthetic: seeded counter-hash generator, random-init weights of the workload's shapes",
+        "config": {"workload": f"prefill_{w.name}", "layers": w.n_layers, "d_model": w.d_model,
+                   "batch_per_gpu": w.batch, "prompt_tokens": n_tok, "rows": w.batch * n_tok,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "compute-bound; weights re-read per 256-row block, no flush"},
+        "roofline": {"kernel": "whole prefill pass (24 x {QKV, causal attention, O, gate/up, down})",
+                     "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "peak_kind": kind, "flops_per_step": flops, "traffic": None},
+        "cpu_baseline": {"value": w.batch * n_tok / cpu_s, "unit": "prefill tokens/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": samp.describe()},
+        "e2e": {"value": tokens / e2e_s, "unit": "prefill tokens/s", "h2d_bytes_per_step": int(prompt_np.nbytes),
+                "d2h_bytes_per_step": 0,
+                "api": "dualflow_prefill with the prompt copied from pinned host memory, stream sync per call"},
+        "gpu_launches": steps * (1 + 5 * w.n_layers + 1), "launches_per_step": 1 + 5 * w.n_layers + 1,
         "clocks": sampler.summary(),
     }
 
@@ -663,7 +824,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: run the workload with this many layers")
     ap.add_argument("--quick", action="store_true", help="profiling captures only: time the step, skip the rest")
-    ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged"], default="dense")
+    ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged", "prefill"], default="dense")
     ap.add_argument("--sweep-topk-aux", default="",
                     help="MoE only: comma-separated auxiliary fan-outs to time as well (cost side of the decode budget)")
     args = ap.parse_args()
@@ -683,7 +844,9 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    if w.kind == "attention":
+    if args.workload == "prefill":
+        res = run_ours_prefill(args, w, rank, world, local_rank)
+    elif w.kind == "attention":
         res = run_ours_attention(args, w, rank, world, local_rank)
     else:
         res = run_ours(args, w, rank, world, local_rank)
