@@ -43,6 +43,7 @@ namespace {
 constexpr int kStages = 4;                 // most pipeline stages (barrier arrays are sized for it)
 constexpr int kStageBudget = 96 * 1024;    // stage bytes that still let two CTAs share an SM
 constexpr int kStageBudget3 = 68 * 1024;   // ... three CTAs
+constexpr int kStageBudgetRows = 192 * 1024;  // ... one CTA (row-blocked launches)
 constexpr int kThreads = 128;
 constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per stage
 constexpr int kSplitMaxRows = 208;                    // padded activation rows a split CTA can hold
@@ -807,7 +808,9 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   while ((int)tcols < p.n_pad) tcols <<= 1;
   const bool three = ctas > 2 * ctx->num_sms && ctas <= 3 * ctx->num_sms && 3 * tcols <= 512 &&
                      2 * (kABytes + p.n_pad * 128) <= kStageBudget3 && 512 * p.n_pad <= kStageBudget3;
-  p.stages = (three ? kStageBudget3 : kStageBudget) / (kABytes + p.n_pad * 128);
+  // row-blocked (prefill) launches hold a 128 KB accumulator tile: one CTA per SM, so the pipeline
+  // takes the room that leaves (the same bytes later hold the tile)
+  p.stages = (a.row_blocked ? kStageBudgetRows : three ? kStageBudget3 : kStageBudget) / (kABytes + p.n_pad * 128);
   p.stages = p.stages > kStages ? kStages : (p.stages < 2 ? 2 : p.stages);
   const int pipe = p.stages * (kABytes + p.n_pad * 128);
   // split-K partials: staged in the CTA's own pipeline bytes and pulled by their owners when the
