@@ -50,7 +50,7 @@ def load_peaks() -> tuple[float, str]:
 def workload(name: str = "dense"):
     from dfsynth import workloads as W
     return {"dense": W.DENSE_24L_B32_L4096, "moe": W.MOE_16L_B64, "attn": W.ATTN_B8_L2048,
-            "paged": W.PAGED_RAGGED_B64, "prefill": W.DENSE_24L_B32_L4096}[name]
+            "paged": W.PAGED_RAGGED_B64, "prefill": W.DENSE_24L_B32_L4096, "dense_paged": W.DENSE_PAGED_RAGGED_B32}[name]
 
 
 PREFILL_TOKENS = 512  # prompt tokens per sequence of the prefill workload (from an empty cache)
@@ -233,6 +233,9 @@ class OracleSample:
         self.layers = [H.LazyLayers(ws)[l] for l in range(n_layers)]
         self.caches = []
         for l in range(n_layers):
+            if ws.paged:  # the pages of the sampled sequences, drawn on first use
+                self.caches.append(H.oracle_cache(ws, l))
+                continue
             kc, vc = H.LazySeqCache(ws, f"L{l}.K"), H.LazySeqCache(ws, f"L{l}.V")
             self.caches.append(O.DenseCache({b: kc[b] for b in self.rows}, {b: vc[b] for b in self.rows}))
         self.glob = {"E1": H.LazyRows(ws, "E1"), "E2": H.LazyRows(ws, "E2"), "W_lm": H.host_f64(ws, "W_lm"),
@@ -655,8 +658,12 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     tok = torch.from_numpy(run.tokens_np.copy()).pin_memory()
     tok_out = torch.empty((1, w.batch), dtype=torch.int32).pin_memory()
     seq_keep = run.seq_len.clone()
+    out = torch.empty((2, w.batch, w.vocab), dtype=torch.float32).pin_memory()
 
     def e2e_call():
+        if w.paged:  # the workload's pages end at slot L_b: no room to advance, logits out instead
+            dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
+            return
         with torch.cuda.stream(stream):
             run.seq_len.copy_(seq_keep)
         dfl.dualflow_generate_host(run.ctx, run.weights, run.kv, tok, w.batch, 1, tok_out, stream=stream)
@@ -671,7 +678,6 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         e2e_call()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     # the same with the full logits [2, B, V] copied back every step instead of the tokens
-    out = torch.empty((2, w.batch, w.vocab), dtype=torch.float32).pin_memory()
     for _ in range(3):
         dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
     t0 = time.perf_counter()
@@ -688,7 +694,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     # workload's
     gen_n, gen_reps = 16, 3
     gen = None
-    if w.max_ctx - 1 - int(run.seq_len_np.max()) >= gen_n:
+    if not w.paged and w.max_ctx - 1 - int(run.seq_len_np.max()) >= gen_n:
         seq0 = run.seq_len.clone()
         tok_out = torch.empty((gen_n, w.batch), dtype=torch.int32, device=dev)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -741,15 +747,18 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         "roofline": {"kernel": "attn_bf16_kernel (shared-KV decode attention)", "bound": "hbm",
                      "achieved": att_gbs, "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "bytes_per_launch": nb["attention_per_launch"],
-                     "avg_launch_ms": att_ms, "traffic": attention_traffic()},
+                     "avg_launch_ms": att_ms,
+                     # the committed ncu capture is of the dense workload's attention launch
+                     "traffic": attention_traffic() if w.name == workload("dense").name else None},
         "kernel_ms_per_step": {n: fam_ms[i] / nprof for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
         "kernel_share": {n: fam_ms[i] / nprof / prof_total for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
         "cpu_baseline": {"value": w.batch / cpu_s, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": cpu_desc},
         "e2e": {"value": world * w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(tok.numel() * 4),
-                "d2h_bytes_per_step": int(tok_out.numel() * 4),
-                "api": "dualflow_generate_host, one step per call (pinned host tokens in, the step's chosen "
-                       "tokens out, stream sync per step)"},
+                "d2h_bytes_per_step": int((out if w.paged else tok_out).numel() * 4),
+                "api": ("dualflow_step_host (pinned host tokens in, host logits out, sync per step)" if w.paged else
+                        "dualflow_generate_host, one step per call (pinned host tokens in, the step's chosen "
+                        "tokens out, stream sync per step)")},
         "e2e_logits": {"value": world * w.batch / e2e_logits_s, "unit": "tokens/s",
                        "h2d_bytes_per_step": int(tok.numel() * 4), "d2h_bytes_per_step": int(out.numel() * 4),
                        "api": "dualflow_step_host (pinned host tokens in, host logits [2, B, V] out, sync per step)"},
@@ -824,7 +833,7 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: run the workload with this many layers")
     ap.add_argument("--quick", action="store_true", help="profiling captures only: time the step, skip the rest")
-    ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged", "prefill"], default="dense")
+    ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged", "prefill", "dense_paged"], default="dense")
     ap.add_argument("--sweep-topk-aux", default="",
                     help="MoE only: comma-separated auxiliary fan-outs to time as well (cost side of the decode budget)")
     args = ap.parse_args()

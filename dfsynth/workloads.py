@@ -201,10 +201,16 @@ PAGED_RAGGED_B64 = Workload(
     d_model=4096, n_q_heads=32, n_kv_heads=8, head_dim=128, ffn_hidden=0, vocab=0, batch=64, ctx_len=0,
     ctx_lo=1024, ctx_hi=32768, paged=True, page_size=16, w_sigma=0.02, kv_sigma=1.0, coup_sigma=0.1)
 
+# config 3's model on config 4's cache layout: pages of 16, shuffled, ragged lengths
+DENSE_PAGED_RAGGED_B32 = DENSE_24L_B32_L4096.replace(
+    name="dense_24l_d2048_b32_paged_l1k-32k_bf16", seed=1006, ctx_len=0, ctx_lo=1024, ctx_hi=32768, paged=True,
+    page_size=16)
+
 MOE_16L_B64 = Workload(
     name="moe_16l_e16_top2_top4_b64_l4096_bf16", kind="step", dtype="bf16", seed=1005, n_layers=16,
     d_model=2048, n_q_heads=16, n_kv_heads=4, head_dim=128, ffn_hidden=1408, vocab=32000, batch=64,
     ctx_len=4096, n_experts=16, topk_primary=2, topk_aux=4, w_sigma=0.02, emb_sigma=0.02, kv_sigma=1.0,
     coup_sigma=0.1)
 
-WORKLOADS = {w.name: w for w in (TINY_F32, ATTN_B8_L2048, DENSE_24L_B32_L4096, PAGED_RAGGED_B64, MOE_16L_B64)}
+WORKLOADS = {w.name: w for w in (TINY_F32, ATTN_B8_L2048, DENSE_24L_B32_L4096, PAGED_RAGGED_B64, MOE_16L_B64,
+                                  DENSE_PAGED_RAGGED_B32)}

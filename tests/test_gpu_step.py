@@ -157,3 +157,39 @@ def test_step_full_dense_24l_sampled(cuda_device):
         _check_cache(run, w, rows, 2e-2, ref, None)
     finally:
         run.close()
+
+
+def test_step_parity_paged_ragged(cuda_device):
+    """The full step on a paged cache (pages of 16, shuffled physical pages) with ragged lengths: the
+    oracle's logits, the appended entry in the page that holds slot L_b, every other element of the
+    pages unchanged, and the primary flow bit-identical without the auxiliary flow."""
+    w = W.DENSE_24L_B32_L4096.replace(**dict(SMALL, batch=5, paged=True, page_size=16))
+    run = H.DeviceRun(w, cuda_device)
+    try:
+        before = {k: v.clone() for k, v in run.t.items() if k.endswith((".K", ".V"))}
+        rows = list(range(w.batch))
+        run.step(aux_on=1)
+        assert run.status() == 0
+        ref = H.oracle_step(w, rows=rows)
+        got = H.to_f64(run.logits)
+        for f in range(2):
+            err = H.rel_err(got[f], ref["logits"][f])
+            assert err <= 2e-2, f"flow {f + 1} logits: rel err {err:.3e}"
+        lens, table = run.seq_len_np, run.table_np
+        for l in range(w.n_layers):
+            for kind, key in (("K", "k_new"), ("V", "v_new")):
+                t = run.t[f"L{l}.{kind}"]
+                exp = before[f"L{l}.{kind}"].clone()
+                for i, b in enumerate(rows):
+                    pid, slot = int(table[b, lens[b] // 16]), int(lens[b] % 16)
+                    assert H.rel_err(H.to_f64(t[pid, :, slot, :]), ref[key][l, i]) <= 2e-2
+                    exp[pid, :, slot, :] = t[pid, :, slot, :]
+                assert torch.equal(exp, t), f"layer {l} {kind}: pages changed outside slot L_b"
+        dual = run.logits.clone()
+        for k in before:
+            run.t[k].copy_(before[k])
+        run.step(aux_on=0)
+        assert run.status() == 0
+        assert torch.equal(run.logits[0], dual[0])
+    finally:
+        run.close()
