@@ -162,24 +162,22 @@ __device__ __forceinline__ void reduce_pair(const RedSrc& r, int lo0, int n, int
   }
   if (r.remote) {
     const uint32_t off = (uint32_t)((n * 2 * r.nl + 4 * qd) * 4), offh = off + (uint32_t)(r.nl * 4);
-    // four ranks' partials in flight at a time, summed in rank order
+    // every rank's partials in flight at once (one round trip), then summed in rank order
+    float4 pl[8], ph[8];
 #pragma unroll
-    for (int k0 = 0; k0 < 8; k0 += 4) {
-      if (k0 >= r.S) break;
-      float4 pl[4], ph[4];
+    for (int k = 0; k < 8; ++k)
+      if (k < r.S) {
+        pl[k] = ld_dsmem_f4(r.rb[k] + off);
+        ph[k] = ld_dsmem_f4(r.rb[k] + offh);
+      }
+    lo = pl[0];
+    hi = ph[0];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (k0 + k < r.S) {
-          pl[k] = ld_dsmem_f4(r.rb[k0 + k] + off);
-          ph[k] = ld_dsmem_f4(r.rb[k0 + k] + offh);
-        }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (k0 + k < r.S) {
-          lo = (k0 + k == 0) ? pl[k] : f4_add(lo, pl[k]);
-          hi = (k0 + k == 0) ? ph[k] : f4_add(hi, ph[k]);
-        }
-    }
+    for (int k = 1; k < 8; ++k)
+      if (k < r.S) {
+        lo = f4_add(lo, pl[k]);
+        hi = f4_add(hi, ph[k]);
+      }
     return;
   }
   const int fs = r.n_pad + 4;                   // feature row stride
