@@ -44,6 +44,7 @@ constexpr int kStages = 4;                 // most pipeline stages (barrier arra
 constexpr int kStageBudget = 96 * 1024;    // stage bytes that still let two CTAs share an SM
 constexpr int kStageBudget3 = 68 * 1024;   // ... three CTAs
 constexpr int kStageBudgetRows = 192 * 1024;  // ... one CTA (row-blocked launches)
+constexpr int kRowGroup = 8;               // row blocks per L2-resident group (row-blocked launches)
 constexpr int kThreads = 128;
 constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per stage
 constexpr int kSplitMaxRows = 208;                    // padded activation rows a split CTA can hold
@@ -239,8 +240,17 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
 
   GemmArgs a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = blockIdx.x, split = p.row_blocks > 1 ? 0 : blockIdx.y, grp = blockIdx.z;
-  const int rbase = p.row_blocks > 1 ? blockIdx.y * kGemmMaxAct : 0;  // first activation row of this CTA
+  // row-blocked launches: CTAs in launch order sweep groups of kRowGroup row blocks, every tile of a
+  // group before the next group, so the weight tiles and row blocks in flight stay L2-resident
+  int tile = blockIdx.x, rblk = 0;
+  if (p.row_blocks > 1) {
+    const int lin = blockIdx.x + gridDim.x * blockIdx.y, per = kRowGroup * gridDim.x;
+    const int g0 = (lin / per) * kRowGroup, in_g = min(kRowGroup, p.row_blocks - g0), w_ = lin % per;
+    rblk = g0 + w_ % in_g;
+    tile = w_ / in_g;
+  }
+  const int split = p.row_blocks > 1 ? 0 : blockIdx.y, grp = blockIdx.z;
+  const int rbase = rblk * kGemmMaxAct;  // first activation row of this CTA
   if (p.row_blocks > 1) {
     // this CTA's block of rows: the epilogue's row-indexed operands start at its first row
     const size_t ye = (EPI == EPI_STORE_BF16 || EPI == EPI_SWIGLU) ? 2 : 4;
