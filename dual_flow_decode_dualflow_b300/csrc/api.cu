@@ -597,6 +597,9 @@ int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
     return fail(DF_ERR_OOM);
   if (dalloc(&ctx->attn_cnt, (size_t)pairs * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
   cudaMemset(ctx->attn_cnt, 0, (size_t)pairs * sizeof(int32_t));
+  ctx->gemm_part_floats = df::gemm_part_floats(ctx);
+  if (ctx->gemm_part_floats > 0 && dalloc(&ctx->gemm_part, ctx->gemm_part_floats * sizeof(float)) != DF_OK)
+    return fail(DF_ERR_OOM);
   const size_t xw = std::max({c.d_model, c.ffn_hidden, qd});
   const size_t raw_n = std::max({qkv_n, 2 * c.ffn_hidden, c.d_model, c.vocab, qd});
   if (dalloc(&ctx->h, (size_t)MB * c.d_model * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
@@ -641,7 +644,7 @@ int dualflow_free(dualflow_ctx* ctx) {
   void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
                   ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss,
                   ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids, ctx->gen_tokens, ctx->gen_out_dev, ctx->gen_u_dev,
-                  ctx->pf_h,   ctx->pf_x,    ctx->pf_q,      ctx->pf_o,     ctx->pf_u,     ctx->pf_ss};
+                  ctx->pf_h,   ctx->pf_x,    ctx->pf_q,      ctx->pf_o,     ctx->pf_u,     ctx->pf_ss, ctx->gemm_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   delete ctx;

@@ -13,12 +13,11 @@
 //
 // When the output has too few tiles to fill the GPU the reduction dimension is split across the S
 // CTAs of a thread-block cluster (S <= 8). Every CTA owns a 1/S slice of the tile's features --
-// feature i and its RoPE / gate-up partner i + 64 travel together, four at a time. Each CTA stages
-// its partial tile from TMEM in its own shared memory and, after a cluster barrier, the owner of a
-// slice reads the S partials of it over distributed shared memory (16-byte loads, four ranks in
-// flight); when staging would not fit in the pipeline's bytes, the partials are instead pushed
-// straight from registers into the owners' shared memory by 16-byte asynchronous remote stores.
-// The owner sums the S partials in rank order (deterministic, and independent of which flows are
+// feature i and its RoPE / gate-up partner i + 64 travel together, four at a time. Each CTA writes
+// its fp32 partial tile from TMEM to a small exchange area that stays in L2, already cut into the S
+// owners' slices; after a cluster barrier (release / acquire, which orders those global stores
+// for the cluster) the owner of a slice reads its S partials back from L2 with every rank's load
+// in flight at once, sums them in rank order (deterministic, and independent of which flows are
 // present) and runs the epilogue on its slice:
 //   EPI_QKV      q1 = Wq.x1, q2 = Wq.x2 + a (*) q1 (before RoPE), RoPE(q1, q2, k1) at position
 //                seq_len[b], q stored bf16, primary k1/v1 appended to the cache at slot seq_len[b]
@@ -47,7 +46,7 @@ constexpr int kStageBudgetRows = 192 * 1024;  // ... one CTA (row-blocked launch
 constexpr int kRowGroup = 8;               // row blocks per L2-resident group (row-blocked launches)
 constexpr int kThreads = 128;
 constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per stage
-constexpr int kSplitMaxRows = 208;                    // padded activation rows a split CTA can hold
+constexpr int kSplitMaxRows = 208;                    // most padded activation rows of a split launch
 
 struct GemmParams {
   GemmArgs a;
@@ -59,8 +58,7 @@ struct GemmParams {
   int stages;    // pipeline stages in use (2..kStages)
   int region;    // bytes of the data region (pipeline stages, later the partial tiles)
   int row_blocks;  // > 1: grid y runs over blocks of 256 activation rows (splits == 1)
-  int push_async;  // split-K partials pushed by 16-byte asynchronous stores into the owners' areas
-  int pull;        // split-K partials staged locally and read by their owners over DSMEM
+  float* part;     // S > 1: the split-K exchange area, [CTA of the launch][S slices][n_pad][2 nl]
   int32_t* status;
 };
 
@@ -138,19 +136,15 @@ __device__ __forceinline__ size_t cache_slot(const GemmArgs& a, int b, int hk, i
 }
 
 // Where a CTA finds the fp32 partial tiles of its output slice. S == 1: its own accumulator tile
-// acc[n][128]. S > 1, local feature fl of the slice (fl < nl: feature lo0 + fl; fl >= nl: its
-// partner lo0 + 64 + fl - nl): pulled, rank r's staged slice [n][2nl] row-major in rank r's shared
-// memory (rb[r]); pushed, this CTA's receive area recv[r][fl][n_pad + 4], feature-major.
+// acc[n][128] in shared memory. S > 1: rank k's partial of the slice at g + k * gstride in the
+// exchange area, [n][2nl] with local feature fl < nl the tile feature lo0 + fl and fl >= nl its
+// partner lo0 + 64 + fl - nl.
 struct RedSrc {
   const float* base;
-  int S, n_pad, nl;
-  int remote;       // row-major slices read from the cluster's CTAs at rb[k] (shared::cluster addresses)
-  uint32_t rb[8];
+  const float* g;
+  int gstride;
+  int S, nl;
 };
-
-__device__ __forceinline__ float4 col4(const float* e, int stride) {
-  return make_float4(e[0], e[stride], e[2 * stride], e[3 * stride]);
-}
 
 // Reduced accumulators of activation row n at the slice's quad qd: low features (lo) and their
 // partners 64 apart (hi), summed over the S partials in rank order.
@@ -161,15 +155,14 @@ __device__ __forceinline__ void reduce_pair(const RedSrc& r, int lo0, int n, int
     hi = *reinterpret_cast<const float4*>(e + 64);
     return;
   }
-  if (r.remote) {
-    const uint32_t off = (uint32_t)((n * 2 * r.nl + 4 * qd) * 4), offh = off + (uint32_t)(r.nl * 4);
-    // every rank's partials in flight at once (one round trip), then summed in rank order
+  {
+    const float* e = r.g + n * 2 * r.nl + 4 * qd;
     float4 pl[8], ph[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k)
       if (k < r.S) {
-        pl[k] = ld_dsmem_f4(r.rb[k] + off);
-        ph[k] = ld_dsmem_f4(r.rb[k] + offh);
+        pl[k] = __ldcg(reinterpret_cast<const float4*>(e + k * r.gstride));
+        ph[k] = __ldcg(reinterpret_cast<const float4*>(e + k * r.gstride + r.nl));
       }
     lo = pl[0];
     hi = ph[0];
@@ -180,15 +173,6 @@ __device__ __forceinline__ void reduce_pair(const RedSrc& r, int lo0, int n, int
         hi = f4_add(hi, ph[k]);
       }
     return;
-  }
-  const int fs = r.n_pad + 4;                   // feature row stride
-  const int rs = 2 * r.nl * fs;                 // one rank's slice
-  const float* e = r.base + (4 * qd) * fs + n;
-  lo = col4(e, fs);
-  hi = col4(e + r.nl * fs, fs);
-  for (int k = 1; k < r.S; ++k) {
-    lo = f4_add(lo, col4(e + k * rs, fs));
-    hi = f4_add(hi, col4(e + k * rs + r.nl * fs, fs));
   }
 }
 
@@ -215,8 +199,12 @@ __device__ __forceinline__ void store4(const GemmArgs& a, int vec_ok, int n, int
   }
 }
 
+// Grouped (expert) launches may run three CTAs per SM (see the stage budgets), the others two.
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (see the stage budgets)
+constexpr int min_ctas_per_sm() { return (EPI == EPI_MOE_GATEUP || EPI == EPI_MOE_DOWN) ? 3 : 2; }
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_pf, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -228,14 +216,10 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.region);
   uint64_t* empty = full + kStages;
   uint64_t* done = empty + kStages;
-  uint64_t* recv_bar = done + 1;                             // S > 1: the cluster's partials arrived
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(recv_bar + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   float* rstd_s = reinterpret_cast<float*>(tmem_slot + 4);  // [256] 1 / rms of each activation row
   int* sel_s = reinterpret_cast<int*>(rstd_s + kGemmMaxAct);  // [256] grouped: row selected this expert
-  // After the main loop the pipeline bytes hold, for S == 1, the accumulator tile acc[n][128];
-  // for S > 1 and staged partials, the partial split into S slices [S][n_pad * 2nl + 8] (the pad
-  // spreads the slices over the banks) followed by the receive area [S][n_pad][2nl]; for pushed
-  // partials, the receive area [S][2nl][n_pad + 4] only (see RedSrc).
+  // S == 1: after the main loop the pipeline bytes hold the accumulator tile acc[n][128]
   float* acc_s = reinterpret_cast<float*>(smem);
 
   GemmArgs a = p.a;
@@ -269,10 +253,11 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
   while ((int)ncols < p.n_pad) ncols <<= 1;
   const int S = p.splits;
   const int nl = 64 / S, lo0 = split * nl, nq = nl / 4, nfs = 2 * nl;
-  const int fstride = p.n_pad + 4;                 // pushed: floats per feature row
-  const int slice_floats = nfs * fstride;          // pushed: one rank's slice partial
-  const int stage_stride = p.n_pad * nfs + 8;      // pulled: staged slices, bank-spread
-  float* recv_s = acc_s;                           // pushed: the receive area
+  // S > 1: the tile's S partials sit side by side in the exchange area, each cut into S slices
+  // [n_pad][2nl] (slice r is read by rank r)
+  const size_t cta_floats = (size_t)kGemmTileN * p.n_pad;
+  const size_t tile_cta0 = ((size_t)grp * p.n_tiles + tile) * S;  // the tile's rank-0 CTA
+  const size_t slice_off = (size_t)split * p.n_pad * nfs;         // this CTA's slice in a partial
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -280,10 +265,7 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
       mbar_init(&empty[s], 1);
     }
     mbar_init(done, 1);
-    mbar_init(recv_bar, 1);
     fence_mbar_init();
-    // the S slices of this CTA's output arrive by bulk copy from the cluster's CTAs
-    if (S > 1 && p.push_async) mbar_arrive_expect_tx(recv_bar, (uint32_t)(S * nfs * p.n_pad * 4));
     tma_prefetch_map(&map_w);
     tma_prefetch_map(&map_x);
   }
@@ -395,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
   }
   __syncwarp();
 
-  // ---- accumulator: TMEM -> registers -> shared memory ----
+  // ---- accumulator: TMEM -> registers -> shared memory (S == 1) or the exchange area ----
   const bool acc_ok = mbar_wait(done, 0);
   tc_fence_after();
   if (!acc_ok) set_status(p.status, DF_ERR_TIMEOUT);
@@ -403,19 +385,8 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
   const int hf = tf & 63, dst_rank = hf / nl;  // split-K: the rank that owns feature tf
   const int fl = (tf >> 6) * nl + hf % nl;     // and its index there
-  float* dst = acc_s + tf;                      // S == 1: acc[n][128]
-  int dstride = kGemmTileN;
-  uint32_t adst = 0, abar = 0;
-  if (S > 1 && p.push_async) {
-    // the owners' receive areas are their pipeline bytes: written once every CTA has drained its own
-    cluster_arrive();
-    cluster_wait();
-    adst = mapa_shared(smem_u32(recv_s + split * slice_floats + fl * fstride), (uint32_t)dst_rank);
-    abar = mapa_shared(smem_u32(recv_bar), (uint32_t)dst_rank);
-  } else if (S > 1) {
-    dst = acc_s + dst_rank * stage_stride + fl;  // pulled: the staged slice of rank dst_rank, row-major
-    dstride = nfs;
-  }
+  float* dst = acc_s + tf;  // S == 1: acc[n][128]
+  float* gdst = S > 1 ? p.part + (tile_cta0 + split) * cta_floats + (size_t)dst_rank * p.n_pad * nfs + fl : nullptr;
   // four 16-column TMEM loads in flight per wait
   for (int c0 = 0; c0 < p.n_pad; c0 += 64) {
     uint32_t v[4][16];
@@ -424,43 +395,34 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
     for (int q = 0; q < 4; ++q)
       if (q < nblk) tmem_ld16_nowait(lane_base + (uint32_t)(c0 + 16 * q), v[q]);
     tmem_ld_wait();
-    if (S > 1 && p.push_async) {
-      // feature tf's column, straight into the owner's receive area (16-byte asynchronous stores)
+    if (S > 1) {
+      // feature tf's column into its owner's slice of this CTA's partial (cached in L2 only)
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (q < nblk)
 #pragma unroll
-          for (int jj = 0; jj < 16; jj += 4)
-            st_async_v4(adst + (uint32_t)((c0 + 16 * q + jj) * 4), __uint_as_float(v[q][jj]),
-                        __uint_as_float(v[q][jj + 1]), __uint_as_float(v[q][jj + 2]), __uint_as_float(v[q][jj + 3]),
-                        abar);
+          for (int j = 0; j < 16; ++j) __stcg(gdst + (size_t)(c0 + 16 * q + j) * nfs, __uint_as_float(v[q][j]));
     } else {
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if (q < nblk)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst[(c0 + 16 * q + j) * dstride] = __uint_as_float(v[q][j]);
+          for (int j = 0; j < 16; ++j) dst[(c0 + 16 * q + j) * kGemmTileN] = __uint_as_float(v[q][j]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, ncols);
   griddep_wait();  // the epilogue reads and writes buffers of the preceding kernels
-  if (S > 1 && p.pull) {
-    cluster_arrive();  // this CTA's partials are staged
-    cluster_wait();
-  } else if (S > 1) {
-    if (!mbar_wait(recv_bar, 0)) set_status(p.status, DF_ERR_TIMEOUT);
-    cluster_arrive();  // this CTA has received everything pushed to it (its own pushes are done too)
+  if (S > 1) {
+    cluster_arrive();  // this CTA's partial is written (release: its global stores included)
+    cluster_wait();    // and so are the other ranks'
   }
   RedSrc red;
-  red.base = S == 1 ? acc_s : recv_s;
-  red.remote = S > 1 && p.pull;
-#pragma unroll
-  for (int k = 0; k < 8; ++k)
-    red.rb[k] = (red.remote && k < S) ? mapa_shared(smem_u32(acc_s + split * stage_stride), (uint32_t)k) : 0u;
+  red.base = acc_s;
+  red.g = S > 1 ? p.part + tile_cta0 * cta_floats + slice_off : nullptr;
+  red.gstride = (int)cta_floats;
   red.S = S;
-  red.n_pad = p.n_pad;
   red.nl = nl;
   const bool scaled = a.ss_in != nullptr;
   const bool norm_out = (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD) && a.g_next != nullptr;
@@ -699,10 +661,6 @@ __global__ void __launch_bounds__(kThreads, 3)  // three CTAs per SM must fit (s
       }
     }
   }
-  // no CTA may leave before every copy into or out of its shared memory has completed (or every
-  // read of its staged partials)
-  if (S > 1 && p.pull) cluster_arrive();
-  if (S > 1) cluster_wait();
 }
 
 template <int EPI>
@@ -755,8 +713,8 @@ int gemm_tiles(int n_out, int epi) {
 
 // Reduction splits (cluster size): the smallest power of two, at most 8, that gives every SM a
 // tile slice, with at least 2 k-blocks per CTA. Depends only on the weight shape and the context's
-// capacity, never on which flows are present. A split CTA receives its slice of the S partials
-// (512 B per padded activation row); contexts with more than 208 rows of capacity do not split.
+// capacity, never on which flows are present. Contexts with more than 208 rows of capacity do not
+// split (the split-K exchange area is sized for at most 208 padded rows).
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups) {
   const int tiles = gemm_tiles(n_out, epi) * groups;
   const int kb = k / kGemmTileK;
@@ -765,6 +723,14 @@ int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups) 
   int s = 1;
   while (s < 8 && tiles * s < ctx->num_sms && 2 * (2 * s) <= kb) s *= 2;
   return s;
+}
+
+// Floats of the split-K exchange area: every CTA of the largest split launch (tiles x S < 2 SMs'
+// worth, see gemm_splits) holds a 128 x padded-rows partial.
+size_t gemm_part_floats(const dualflow_ctx* ctx) {
+  const int max_rows = ((2 * ctx->cfg.max_batch + 15) / 16) * 16;
+  if (max_rows > kSplitMaxRows) return 0;
+  return (size_t)2 * ctx->num_sms * kGemmTileN * max_rows;
 }
 
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
@@ -806,27 +772,29 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
     rc = encode_map_2d_bf16(&mpf, a.pf_W, (uint64_t)a.pf_k, (uint64_t)a.pf_rows, (uint64_t)a.pf_k * 2, kGemmTileK, 64);
     if (rc != DF_OK) return rc;
   }
-  // data region: the pipeline stages; after the main loop the partial tile (512 B per activation
-  // row) or, when split, the staged slices plus the receive area (1 KB per row + bank pads). Then
-  // the barriers, the TMEM address slot and the 256-float row-scale array.
-  // as many stages (up to 4) as fit the budget that keeps two CTAs per SM; a grid of more than two
-  // CTAs per SM (grouped launches) keeps three per SM on fewer stages, so that it runs as one wave
+  // data region: the pipeline stages; after the main loop, unsplit, the accumulator tile (512 B
+  // per activation row). Then the barriers, the TMEM address slot and the 256-float row-scale array.
+  // as many stages (up to 4) as fit the budget that keeps two CTAs per SM; a grouped launch of more
+  // than two CTAs per SM keeps three per SM on fewer stages, so that it runs as one wave
   const int ctas = p.n_tiles * p.splits * groups;
   uint32_t tcols = 32;
   while ((int)tcols < p.n_pad) tcols <<= 1;
-  const bool three = ctas > 2 * ctx->num_sms && ctas <= 3 * ctx->num_sms && 3 * tcols <= 512 &&
+  const bool grouped_epi = a.epi == EPI_MOE_GATEUP || a.epi == EPI_MOE_DOWN;  // built for three per SM
+  const bool three = grouped_epi && ctas > 2 * ctx->num_sms && ctas <= 3 * ctx->num_sms && 3 * tcols <= 512 &&
                      2 * (kABytes + p.n_pad * 128) <= kStageBudget3 && 512 * p.n_pad <= kStageBudget3;
   // row-blocked (prefill) launches hold a 128 KB accumulator tile: one CTA per SM, so the pipeline
   // takes the room that leaves (the same bytes later hold the tile)
   p.stages = (a.row_blocked ? kStageBudgetRows : three ? kStageBudget3 : kStageBudget) / (kABytes + p.n_pad * 128);
   p.stages = p.stages > kStages ? kStages : (p.stages < 2 ? 2 : p.stages);
   const int pipe = p.stages * (kABytes + p.n_pad * 128);
-  // split-K partials: staged in the CTA's own pipeline bytes and pulled by their owners when the
-  // staging fits, else pushed from TMEM by asynchronous stores into the owners' receive areas
-  const int staged_pull = 512 * p.n_pad + 32 * p.splits;  // the S staged slices
-  p.pull = p.splits > 1 && staged_pull <= pipe;
-  p.push_async = (p.splits > 1 && !p.pull) ? 1 : 0;
-  const int parts = p.splits == 1 ? 512 * p.n_pad : p.push_async ? 512 * (p.n_pad + 4) : staged_pull;
+  // split-K partials go to the exchange area (sized at init for the largest split launch)
+  p.part = nullptr;
+  if (p.splits > 1) {
+    if (ctx->gemm_part == nullptr || (size_t)ctas * kGemmTileN * p.n_pad > ctx->gemm_part_floats)
+      return DF_ERR_UNSUPPORTED;
+    p.part = ctx->gemm_part;
+  }
+  const int parts = p.splits == 1 ? 512 * p.n_pad : 0;  // S == 1: the accumulator tile
   p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
   const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 8;
   switch (a.epi) {

@@ -149,6 +149,8 @@ struct dualflow_ctx {
   void* pf_o = nullptr;            // [pf_rows][Hq * D] bf16
   void* pf_u = nullptr;            // [pf_rows][F] bf16
   float* pf_ss = nullptr;          // [pf_rows][ss_ld]
+  float* gemm_part = nullptr;      // split-K partials exchanged through L2 (gemm_part_floats)
+  size_t gemm_part_floats = 0;
   int32_t* gen_tokens = nullptr;   // [max_batch] input tokens of the generation loop's next step
   int32_t* gen_out_dev = nullptr;  // [kGenHostMaxSteps][max_batch] dualflow_generate_host staging
   float* gen_u_dev = nullptr;      // [kGenHostMaxSteps][max_batch]
@@ -176,6 +178,7 @@ int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s);
 int gemm_splits(const dualflow_ctx* ctx, int n_out, int k, int epi, int groups = 1);
 int gemm_tiles(int n_out, int epi);
+size_t gemm_part_floats(const dualflow_ctx* ctx);
 // Fills cur's L2-prefetch fields from the (ungrouped) projection `next` that follows it.
 void gemm_prefetch_next(const dualflow_ctx* ctx, GemmArgs& cur, const GemmArgs& next);
 int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl = 0);

@@ -227,25 +227,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // ---------------------------------------------------------------------------------------------
 // Thread-block clusters: distributed shared memory
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
 // Address of the same shared-memory location in the cluster's CTA of rank `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
-}
-// No "memory" clobber: several of these may be in flight at once; ordering against the writes
-// they read comes from the cluster barrier (which clobbers memory) that precedes them.
-__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
 }
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   float v;
@@ -265,14 +251,6 @@ __device__ __forceinline__ void cluster_sync() {
 // The two halves of cluster_sync, so that work can be placed between them.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-
-// Asynchronous 16-byte store into shared memory of a CTA in the cluster (dst and its mbarrier as
-// shared::cluster addresses); completion is counted in bytes on that mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, float c, float d, uint32_t bar) {
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
-               "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
-               : "memory");
-}
 
 // Programmatic dependent launch: wait until the preceding kernel of the stream has completed and
 // its writes are visible (a no-op without the launch attribute); allow the next kernel to launch.
