@@ -24,7 +24,8 @@ C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dual
                "dualflow_stacked_linear", "dualflow_coupled_mlp", "dualflow_step", "dualflow_step_host",
                "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
                "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head",
-               "dualflow_generate", "dualflow_generate_host", "dualflow_prefill_reserve", "dualflow_prefill")
+               "dualflow_generate", "dualflow_generate_host", "dualflow_prefill_reserve", "dualflow_prefill",
+               "dualflow_prefill_slots", "dualflow_release_slots")
 DF_PROF_FAMILIES = 8
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
@@ -90,6 +91,9 @@ def load_library(path: str = LIB_PATH):
                                i32, vp], i32),
         "dualflow_prefill_reserve": ([vp, i32], i32),
         "dualflow_prefill": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp], i32),
+        "dualflow_prefill_slots": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, vp, i32, i32, vp, vp, vp],
+                                   i32),
+        "dualflow_release_slots": ([vp, POINTER(dualflow_kv), vp, i32, vp, vp, vp], i32),
         "dualflow_generate_host": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, i32, vp],
                                    i32),
     }
@@ -250,6 +254,24 @@ def dualflow_prefill(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens, batc
     rc = load_library().dualflow_prefill(ctx, ctypes.byref(w), ctypes.byref(kv), _ptr(tokens), batch, n_tok,
                                          _stream(stream))
     _check("dualflow_prefill", rc)
+
+
+def dualflow_prefill_slots(ctx, w: "dualflow_weights", kv: "dualflow_kv", tokens, slots, n_seq: int, n_tok: int,
+                           free_pages=None, n_free=None, stream=None) -> None:
+    """Primary-only prefill of tokens [n_seq, n_tok] into cache slots slots[i] (device int32, or
+    None for 0 .. n_seq - 1); paged contexts may pass a free list to map the prompts' pages."""
+    rc = load_library().dualflow_prefill_slots(ctx, ctypes.byref(w), ctypes.byref(kv), _ptr(tokens), _ptr(slots),
+                                               n_seq, n_tok, _ptr(free_pages), _ptr(n_free), _stream(stream))
+    _check("dualflow_prefill_slots", rc)
+
+
+def dualflow_release_slots(ctx, kv: "dualflow_kv", slots, n_slots: int, free_pages=None, n_free=None,
+                           stream=None) -> None:
+    """Ends the sequences of cache slots slots[0 .. n_slots): lengths to 0, a paged slot's pages
+    back on the free list."""
+    rc = load_library().dualflow_release_slots(ctx, ctypes.byref(kv), _ptr(slots), n_slots, _ptr(free_pages),
+                                               _ptr(n_free), _stream(stream))
+    _check("dualflow_release_slots", rc)
 
 
 def dualflow_sync_status(ctx, stream=None) -> int:

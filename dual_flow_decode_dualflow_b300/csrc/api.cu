@@ -857,7 +857,7 @@ int dualflow_step_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualf
 int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows) {
   if (!ctx || max_rows < 0) return DF_ERR_ARG;
   const dualflow_config& c = ctx->cfg;
-  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0 || c.paged) return DF_ERR_UNSUPPORTED;
+  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0) return DF_ERR_UNSUPPORTED;
   if (max_rows <= ctx->pf_rows) return DF_OK;
   for (void* p : {(void*)ctx->pf_h, ctx->pf_x, ctx->pf_q, ctx->pf_o, ctx->pf_u, (void*)ctx->pf_ss})
     if (p) cudaFree(p);
@@ -884,19 +884,30 @@ int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows) {
 
 int dualflow_prefill(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
                      int32_t batch, int32_t n_tok, dualflow_stream stream) {
+  return dualflow_prefill_slots(ctx, w, kv, tokens, nullptr, batch, n_tok, nullptr, nullptr, stream);
+}
+
+int dualflow_prefill_slots(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+                           const int32_t* tokens, const int32_t* slots, int32_t n_seq, int32_t n_tok,
+                           int32_t* free_pages, int32_t* n_free, dualflow_stream stream) {
   if (!ctx || !tokens) return DF_ERR_ARG;
   const dualflow_config& c = ctx->cfg;
-  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0 || c.paged) return DF_ERR_UNSUPPORTED;
+  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0) return DF_ERR_UNSUPPORTED;
   const int G = c.n_q_heads / c.n_kv_heads;
   if (G != 1 && G != 2 && G != 4) return DF_ERR_UNSUPPORTED;
-  if (batch <= 0 || batch > c.max_batch || n_tok < 0) return DF_ERR_SHAPE;
+  if ((free_pages == nullptr) != (n_free == nullptr)) return DF_ERR_ARG;
+  if (!c.paged && free_pages) return DF_ERR_ARG;
+  if (n_seq <= 0 || n_seq > c.max_batch || n_tok < 0) return DF_ERR_SHAPE;
   if (n_tok == 0) return DF_OK;
-  if ((long long)batch * n_tok > ctx->pf_rows) return DF_ERR_SHAPE;
+  if ((long long)n_seq * n_tok > ctx->pf_rows) return DF_ERR_SHAPE;
   DF_TRY(check_weights(ctx, w));
   if (!kv || kv->n_layers != c.n_layers) return DF_ERR_ARG;
   for (int l = 0; l < c.n_layers; ++l) DF_TRY(check_kv(ctx, kv, l));
   cudaStream_t s = S(stream);
-  const int R = batch * n_tok;
+  const int R = n_seq * n_tok;
+  int32_t* table = const_cast<int32_t*>(kv->page_table);
+  if (free_pages)
+    DF_TRY(launch_prefill_pages(c, kv->seq_len, slots, n_seq, n_tok, table, free_pages, n_free, ctx->status, s));
   const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
   const int d_tiles = (c.d_model + kGemmTileN - 1) / kGemmTileN;
   // the decode step's kernels on the prefill rows: the context's activation buffers point at the
@@ -928,6 +939,8 @@ int dualflow_prefill(dualflow_ctx* ctx, const dualflow_weights* w, const dualflo
     g.m_a = 0;
     g.row_blocked = 1;
     g.seq_rows = n_tok;
+    g.slots = slots;
+    g.max_batch = c.max_batch;
   };
   auto normed_input = [&](GemmArgs& g) {
     g.ss_in = ctx->ss;
@@ -954,10 +967,11 @@ int dualflow_prefill(dualflow_ctx* ctx, const dualflow_weights* w, const dualflo
     g.seq_len = kv->seq_len;
     g.k_cache = kv->k[l];
     g.v_cache = kv->v[l];
+    g.page_table = kv->page_table;
     normed_input(g);
     DF_TRY(launch_gemm_tc(ctx, g, s));
-    DF_TRY(launch_attention_prefill(c, ctx->q, ctx->o, kv->k[l], kv->v[l], kv->seq_len, batch, n_tok, ctx->status,
-                                    s));
+    DF_TRY(launch_attention_prefill(c, ctx->q, ctx->o, kv->k[l], kv->v[l], kv->seq_len, kv->page_table, slots, n_seq,
+                                    n_tok, ctx->status, s));
     GemmArgs o = gemm_args(ctx);
     o.x = ctx->o;
     o.W = w->Wo[l];
@@ -996,7 +1010,19 @@ int dualflow_prefill(dualflow_ctx* ctx, const dualflow_weights* w, const dualflo
     DF_TRY(launch_gemm_tc(ctx, dn, s));
     ss_parts = d_tiles;
   }
-  return launch_seq_advance(const_cast<int32_t*>(kv->seq_len), batch, n_tok, s);
+  return launch_seq_advance(const_cast<int32_t*>(kv->seq_len), slots, n_seq, c.max_batch, n_tok, s);
+}
+
+int dualflow_release_slots(dualflow_ctx* ctx, const dualflow_kv* kv, const int32_t* slots, int32_t n_slots,
+                           int32_t* free_pages, int32_t* n_free, dualflow_stream stream) {
+  if (!ctx || !kv || !kv->seq_len || !slots) return DF_ERR_ARG;
+  const dualflow_config& c = ctx->cfg;
+  if (n_slots < 0 || n_slots > c.max_batch) return DF_ERR_SHAPE;
+  if (c.paged && (!kv->page_table || !free_pages || !n_free)) return DF_ERR_ARG;
+  if (!c.paged && (free_pages || n_free)) return DF_ERR_ARG;
+  if (n_slots == 0) return DF_OK;
+  return launch_release_slots(c, const_cast<int32_t*>(kv->seq_len), slots, n_slots,
+                              const_cast<int32_t*>(kv->page_table), free_pages, n_free, ctx->status, S(stream));
 }
 
 int dualflow_generate_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,

@@ -5,7 +5,11 @@
 // p = seq_len[b] + t, and its query attends the cached keys/values of positions 0 .. p (the
 // prompt's own keys/values are already in the cache, written by the QKV projection).
 //
-// One CTA per (block of prompt positions, KV head g, sequence b): its 64 query rows are the G query
+// Prompt sequence i is held by cache slot b = slots[i] (or i); its keys/values sit in the contiguous
+// cache [max_batch, Hkv, max_ctx, D] or in the pages the slot's page-table row maps (every 16-byte
+// chunk of a key row is fetched from the row's own page, so any page size works).
+//
+// One CTA per (block of prompt positions, KV head g, prompt sequence i): its 64 query rows are the G query
 // heads of group g at 64 / G consecutive positions, so every K/V tile it loads serves all of
 // them. Four warps each own 16 query rows (one head, 16 positions): S = Q K^T and O += P V with
 // mma.sync m16n8k16 (queries as M), online softmax per row in the log2 domain, the causal bound
@@ -39,10 +43,13 @@ __device__ __forceinline__ void cp_async_wait() {
 struct PrefillAttnArgs {
   const __nv_bfloat16* q;  // [B * n_tok, Hq, D] post-RoPE
   __nv_bfloat16* o;        // [B * n_tok, Hq, D]
-  const __nv_bfloat16* k_cache;  // [max_batch, Hkv, max_ctx, D]
+  const __nv_bfloat16* k_cache;  // [max_batch, Hkv, max_ctx, D], or pages [max_pages, Hkv, page_size, D]
   const __nv_bfloat16* v_cache;
-  const int32_t* seq_len;  // [B] positions cached before the prompt
-  int n_tok, n_q_heads, n_kv_heads, max_ctx;
+  const int32_t* seq_len;  // [max_batch] positions cached before the prompt
+  const int32_t* slots;    // [n_seq] cache slot of each prompt sequence (nullptr: slot i)
+  const int32_t* page_table;  // paged: [max_batch, pages_per_seq]
+  int n_tok, n_q_heads, n_kv_heads, max_ctx, max_batch;
+  int paged, page_size, pages_per_seq, max_pages;
   float scale_log2;
   int32_t* status;
 };
@@ -52,8 +59,13 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const PrefillA
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const uint32_t sQ = smem_u32(smem), sK = sQ + kPfTile, sV = sK + 2 * kPfTile;
   const int Hq = A.n_q_heads, Hkv = A.n_kv_heads, G = Hq / Hkv, PP = kPfRows / G;
-  const int g = blockIdx.y, b = blockIdx.z, t0 = blockIdx.x * PP;
+  const int g = blockIdx.y, si = blockIdx.z, t0 = blockIdx.x * PP;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = A.slots ? A.slots[si] : si;  // cache slot
+  if (b < 0 || b >= A.max_batch) {
+    if (tid == 0) atomicCAS(A.status, 0, DF_ERR_DEVICE_BOUNDS);
+    return;
+  }
   const int L = A.seq_len[b];
   if (L < 0 || L + A.n_tok > A.max_ctx) {
     if (tid == 0) atomicCAS(A.status, 0, DF_ERR_DEVICE_BOUNDS);
@@ -62,21 +74,33 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const PrefillA
   const int npos = min(PP, A.n_tok - t0);
   const int last = L + t0 + npos - 1;       // the block's last absolute position
   const int ntiles = last / kPfKeys + 1;    // key tiles 0 .. last
-  const size_t kv_base = ((size_t)b * Hkv + g) * A.max_ctx * kHeadDim;
+  const size_t kv_base = A.paged ? 0 : ((size_t)b * Hkv + g) * A.max_ctx * kHeadDim;  // contiguous
 
   // Q block: row r = head hh (of the group) * PP + local position tl; rows past the prompt are zero
   for (int e = tid; e < kPfRows * 16; e += kPfThreads) {
     const int r = e >> 4, ch = e & 15, hh = r / PP, tl = r % PP;
     const bool ok = tl < npos;
     const __nv_bfloat16* src =
-        A.q + (((size_t)b * A.n_tok + (ok ? t0 + tl : 0)) * Hq + g * G + hh) * kHeadDim + ch * 8;
+        A.q + (((size_t)si * A.n_tok + (ok ? t0 + tl : 0)) * Hq + g * G + hh) * kHeadDim + ch * 8;
     cp_async16(sQ + pf_swz(r, ch), src, ok ? 16u : 0u);
   }
   auto load_tile = [&](int j, int st) {
     for (int e = tid; e < kPfKeys * 16; e += kPfThreads) {
       const int r = e >> 4, ch = e & 15, key = j * kPfKeys + r;
-      const bool ok = key <= last;  // later keys are masked; they are never read from global
-      const size_t off = kv_base + (size_t)(ok ? key : 0) * kHeadDim + ch * 8;
+      bool ok = key <= last;  // later keys are masked; they are never read from global
+      size_t off = 0;
+      if (ok && !A.paged) {
+        off = kv_base + (size_t)key * kHeadDim + ch * 8;
+      } else if (ok) {
+        const int lp = key / A.page_size;
+        const int pid = lp < A.pages_per_seq ? A.page_table[(size_t)b * A.pages_per_seq + lp] : -1;
+        if (pid < 0 || pid >= A.max_pages) {
+          ok = false;  // unmapped page: zeros, and the error is latched
+          atomicCAS(A.status, 0, DF_ERR_DEVICE_BOUNDS);
+        } else {
+          off = (((size_t)pid * Hkv + g) * A.page_size + key % A.page_size) * kHeadDim + ch * 8;
+        }
+      }
       cp_async16(sK + st * kPfTile + pf_swz(r, ch), A.k_cache + off, ok ? 16u : 0u);
       cp_async16(sV + st * kPfTile + pf_swz(r, ch), A.v_cache + off, ok ? 16u : 0u);
     }
@@ -196,10 +220,10 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const PrefillA
   for (int i = 0; i < 16; ++i) {
     const int d = 8 * i + dcol;
     if (tl0 < npos)
-      *reinterpret_cast<uint32_t*>(A.o + (((size_t)b * A.n_tok + t0 + tl0) * Hq + h0) * kHeadDim + d) =
+      *reinterpret_cast<uint32_t*>(A.o + (((size_t)si * A.n_tok + t0 + tl0) * Hq + h0) * kHeadDim + d) =
           pack_bf16x2(o[i][0] * inv0, o[i][1] * inv0);
     if (tl1 < npos)
-      *reinterpret_cast<uint32_t*>(A.o + (((size_t)b * A.n_tok + t0 + tl1) * Hq + h1) * kHeadDim + d) =
+      *reinterpret_cast<uint32_t*>(A.o + (((size_t)si * A.n_tok + t0 + tl1) * Hq + h1) * kHeadDim + d) =
           pack_bf16x2(o[i][2] * inv1, o[i][3] * inv1);
   }
 }
@@ -207,9 +231,10 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const PrefillA
 }  // namespace
 
 int launch_attention_prefill(const dualflow_config& c, const void* q, void* o, const void* k_cache,
-                             const void* v_cache, const int32_t* seq_len, int batch, int n_tok, int32_t* status,
-                             cudaStream_t s) {
-  if (batch <= 0 || n_tok <= 0) return DF_OK;
+                             const void* v_cache, const int32_t* seq_len, const int32_t* page_table,
+                             const int32_t* slots, int n_seq, int n_tok, int32_t* status, cudaStream_t s) {
+  if (n_seq <= 0 || n_tok <= 0) return DF_OK;
+  if (c.paged && (!page_table || c.page_size <= 0)) return DF_ERR_ARG;
   const int G = c.n_q_heads / c.n_kv_heads;
   if (c.head_dim != kHeadDim || (G != 1 && G != 2 && G != 4)) return DF_ERR_UNSUPPORTED;
   PrefillAttnArgs A;
@@ -218,6 +243,13 @@ int launch_attention_prefill(const dualflow_config& c, const void* q, void* o, c
   A.k_cache = static_cast<const __nv_bfloat16*>(k_cache);
   A.v_cache = static_cast<const __nv_bfloat16*>(v_cache);
   A.seq_len = seq_len;
+  A.slots = slots;
+  A.page_table = page_table;
+  A.paged = c.paged;
+  A.page_size = c.paged ? c.page_size : 1;
+  A.pages_per_seq = c.paged ? (c.max_ctx + c.page_size - 1) / c.page_size : 0;
+  A.max_pages = c.max_pages;
+  A.max_batch = c.max_batch;
   A.n_tok = n_tok;
   A.n_q_heads = c.n_q_heads;
   A.n_kv_heads = c.n_kv_heads;
@@ -229,7 +261,7 @@ int launch_attention_prefill(const dualflow_config& c, const void* q, void* o, c
   if (cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return DF_ERR_CUDA;
-  dim3 grid((n_tok + PP - 1) / PP, c.n_kv_heads, batch);
+  dim3 grid((n_tok + PP - 1) / PP, c.n_kv_heads, n_seq);
   attn_prefill_kernel<<<grid, kPfThreads, smem, s>>>(A);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }

@@ -595,9 +595,12 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
           }
         }
       } else if (EPI == EPI_PREFILL_QKV) {
-        // prompt token t of sequence b (activation row b * seq_rows + t) at position seq_len[b] + t
+        // prompt token t of prompt sequence i (activation row i * seq_rows + t), held by cache slot
+        // b = slots[i], at position seq_len[b] + t
         const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, grow = a.row_base + n;
-        const int b = grow / a.seq_rows, pos = a.seq_len[b] + grow % a.seq_rows;
+        const int si = grow / a.seq_rows, b = a.slots ? a.slots[si] : si;
+        const bool slot_ok = b >= 0 && b < a.max_batch;
+        const int pos = slot_ok ? a.seq_len[b] + grow % a.seq_rows : -1;
         if (pos < 0 || pos >= a.max_ctx) {
           set_status(p.status, DF_ERR_DEVICE_BOUNDS);
         } else {

@@ -86,8 +86,11 @@ struct GemmArgs {
   int pf_k, pf_rows, pf_tiles, pf_splits, pf_tile_rows, pf_half, pf_depth;
   // Prefill: more activation rows than one tile holds. The rows are cut into blocks of 256
   // (grid y), each CTA offsets y / x_next / ss_in / ss_out by its block; row_base is the block's
-  // first row, seq_rows the prompt positions per sequence (row r = b * seq_rows + t). m_a = 0.
+  // first row, seq_rows the prompt positions per sequence (row r = i * seq_rows + t). m_a = 0.
+  // Prompt sequence i lives in cache slot slots[i] (slots = nullptr: slot i), 0 <= slot < max_batch.
   int row_blocked, seq_rows, row_base;
+  const int32_t* slots;
+  int max_batch;
 };
 
 struct AttnArgs {
@@ -205,9 +208,13 @@ int launch_moe_combine(dualflow_ctx* ctx, float* h, int batch, int aux_on, const
 int launch_mixture_head(const float* logits, int batch, int vocab, const float* u, float* alpha, float* p_mix,
                         int32_t* token, int32_t* token2, int aux_on, cudaStream_t s);
 int launch_attention_prefill(const dualflow_config& c, const void* q, void* o, const void* k_cache,
-                             const void* v_cache, const int32_t* seq_len, int batch, int n_tok, int32_t* status,
-                             cudaStream_t s);
-int launch_seq_advance(int32_t* seq_len, int batch, int n, cudaStream_t s);
+                             const void* v_cache, const int32_t* seq_len, const int32_t* page_table,
+                             const int32_t* slots, int n_seq, int n_tok, int32_t* status, cudaStream_t s);
+int launch_seq_advance(int32_t* seq_len, const int32_t* slots, int n_seq, int max_batch, int n, cudaStream_t s);
+int launch_prefill_pages(const dualflow_config& c, const int32_t* seq_len, const int32_t* slots, int n_seq, int n,
+                         int32_t* table, int32_t* free_pages, int32_t* n_free, int32_t* status, cudaStream_t s);
+int launch_release_slots(const dualflow_config& c, int32_t* seq_len, const int32_t* slots, int n_slots, int32_t* table,
+                         int32_t* free_pages, int32_t* n_free, int32_t* status, cudaStream_t s);
 int launch_gen_advance(const dualflow_config& c, int32_t* seq_len, int batch, int32_t* table, int32_t* free_pages,
                        int32_t* n_free, int32_t* status, cudaStream_t s);
 int launch_rmsnorm(dualflow_ctx* ctx, const float* h, const void* g, void* x, int batch, int aux_on, cudaStream_t s);

@@ -298,17 +298,108 @@ __global__ void gen_advance_kernel(int32_t* seq_len, int B, int max_ctx, int pag
   }
 }
 
-__global__ void seq_advance_kernel(int32_t* seq_len, int B, int n) {
-  const int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B) seq_len[b] += n;
+__global__ void seq_advance_kernel(int32_t* seq_len, const int32_t* slots, int n_seq, int max_batch, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_seq) return;
+  const int b = slots ? slots[i] : i;
+  if (b >= 0 && b < max_batch) seq_len[b] += n;
+}
+
+// Before a prefill of n positions into the cache slots of the prompt sequences (slots[i], or i):
+// every page of a paged slot that positions seq_len[b] .. seq_len[b] + n touch (the prompt, and the
+// slot the next decode step writes, while it is below max_ctx) and that the table does not map yet
+// is taken from the top of the free list, in prompt order and page order. One thread: the page
+// assignment does not depend on scheduling. A slot or page outside the table, or an empty free
+// list, latches DF_ERR_DEVICE_BOUNDS and leaves the rest of that sequence's pages unmapped (the
+// prefill's accesses there are then skipped and latch the same error).
+__global__ void prefill_pages_kernel(const int32_t* seq_len, const int32_t* slots, int n_seq, int n, int max_batch,
+                                     int max_ctx, int page_size, int32_t* table, int pages_per_seq, int max_pages,
+                                     int32_t* free_pages, int32_t* n_free, int32_t* status) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  for (int i = 0; i < n_seq; ++i) {
+    const int b = slots ? slots[i] : i;
+    if (b < 0 || b >= max_batch) {
+      atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const int L = seq_len[b];
+    if (L < 0 || L + n > max_ctx) {
+      atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    const int last = min(L + n, max_ctx - 1);
+    for (int j = L / page_size; j <= last / page_size; ++j) {
+      int32_t* e = table + (size_t)b * pages_per_seq + j;
+      if (j >= pages_per_seq) {
+        atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+        break;
+      }
+      if (*e >= 0) continue;
+      const int nf = *n_free;
+      const int pid = nf > 0 ? free_pages[nf - 1] : -1;
+      if (pid < 0 || pid >= max_pages) {
+        atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+        break;
+      }
+      *e = pid;
+      *n_free = nf - 1;
+    }
+  }
+}
+
+// Ends the sequences held by the listed cache slots: a paged slot's mapped pages go back on top of
+// the free list in page order and its table row is cleared; every listed slot's length becomes 0.
+// One thread. A slot outside the table, or a free list that already holds max_pages entries,
+// latches DF_ERR_DEVICE_BOUNDS (the page then stays mapped to the slot).
+__global__ void release_slots_kernel(int32_t* seq_len, const int32_t* slots, int n, int max_batch, int paged,
+                                     int32_t* table, int pages_per_seq, int max_pages, int32_t* free_pages,
+                                     int32_t* n_free, int32_t* status) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  for (int i = 0; i < n; ++i) {
+    const int b = slots[i];
+    if (b < 0 || b >= max_batch) {
+      atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+      continue;
+    }
+    if (paged)
+      for (int j = 0; j < pages_per_seq; ++j) {
+        int32_t* e = table + (size_t)b * pages_per_seq + j;
+        if (*e < 0) continue;
+        const int nf = *n_free;
+        if (nf < 0 || nf >= max_pages) {
+          atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+          continue;
+        }
+        free_pages[nf] = *e;
+        *n_free = nf + 1;
+        *e = -1;
+      }
+    seq_len[b] = 0;
+  }
 }
 
 }  // namespace
 
-// After a prefill of n positions: every sequence's cached length grows by n (the bounds were
-// checked by the kernels that wrote the entries).
-int launch_seq_advance(int32_t* seq_len, int batch, int n, cudaStream_t s) {
-  seq_advance_kernel<<<(batch + 127) / 128, 128, 0, s>>>(seq_len, batch, n);
+// After a prefill of n positions: the cached length of every prompt sequence's slot grows by n (the
+// bounds were checked by the kernels that wrote the entries).
+int launch_seq_advance(int32_t* seq_len, const int32_t* slots, int n_seq, int max_batch, int n, cudaStream_t s) {
+  seq_advance_kernel<<<(n_seq + 127) / 128, 128, 0, s>>>(seq_len, slots, n_seq, max_batch, n);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_prefill_pages(const dualflow_config& c, const int32_t* seq_len, const int32_t* slots, int n_seq, int n,
+                         int32_t* table, int32_t* free_pages, int32_t* n_free, int32_t* status, cudaStream_t s) {
+  const int pps = (c.max_ctx + c.page_size - 1) / c.page_size;
+  prefill_pages_kernel<<<1, 32, 0, s>>>(seq_len, slots, n_seq, n, c.max_batch, c.max_ctx, c.page_size, table, pps,
+                                        c.max_pages, free_pages, n_free, status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_release_slots(const dualflow_config& c, int32_t* seq_len, const int32_t* slots, int n_slots, int32_t* table,
+                         int32_t* free_pages, int32_t* n_free, int32_t* status, cudaStream_t s) {
+  const int pps = c.paged ? (c.max_ctx + c.page_size - 1) / c.page_size : 0;
+  release_slots_kernel<<<1, 32, 0, s>>>(seq_len, slots, n_slots, c.max_batch, c.paged, table, pps, c.max_pages,
+                                        free_pages, n_free, status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 

@@ -231,10 +231,10 @@ DF_API int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const
                              int32_t* tokens_out, float* logits, float* logits_all, int32_t* free_pages,
                              int32_t* n_free, int32_t aux_on, dualflow_stream stream);
 
-/* Workspace for dualflow_prefill: room for max_rows = batch * prompt tokens activation rows
- * (about (4 d + 4 Hq D + 2 F + 4 ss) bytes per row). Allocates (cold call, not for a hot loop);
- * a smaller request than the current room does nothing. bf16 dense contiguous-cache contexts only
- * (DF_ERR_UNSUPPORTED otherwise); DF_ERR_OOM leaves no prefill room. */
+/* Workspace for dualflow_prefill / dualflow_prefill_slots: room for max_rows = prompt sequences *
+ * prompt tokens activation rows (about (4 d + 4 Hq D + 2 F + 4 ss) bytes per row). Allocates (cold
+ * call, not for a hot loop); a smaller request than the current room does nothing. bf16 dense
+ * contexts only (DF_ERR_UNSUPPORTED otherwise); DF_ERR_OOM leaves no prefill room. */
 DF_API int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows);
 
 /* Primary-only prefill ("Custos de Inferencia vs. Treinamento", gist.science technical summary: the
@@ -245,11 +245,43 @@ DF_API int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows);
  * the cached positions 0 .. itself (causal). Then seq_len[b] += n_tok (device). No logits: the
  * caller runs the prompt's last token as the first decode step (dualflow_step / dualflow_generate),
  * where the auxiliary flow joins. Needs dualflow_prefill_reserve(ctx, >= batch * n_tok)
- * (DF_ERR_SHAPE otherwise); bf16 dense contexts with contiguous caches and G = Hq / Hkv in
- * {1, 2, 4} (DF_ERR_UNSUPPORTED otherwise). A position seq_len[b] + t >= max_ctx latches
- * DF_ERR_DEVICE_BOUNDS. Asynchronous on `stream`, launched eagerly (no graph). */
+ * (DF_ERR_SHAPE otherwise); bf16 dense contexts with G = Hq / Hkv in {1, 2, 4}
+ * (DF_ERR_UNSUPPORTED otherwise). A position seq_len[b] + t >= max_ctx latches
+ * DF_ERR_DEVICE_BOUNDS; so does, with a paged cache, a prompt position whose page the table does
+ * not map (this call takes no free list: see dualflow_prefill_slots). Asynchronous on `stream`,
+ * launched eagerly (no graph). Same as dualflow_prefill_slots(ctx, w, kv, tokens, NULL, batch,
+ * n_tok, NULL, NULL, stream). */
 DF_API int dualflow_prefill(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
                             const int32_t* tokens, int32_t batch, int32_t n_tok, dualflow_stream stream);
+
+/* Continuous batching, admission: the primary-only prefill of dualflow_prefill for n_seq prompts
+ * (device int32 tokens [n_seq, n_tok]) into chosen cache slots: prompt i goes to slot slots[i]
+ * (device int32 [n_seq], distinct values in [0, max_batch); NULL: slot i), at positions
+ * seq_len[slots[i]] + t, and afterwards seq_len[slots[i]] += n_tok. The other slots' cache
+ * entries, lengths and table rows are not touched. A new sequence enters a slot whose length is
+ * 0 (dualflow_release_slots). Paged contexts: with a free list (free_pages: device int32 array of
+ * free physical page ids, *n_free of them in use, the top at free_pages[*n_free - 1]; both NULL or
+ * both set), first every page that positions seq_len[b] .. seq_len[b] + n_tok of a slot touch
+ * (the prompt and the slot the next decode step writes, below max_ctx) and that the table does
+ * not map yet is popped from the top of the free list, prompt by prompt in page order, on the
+ * device; without one the table must already map the prompt's pages. An empty free list, a slot
+ * outside [0, max_batch) or an unmapped page latches DF_ERR_DEVICE_BOUNDS and the affected
+ * writes are skipped. Contiguous contexts take no free list (DF_ERR_ARG). n_seq in [1, max_batch]
+ * and n_seq * n_tok <= the reserved rows (DF_ERR_SHAPE otherwise). Asynchronous on `stream`. */
+DF_API int dualflow_prefill_slots(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv,
+                                  const int32_t* tokens, const int32_t* slots, int32_t n_seq, int32_t n_tok,
+                                  int32_t* free_pages, int32_t* n_free, dualflow_stream stream);
+
+/* Continuous batching, retirement: ends the sequences held by the cache slots slots[0 .. n_slots)
+ * (device int32, distinct values in [0, max_batch)). Every listed slot's length becomes 0; in a
+ * paged context its mapped pages are pushed on top of the free list in page order
+ * (free_pages[(*n_free)++] = page; the array must hold max_pages entries) and its table row is
+ * set to -1. Cache contents are left as they are (a new sequence overwrites them). A slot outside
+ * [0, max_batch), or a free list already holding max_pages entries, latches DF_ERR_DEVICE_BOUNDS.
+ * Paged contexts need free_pages and n_free, contiguous ones take neither (DF_ERR_ARG);
+ * 0 <= n_slots <= max_batch (DF_ERR_SHAPE). One device thread, asynchronous on `stream`. */
+DF_API int dualflow_release_slots(dualflow_ctx* ctx, const dualflow_kv* kv, const int32_t* slots, int32_t n_slots,
+                                  int32_t* free_pages, int32_t* n_free, dualflow_stream stream);
 
 /* dualflow_generate with HOST buffers, for contiguous caches: copies tokens_host [batch] (and
  * u_host [n_steps, batch] if not NULL) to the device, runs n_steps of the decode loop (step, mixture

@@ -74,3 +74,10 @@ def test_null_arguments_rejected():
     assert lib.dualflow_coupled_mlp(None, None, None, 0, 1, 1, None, None) == dfl.DF_ERR_ARG
     assert lib.dualflow_set_graphs(None, 1) == dfl.DF_ERR_ARG
     assert lib.dualflow_sync_status(None, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_mixture_head(None, None, 1, None, None, None, None, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_generate(None, None, None, None, 1, 1, None, None, None, None, None, None, 1,
+                                 None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_prefill_reserve(None, 16) == dfl.DF_ERR_ARG
+    assert lib.dualflow_prefill(None, None, None, None, 1, 1, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_prefill_slots(None, None, None, None, None, 1, 1, None, None, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_release_slots(None, None, None, 1, None, None, None) == dfl.DF_ERR_ARG

@@ -99,3 +99,54 @@ def test_prefill_rejects_without_room(cuda_device):
         assert np.array_equal(run.seq_len.cpu().numpy(), run.seq_len_np)  # nothing ran
     finally:
         run.close()
+
+
+def test_prefill_into_released_slot(cuda_device):
+    """Continuous batching on a contiguous cache: the sequence of slot 1 ends (length 0) and a new
+    prompt is prefilled into that slot alone. The other slots' cache entries and lengths stay bit
+    for bit; the new prompt's keys/values, and a decode step of all slots after it, match the
+    oracle (the new sequence prefilled from an empty cache, the others as they were)."""
+    w, _, _ = CASES["g4_b3_n9"]
+    n = 23
+    run = H.DeviceRun(w, cuda_device)
+    try:
+        L = run.seq_len_np.astype(np.int64)
+        slot = torch.tensor([1], dtype=torch.int32, device=cuda_device)
+        before = {k: v.clone() for k, v in run.t.items() if k.endswith((".K", ".V"))}
+        dfl.dualflow_release_slots(run.ctx, run.kv, slot, 1)
+        assert run.status() == 0
+        assert np.array_equal(run.seq_len.cpu().numpy(), [L[0], 0, L[2]])
+        prompt = np.random.default_rng(43).integers(0, w.vocab, size=(1, n)).astype(np.int32)
+        dfl.dualflow_prefill_reserve(run.ctx, n)
+        dfl.dualflow_prefill_slots(run.ctx, run.weights, run.kv, torch.from_numpy(prompt).to(cuda_device), slot, 1, n)
+        assert run.status() == 0
+        L2 = np.array([L[0], n, L[2]])
+        assert np.array_equal(run.seq_len.cpu().numpy(), L2)
+
+        caches = _oracle_caches(w)
+        glob = {"E1": H.LazyRows(w, "E1"), "E2": H.LazyRows(w, "E2"), "W_lm": H.host_f64(w, "W_lm"),
+                "g_final": H.host_f64(w, "g_final")}
+        layers = H.LazyLayers(w)
+        O.prefill(H.hparams(w), glob, layers, [O.DenseCache(K=c.K[1:2], V=c.V[1:2]) for c in caches], prompt,
+                  np.array([0]), mirror=True)
+        for l in range(w.n_layers):
+            for kind in ("K", "V"):
+                t = run.t[f"L{l}.{kind}"]
+                ref = caches[l].K if kind == "K" else caches[l].V
+                err = H.rel_err(H.to_f64(t[1, :, :n, :]), ref[1][:, :n, :])
+                assert err <= TOL, f"layer {l} {kind}: rel err {err:.3e}"
+                exp = before[f"L{l}.{kind}"].clone()
+                exp[1, :, :n, :] = t[1, :, :n, :]
+                assert torch.equal(exp, t), f"layer {l} {kind}: cache changed outside the new prompt's rows"
+
+        nxt = np.random.default_rng(44).integers(0, w.vocab, size=w.batch).astype(np.int32)
+        run.tokens.copy_(torch.from_numpy(nxt))
+        run.step(aux_on=1)
+        assert run.status() == 0
+        ref = O.decode_step(H.hparams(w), glob, layers, caches, nxt, L2, aux_on=True, mirror=True)
+        got = H.to_f64(run.logits)
+        for f in range(2):
+            err = H.rel_err(got[f], ref["logits"][f])
+            assert err <= TOL, f"decode after the slot prefill, flow {f + 1}: rel err {err:.3e}"
+    finally:
+        run.close()
