@@ -38,6 +38,41 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6400.0
 
 
+class Replicas:
+    """Multi-GPU mode: one replica of the decode path per rank. Sequences are independent and each
+    sequence's cache lives with it, so the batch shards across ranks with no exchange on the data
+    path; the only collectives are the timing bookkeeping around it: a barrier on both sides of
+    every timed region and the maximum of each measured time over the ranks."""
+
+    def __init__(self, rank: int = 0, world: int = 1, device=None):
+        self.rank, self.world, self.device = rank, world, device
+
+    @staticmethod
+    def from_env() -> tuple[int, int, int]:
+        """(RANK, WORLD_SIZE, LOCAL_RANK) as torchrun sets them; a single process without it."""
+        env = os.environ
+        return int(env.get("RANK", "0")), int(env.get("WORLD_SIZE", "1")), int(env.get("LOCAL_RANK", "0"))
+
+    def barrier(self) -> None:
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, *vals: float) -> list[float]:
+        """Each value's maximum over the ranks (every rank gets the result)."""
+        if self.world == 1:
+            return [float(v) for v in vals]
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=self.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return [float(x) for x in t.tolist()]
+
+    def rate(self, units_per_rank: float, seconds: float) -> float:
+        """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+        return self.world * units_per_rank / seconds
+
+
 def load_peaks() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -368,7 +403,7 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    dist = torch.distributed if world > 1 else None
+    reps = Replicas(rank, world, dev)
     nb = call_bytes(w)
     copies = max(1, min(16, -(-3 * 126 * 2 ** 20 // nb["total"])))
     runs = [H.DeviceRun(w, dev) for _ in range(copies)]
@@ -394,8 +429,7 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
             for _ in range(max(1, args.warmup // copies)):
                 graph.replay()
         stream.synchronize()
-        if dist:
-            dist.barrier()
+        reps.barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with (sampler if sampler is not None else _Null()):
@@ -409,11 +443,9 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
             e1.synchronize()
             if sampler is not None:
                 sampler.mark(False)
-        ms = e0.elapsed_time(e1) / steps
-        if dist:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        torch.cuda.synchronize()
+        reps.barrier()
+        (ms,) = reps.max(e0.elapsed_time(e1) / steps)
         return ms
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
@@ -448,7 +480,7 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
     cpu_s = samp.full_call(samp.time_rows(rows), rows)
     unit = "sequence-steps/s (one layer)"
     return {
-        "metric": METRIC, "value": world * w.batch / (ms * 1e-3), "unit": unit, "n_gpus": world,
+        "metric": METRIC, "value": reps.rate(w.batch, ms * 1e-3), "unit": unit, "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
         "data": "synthetic: seeded counter-hash generator, random-init weights of the workload's shapes",
@@ -466,7 +498,7 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
                      "avg_launch_ms": ms, "traffic": None},
         "cpu_baseline": {"value": w.batch / cpu_s, "unit": unit, "cores": blas_threads(), "kind": "oracle",
                          "sample": samp.describe(rows)},
-        "e2e": {"value": world * w.batch / e2e_s, "unit": unit,
+        "e2e": {"value": reps.rate(w.batch, e2e_s), "unit": unit,
                 "h2d_bytes_per_step": int((q1_h.numel() + h2_h.numel()) * 2), "d2h_bytes_per_step": int(o_h.numel() * 2),
                 "api": "dualflow_decode_attention with q1, h2 copied from pinned host memory and o copied back, "
                        "stream sync per step"},
@@ -485,7 +517,7 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    dist = torch.distributed if world > 1 else None
+    reps = Replicas(rank, world, dev)
     run = H.DeviceRun(w, dev)
     stream = torch.cuda.Stream(device=dev)
     n_tok = PREFILL_TOKENS
@@ -502,8 +534,8 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
     for _ in range(args.warmup):
         once(prompt)
     stream.synchronize()
-    if dist:
-        dist.barrier()
+    reps.barrier()
+    torch.cuda.synchronize()
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with sampler:
@@ -515,6 +547,8 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
             e1.record(stream)
         e1.synchronize()
         sampler.mark(False)
+    torch.cuda.synchronize()
+    reps.barrier()
     ms = e0.elapsed_time(e1) / steps
     st = dfl.dualflow_sync_status(run.ctx)
     if st != 0:
@@ -531,11 +565,7 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
         stream.synchronize()
         if i >= 3:
             e2e.append(time.perf_counter() - t0)
-    e2e_s = statistics.median(e2e)
-    if dist:
-        t = torch.tensor([ms, e2e_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_s = float(t[0].item()), float(t[1].item())
+    ms, e2e_s = reps.max(ms, statistics.median(e2e))
     run.close()
     if rank != 0:
         return None
@@ -549,9 +579,9 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
     tflops = flops / (ms * 1e-3) / 1e12
     samp = PrefillOracleSample(w, 8, n_tok)
     cpu_s = samp.full(samp.time())
-    tokens = world * w.batch * n_tok
     return {
-        "metric": "primary-only prefill tokens/s at 1 B300", "value": tokens / (ms * 1e-3), "unit": "prefill tokens/s",
+        "metric": "primary-only prefill tokens/s at 1 B300", "value": reps.rate(w.batch * n_tok, ms * 1e-3),
+        "unit": "prefill tokens/s",
         "n_gpus": world, "steps": steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
         "data": "synthetic: seeded counter-hash generator, random-init weights of the workload's shapes",
@@ -564,7 +594,7 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
                      "peak_kind": kind, "flops_per_step": flops, "traffic": None},
         "cpu_baseline": {"value": w.batch * n_tok / cpu_s, "unit": "prefill tokens/s", "cores": blas_threads(),
                          "kind": "oracle", "sample": samp.describe()},
-        "e2e": {"value": tokens / e2e_s, "unit": "prefill tokens/s", "h2d_bytes_per_step": int(prompt_np.nbytes),
+        "e2e": {"value": reps.rate(w.batch * n_tok, e2e_s), "unit": "prefill tokens/s", "h2d_bytes_per_step": int(prompt_np.nbytes),
                 "d2h_bytes_per_step": 0,
                 "api": "dualflow_prefill with the prompt copied from pinned host memory, stream sync per call"},
         "gpu_launches": steps * (1 + 5 * w.n_layers + 1), "launches_per_step": 1 + 5 * w.n_layers + 1,
@@ -580,7 +610,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    dist = torch.distributed if world > 1 else None
+    reps = Replicas(rank, world, dev)
     run = H.DeviceRun(w, dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -589,8 +619,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
             for _ in range(warmup):
                 run.step(aux_on=aux_on, stream=stream)
         stream.synchronize()
-        if dist:
-            dist.barrier()
+        reps.barrier()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ctx = sampler if sampler is not None else _Null()
@@ -606,13 +635,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
             if sampler is not None:
                 sampler.mark(False)
         torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        ms = e0.elapsed_time(e1) / steps
-        if dist:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        reps.barrier()
+        (ms,) = reps.max(e0.elapsed_time(e1) / steps)
         return ms
 
     sampler = ClockSampler(dev.index if dev.index is not None else 0)
@@ -631,7 +655,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     if args.quick:
         run.close()
         if rank == 0:
-            return {"metric": METRIC, "value": world * w.batch / (ms * 1e-3), "unit": "tokens/s",
+            return {"metric": METRIC, "value": reps.rate(w.batch, ms * 1e-3), "unit": "tokens/s",
                     "ms_per_step": ms, "steps": args.steps, "warmup": args.warmup, "n_gpus": world,
                     "config": {"workload": w.name, "layers": w.n_layers}, "note": "quick run (no extras)"}
         return None
@@ -670,8 +694,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
 
     for _ in range(3):
         e2e_call()
-    if dist:
-        dist.barrier()
+    reps.barrier()
     e2e_steps = max(args.steps // 2, 3)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
@@ -684,10 +707,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     for _ in range(e2e_steps):
         dfl.dualflow_step_host(run.ctx, run.weights, run.kv, tok, w.batch, out, 1, stream)
     e2e_logits_s = (time.perf_counter() - t0) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_s, e2e_logits_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s, e2e_logits_s = float(t[0].item()), float(t[1].item())
+    e2e_s, e2e_logits_s = reps.max(e2e_s, e2e_logits_s)
 
     # the decode loop: dualflow_generate (step, mixture head, greedy choice, length advance) for
     # gen_n tokens; the lengths are restored before each repetition so the context stays the
@@ -714,7 +734,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
             raise RuntimeError(f"device status after the decode loop: {dfl.dualflow_status_string(st)}")
         gen = {"api": "dualflow_generate (greedy choice from the mixture head, in-loop length advance)",
                "tokens_per_loop": gen_n, "ms_per_token_step": gen_ms,
-               "tokens_per_s": world * w.batch / (gen_ms * 1e-3)}
+               "tokens_per_s": reps.rate(w.batch, gen_ms * 1e-3)}
     run.close()
     if rank != 0:
         return None
@@ -730,7 +750,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     cpu_desc = samp.describe(4)
     launches_per_step = int(sum(launches))
     res = {
-        "metric": METRIC, "value": world * w.batch / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": reps.rate(w.batch, ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
         "data": "synthetic: seeded counter-hash generator, random-init weights of the workload's shapes",
@@ -754,12 +774,12 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         "kernel_share": {n: fam_ms[i] / nprof / prof_total for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
         "cpu_baseline": {"value": w.batch / cpu_s, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                          "sample": cpu_desc},
-        "e2e": {"value": world * w.batch / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": int(tok.numel() * 4),
+        "e2e": {"value": reps.rate(w.batch, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": int(tok.numel() * 4),
                 "d2h_bytes_per_step": int((out if w.paged else tok_out).numel() * 4),
                 "api": ("dualflow_step_host (pinned host tokens in, host logits out, sync per step)" if w.paged else
                         "dualflow_generate_host, one step per call (pinned host tokens in, the step's chosen "
                         "tokens out, stream sync per step)")},
-        "e2e_logits": {"value": world * w.batch / e2e_logits_s, "unit": "tokens/s",
+        "e2e_logits": {"value": reps.rate(w.batch, e2e_logits_s), "unit": "tokens/s",
                        "h2d_bytes_per_step": int(tok.numel() * 4), "d2h_bytes_per_step": int(out.numel() * 4),
                        "api": "dualflow_step_host (pinned host tokens in, host logits [2, B, V] out, sync per step)"},
         "generate": gen,
@@ -841,9 +861,7 @@ def main():
     w = workload(args.workload)
     if args.layers:
         w = w.replace(n_layers=args.layers)
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    rank, world, local_rank = Replicas.from_env()
     if args.impl == "reference":
         if rank != 0:
             return
