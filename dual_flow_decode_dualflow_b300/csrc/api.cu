@@ -531,6 +531,88 @@ void drop_graphs(dualflow_ctx* ctx) {
   ctx->graphs.clear();
 }
 
+// The MoE MLP of a prefill layer, primary flow only, on the R prompt rows (x = the norm operand
+// with ss_parts partial sums of squares per row, in the context's prefill buffers): router logits,
+// the top-k decision, every row gathered once per chosen expert (expert-major), each expert's
+// gate/up + SwiGLU and down projection on its own rows only (row-blocked tcgen05 launches over
+// the gathered blocks), then the mix in set order with the residual and the next layer's norm
+// operand. The same arithmetic per row as the decode step's MoE MLP for the primary flow.
+int prefill_moe(dualflow_ctx* ctx, const dualflow_weights* w, int l, int R, int ss_parts, cudaStream_t s) {
+  const dualflow_config& c = ctx->cfg;
+  const int E = c.n_experts, RK = R * c.topk_primary, d = c.d_model, F = c.ffn_hidden;
+  auto scaled = [&](GemmArgs& g, const float* ss) {
+    g.ss_in = ss;
+    g.ss_parts = ss_parts;
+    g.ss_ld = ctx->ss_ld;
+    g.inv_d = 1.0f / (float)d;
+    g.eps = c.rms_eps;
+  };
+  GemmArgs r = gemm_args(ctx);
+  r.x = ctx->x;
+  r.W = w->Wr[l];
+  r.n_out = E;
+  r.k = d;
+  r.m_p = R;
+  r.row_blocked = 1;
+  r.seq_rows = 1;
+  r.epi = EPI_STORE_F32;
+  r.y = ctx->pf_rlog;
+  r.ldy = E;
+  scaled(r, ctx->ss);
+  DF_TRY(launch_gemm_tc(ctx, r, s));
+  DF_TRY(launch_moe_route_rows(c, ctx->pf_rlog, R, ctx->pf_sel_pos, ctx->pf_sel_w, s));
+  DF_TRY(launch_moe_plan(c, R, ctx->pf_sel_pos, ctx->pf_perm, ctx->pf_pos, ctx->pf_blk, ctx->pf_nblk, ctx->status, s));
+  DF_TRY(launch_moe_gather(RK, R, d, ctx->x, ctx->ss, ctx->ss_ld, ctx->pf_perm, ctx->pf_xg, ctx->pf_ssg, ctx->status,
+                           s));
+  auto gathered = [&](GemmArgs& g) {
+    g.m_p = RK;
+    g.row_blocked = 1;
+    g.seq_rows = 1;
+    g.n_groups = E;
+    g.blk_info = ctx->pf_blk;
+    g.n_blk = ctx->pf_nblk;
+  };
+  GemmArgs gu = gemm_args(ctx);
+  gu.x = ctx->pf_xg;
+  gu.W = w->We_gu[l];
+  gu.n_out = F;
+  gu.k = d;
+  gu.epi = EPI_SWIGLU;
+  gu.y = ctx->pf_ug;
+  gu.ldy = F;
+  gu.vec = w->b[l];
+  gu.w_group_rows = 2 * F;
+  gathered(gu);
+  scaled(gu, ctx->pf_ssg);
+  DF_TRY(launch_gemm_tc(ctx, gu, s));
+  GemmArgs dn = gemm_args(ctx);
+  dn.x = ctx->pf_ug;
+  dn.W = w->We_d[l];
+  dn.n_out = d;
+  dn.k = F;
+  dn.epi = EPI_STORE_F32;
+  dn.y = ctx->pf_yg;
+  dn.ldy = d;
+  dn.w_group_rows = d;
+  gathered(dn);
+  DF_TRY(launch_gemm_tc(ctx, dn, s));
+  const void* g_next = l + 1 < c.n_layers ? w->g_attn[l + 1] : nullptr;
+  return launch_moe_combine_rows(c, R, ctx->pf_yg, ctx->pf_sel_pos, ctx->pf_sel_w, ctx->pf_pos, ctx->h, g_next, ctx->x,
+                                 ctx->ss, ctx->ss_ld, ctx->status, s);
+}
+
+// Frees the prefill MoE workspace (nullptr-safe).
+void free_prefill_moe(dualflow_ctx* ctx) {
+  void* ps[] = {ctx->pf_rlog, ctx->pf_sel_pos, ctx->pf_sel_w, ctx->pf_perm, ctx->pf_pos, ctx->pf_xg,
+                ctx->pf_ssg,  ctx->pf_ug,      ctx->pf_yg,    ctx->pf_blk,  ctx->pf_nblk};
+  for (void* p : ps)
+    if (p) cudaFree(p);
+  ctx->pf_rlog = ctx->pf_sel_w = ctx->pf_ssg = ctx->pf_yg = nullptr;
+  ctx->pf_sel_pos = ctx->pf_perm = ctx->pf_pos = ctx->pf_nblk = nullptr;
+  ctx->pf_xg = ctx->pf_ug = nullptr;
+  ctx->pf_blk = nullptr;
+}
+
 }  // namespace
 
 // ================================================================== C ABI
@@ -647,6 +729,7 @@ int dualflow_free(dualflow_ctx* ctx) {
                   ctx->pf_h,   ctx->pf_x,    ctx->pf_q,      ctx->pf_o,     ctx->pf_u,     ctx->pf_ss, ctx->gemm_part};
   for (void* p : ptrs)
     if (p) cudaFree(p);
+  free_prefill_moe(ctx);
   delete ctx;
   return DF_OK;
 }
@@ -857,8 +940,10 @@ int dualflow_step_host(dualflow_ctx* ctx, const dualflow_weights* w, const dualf
 int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows) {
   if (!ctx || max_rows < 0) return DF_ERR_ARG;
   const dualflow_config& c = ctx->cfg;
-  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0) return DF_ERR_UNSUPPORTED;
+  if (c.dtype != DF_DTYPE_BF16) return DF_ERR_UNSUPPORTED;
+  if (c.n_experts > 32) return DF_ERR_UNSUPPORTED;
   if (max_rows <= ctx->pf_rows) return DF_OK;
+  free_prefill_moe(ctx);
   for (void* p : {(void*)ctx->pf_h, ctx->pf_x, ctx->pf_q, ctx->pf_o, ctx->pf_u, (void*)ctx->pf_ss})
     if (p) cudaFree(p);
   ctx->pf_h = nullptr;
@@ -878,6 +963,24 @@ int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows) {
   }
   ctx->pf_h = static_cast<float*>(h);
   ctx->pf_ss = static_cast<float*>(ss);
+  if (c.n_experts > 0) {
+    // the MoE rows: routing of every row, then each row once per chosen expert, gathered
+    const size_t E = c.n_experts, RK = R * c.topk_primary, d = c.d_model, F = c.ffn_hidden;
+    if (dalloc(&ctx->pf_rlog, R * E * 4) != DF_OK || dalloc(&ctx->pf_sel_pos, R * E * 4) != DF_OK ||
+        dalloc(&ctx->pf_sel_w, R * E * 4) != DF_OK || dalloc(&ctx->pf_perm, RK * 4) != DF_OK ||
+        dalloc(&ctx->pf_pos, RK * 4) != DF_OK || dalloc(&ctx->pf_xg, RK * d * 2) != DF_OK ||
+        dalloc(&ctx->pf_ssg, RK * ctx->ss_ld * 4) != DF_OK || dalloc(&ctx->pf_ug, RK * F * 2) != DF_OK ||
+        dalloc(&ctx->pf_yg, RK * d * 4) != DF_OK || dalloc(&ctx->pf_blk, ((RK + 255) / 256 + E) * sizeof(int4)) != DF_OK ||
+        dalloc(&ctx->pf_nblk, 4) != DF_OK) {
+      free_prefill_moe(ctx);
+      for (void* p : {(void*)ctx->pf_h, ctx->pf_x, ctx->pf_q, ctx->pf_o, ctx->pf_u, (void*)ctx->pf_ss})
+        if (p) cudaFree(p);
+      ctx->pf_h = nullptr;
+      ctx->pf_x = ctx->pf_q = ctx->pf_o = ctx->pf_u = nullptr;
+      ctx->pf_ss = nullptr;
+      return DF_ERR_OOM;
+    }
+  }
   ctx->pf_rows = max_rows;
   return DF_OK;
 }
@@ -892,7 +995,7 @@ int dualflow_prefill_slots(dualflow_ctx* ctx, const dualflow_weights* w, const d
                            int32_t* free_pages, int32_t* n_free, dualflow_stream stream) {
   if (!ctx || !tokens) return DF_ERR_ARG;
   const dualflow_config& c = ctx->cfg;
-  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 0) return DF_ERR_UNSUPPORTED;
+  if (c.dtype != DF_DTYPE_BF16 || c.n_experts > 32) return DF_ERR_UNSUPPORTED;
   const int G = c.n_q_heads / c.n_kv_heads;
   if (G != 1 && G != 2 && G != 4) return DF_ERR_UNSUPPORTED;
   if ((free_pages == nullptr) != (n_free == nullptr)) return DF_ERR_ARG;
@@ -984,6 +1087,11 @@ int dualflow_prefill_slots(dualflow_ctx* ctx, const dualflow_weights* w, const d
     norm_output(o, w->g_mlp[l]);
     DF_TRY(launch_gemm_tc(ctx, o, s));
     ss_parts = d_tiles;
+    if (c.n_experts > 0) {
+      DF_TRY(prefill_moe(ctx, w, l, R, ss_parts, s));
+      ss_parts = (c.d_model + 511) / 512;
+      continue;
+    }
     GemmArgs gu = gemm_args(ctx);
     gu.x = ctx->x;
     gu.W = w->Wgu[l];

@@ -13,7 +13,9 @@
 // heads of group g at 64 / G consecutive positions, so every K/V tile it loads serves all of
 // them. Four warps each own 16 query rows (one head, 16 positions): S = Q K^T and O += P V with
 // mma.sync m16n8k16 (queries as M), online softmax per row in the log2 domain, the causal bound
-// applied to the tiles that cross it. K/V tiles of 64 keys are double-buffered in shared memory by
+// applied to the tiles that cross it. P enters P V as a bf16 pair hi + lo (lo = the rounding
+// residual of hi, two MMAs), so the probabilities keep ~16 significant bits, as in the decode
+// attention. K/V tiles of 64 keys are double-buffered in shared memory by
 // cp.async, rows XOR-swizzled in 16-byte chunks so that ldmatrix reads are conflict-free.
 #include "internal.h"
 #include "ptx.cuh"
@@ -169,15 +171,19 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const PrefillA
     const float base0 = (n0 == NEG_INF) ? 0.f : n0, base1 = (n1 == NEG_INF) ? 0.f : n1;
     const float c0 = exp2f(m0 - base0), c1 = exp2f(m1 - base1);
     float sum0 = 0.f, sum1 = 0.f;
-    uint32_t pa[4][4];  // P as A fragments for the 4 k-steps of 16 keys
+    uint32_t pa[4][4], pl[4][4];  // P (hi, lo) as A fragments for the 4 k-steps of 16 keys
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
       const float e0 = exp2f(s[nt][0] - base0), e1 = exp2f(s[nt][1] - base0);
       const float e2 = exp2f(s[nt][2] - base1), e3 = exp2f(s[nt][3] - base1);
       sum0 += e0 + e1;
       sum1 += e2 + e3;
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(e0, e1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(e2, e3);
+      const __nv_bfloat162 h01 = __floats2bfloat162_rn(e0, e1), h23 = __floats2bfloat162_rn(e2, e3);
+      const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+      pa[nt >> 1][(nt & 1) * 2 + 0] = *reinterpret_cast<const uint32_t*>(&h01);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = *reinterpret_cast<const uint32_t*>(&h23);
+      pl[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(e0 - f01.x, e1 - f01.y);
+      pl[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(e2 - f23.x, e3 - f23.y);
     }
     l0 = l0 * c0 + sum0;
     l1 = l1 * c1 + sum1;
@@ -201,6 +207,8 @@ __global__ void __launch_bounds__(kPfThreads) attn_prefill_kernel(const PrefillA
         // A fragment: a0 (row, keys 16ks + 2(l%4)), a1 (row + 8), a2 (row, +8 keys), a3 (row + 8, +8)
         mma_bf16_16816(o[2 * dp], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b0, b1);
         mma_bf16_16816(o[2 * dp + 1], pa[ks][0], pa[ks][1], pa[ks][2], pa[ks][3], b2, b3);
+        mma_bf16_16816(o[2 * dp], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pl[ks][0], pl[ks][1], pl[ks][2], pl[ks][3], b2, b3);
       }
     }
     __syncthreads();  // stage st is refilled by the next iteration's loads

@@ -233,12 +233,23 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     rblk = g0 + w_ % in_g;
     tile = w_ / in_g;
   }
-  const int split = p.row_blocks > 1 ? 0 : blockIdx.y, grp = blockIdx.z;
-  const int rbase = rblk * kGemmMaxAct;  // first activation row of this CTA
+  const int split = p.row_blocks > 1 ? 0 : blockIdx.y;
+  int grp = blockIdx.z;
+  int rbase = rblk * kGemmMaxAct;  // first activation row of this CTA
+  int rows_left = p.a.m_p - rbase;
+  if (a.blk_info != nullptr) {
+    // gathered expert rows: this row block is one expert's rows (the grid is sized for the most
+    // blocks the routing can produce; the ones beyond it leave before any setup)
+    if (rblk >= *a.n_blk) return;
+    const int4 bi = a.blk_info[rblk];
+    grp = bi.x;
+    rbase = bi.y;
+    rows_left = bi.z;
+  }
   if (p.row_blocks > 1) {
     // this CTA's block of rows: the epilogue's row-indexed operands start at its first row
     const size_t ye = (EPI == EPI_STORE_BF16 || EPI == EPI_SWIGLU) ? 2 : 4;
-    a.m_p = min(kGemmMaxAct, p.a.m_p - rbase);
+    a.m_p = min(kGemmMaxAct, rows_left);
     a.row_base = rbase;
     if (a.y) a.y = static_cast<uint8_t*>(a.y) + (size_t)rbase * a.ldy * ye;
     if (a.x_next) a.x_next = static_cast<__nv_bfloat16*>(a.x_next) + (size_t)rbase * a.n_out;
@@ -675,7 +686,8 @@ int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& 
   if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
     return DF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.n_tiles, p.row_blocks > 1 ? p.row_blocks : p.splits, p.a.n_groups > 0 ? p.a.n_groups : 1);
+  cfg.gridDim = dim3(p.n_tiles, p.row_blocks > 1 ? p.row_blocks : p.splits,
+                     (p.a.n_groups > 0 && !p.a.blk_info) ? p.a.n_groups : 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -740,8 +752,12 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   const int m = a.m_p + a.m_a;
   if (m <= 0) return DF_OK;
   if (a.k % kGemmTileK != 0 || a.k <= 0) return DF_ERR_SHAPE;
+  if (a.blk_info && !a.row_blocked) return DF_ERR_ARG;
   if (a.row_blocked) {
-    if (a.m_a != 0 || a.n_groups > 0 || a.seq_rows <= 0) return DF_ERR_ARG;
+    // grouped row-blocked launches take their rows gathered per group
+    if (a.m_a != 0 || (a.n_groups > 0) != (a.blk_info != nullptr) || !(a.blk_info == nullptr || a.n_blk) ||
+        a.seq_rows <= 0)
+      return DF_ERR_ARG;
   } else if (m > kGemmMaxAct || m > 2 * ctx->cfg.max_batch) {
     return DF_ERR_SHAPE;
   }
@@ -753,7 +769,8 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   GemmParams p;
   p.a = a;
   p.n_pad = m >= kGemmMaxAct ? kGemmMaxAct : ((m + 15) / 16) * 16;
-  p.row_blocks = a.row_blocked ? (m + kGemmMaxAct - 1) / kGemmMaxAct : 1;
+  // gathered rows: every group's last block may be partial, so at most one block more per group
+  p.row_blocks = a.row_blocked ? (m + kGemmMaxAct - 1) / kGemmMaxAct + (a.blk_info ? groups : 0) : 1;
   p.kb_total = a.k / kGemmTileK;
   p.n_tiles = gemm_tiles(a.n_out, a.epi);
   p.splits = a.row_blocked ? 1 : gemm_splits(ctx, a.n_out, a.k, a.epi, groups);

@@ -91,6 +91,11 @@ struct GemmArgs {
   int row_blocked, seq_rows, row_base;
   const int32_t* slots;
   int max_batch;
+  // Gathered expert rows (row-blocked grouped launch, prefill MoE): row block g of the grid is
+  // expert blk_info[g].x's rows [blk_info[g].y, + blk_info[g].z) of x / y / ss_in; blocks g >=
+  // *n_blk do nothing. m_p is the capacity in rows (the x tensor map's extent).
+  const int4* blk_info;
+  const int32_t* n_blk;
 };
 
 struct AttnArgs {
@@ -152,6 +157,18 @@ struct dualflow_ctx {
   void* pf_o = nullptr;            // [pf_rows][Hq * D] bf16
   void* pf_u = nullptr;            // [pf_rows][F] bf16
   float* pf_ss = nullptr;          // [pf_rows][ss_ld]
+  // prefill MoE (pf_rows rows R, k = topk_primary): routing, the rows gathered per expert
+  float* pf_rlog = nullptr;        // [R][E] router logits
+  int32_t* pf_sel_pos = nullptr;   // [R][E] position of e in the row's expert set, -1 if unused
+  float* pf_sel_w = nullptr;       // [R][E]
+  int32_t* pf_perm = nullptr;      // [R k] source row of gathered row q (expert-major, rows in order)
+  int32_t* pf_pos = nullptr;       // [R][k] gathered row of the row's j-th expert
+  void* pf_xg = nullptr;           // [R k][d] bf16 gathered norm operand
+  float* pf_ssg = nullptr;         // [R k][ss_ld] gathered sums of squares
+  void* pf_ug = nullptr;           // [R k][F] bf16 expert intermediates
+  float* pf_yg = nullptr;          // [R k][d] expert outputs
+  int4* pf_blk = nullptr;          // [R k / 256 + E] row blocks of the gathered rows
+  int32_t* pf_nblk = nullptr;      // [1]
   float* gemm_part = nullptr;      // split-K partials exchanged through L2 (gemm_part_floats)
   size_t gemm_part_floats = 0;
   int32_t* gen_tokens = nullptr;   // [max_batch] input tokens of the generation loop's next step
@@ -203,6 +220,15 @@ int launch_norm_prep(dualflow_ctx* ctx, float* h, const void* g, int batch, int 
 // ceil(d / 512) partial sums of squares per row).
 int launch_moe_route(dualflow_ctx* ctx, const float* rlog, int batch, int aux_on, int32_t* ids, cudaStream_t s,
                      int pdl);
+int launch_moe_plan(const dualflow_config& c, int R, const int32_t* sel_pos, int32_t* perm, int32_t* pos, int4* blk,
+                    int32_t* n_blk, int32_t* status, cudaStream_t s);
+int launch_moe_gather(int rows, int R, int d, const void* x, const float* ss, int ss_ld, const int32_t* perm, void* xg,
+                      float* ssg, int32_t* status, cudaStream_t s);
+int launch_moe_combine_rows(const dualflow_config& c, int R, const float* yg, const int32_t* sel_pos,
+                            const float* sel_w, const int32_t* pos, float* h, const void* g_next, void* x_next,
+                            float* ss, int ss_ld, int32_t* status, cudaStream_t s);
+int launch_moe_route_rows(const dualflow_config& c, const float* rlog, int R, int32_t* sel_pos, float* sel_w,
+                          cudaStream_t s);
 int launch_moe_combine(dualflow_ctx* ctx, float* h, int batch, int aux_on, const void* c_vec, const void* g_next,
                        cudaStream_t s, int pdl);
 int launch_mixture_head(const float* logits, int batch, int vocab, const float* u, float* alpha, float* p_mix,

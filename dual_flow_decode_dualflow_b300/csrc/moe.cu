@@ -172,7 +172,195 @@ __global__ void moe_combine_kernel(const float* Y, int mrows, int d, int B, int 
   (void)status;
 }
 
+// ---- prefill (primary flow only, many rows): the rows each expert serves, gathered contiguously --
+
+// One CTA per expert e (1024 threads). Counts every expert's rows, then lays the experts' row lists
+// end to end in expert order (rows in row order within an expert): perm[q] = source row of gathered
+// row q, pos[r * k + j] = gathered row of row r's j-th expert; expert e's rows are cut into blocks
+// of 256 for the expert GEMMs, blk[g] = (expert, first gathered row, rows), n_blk = number of blocks.
+__global__ void __launch_bounds__(1024) moe_plan_kernel(int R, int E, int k, const int32_t* sel_pos, int32_t* perm,
+                                                        int32_t* pos, int4* blk, int32_t* n_blk, int32_t* status) {
+  __shared__ int cnt[32];
+  __shared__ int wsum[32];
+  __shared__ int off_s, base_s, chunk_s;
+  const int e = blockIdx.x, t = threadIdx.x, lane = t & 31, wid = t >> 5;
+  if (t < 32) cnt[t] = 0;
+  __syncthreads();
+  for (int r0 = 0; r0 < R; r0 += 1024) {
+    const int r = r0 + t;
+    for (int j = 0; j < E; ++j) {
+      const bool f = r < R && sel_pos[(size_t)r * E + j] >= 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, f);
+      if (lane == 0 && bal) atomicAdd(&cnt[j], __popc(bal));
+    }
+  }
+  __syncthreads();
+  if (t == 0) {
+    int off = 0, b0 = 0;
+    for (int j = 0; j < e; ++j) {
+      off += cnt[j];
+      b0 += (cnt[j] + 255) / 256;
+    }
+    const int nb = (cnt[e] + 255) / 256, cap_blk = (R * k + 255) / 256 + E;
+    for (int i = 0; i < nb; ++i)
+      if (b0 + i < cap_blk) blk[b0 + i] = make_int4(e, off + 256 * i, min(256, cnt[e] - 256 * i), 0);
+    if (e == E - 1) *n_blk = min(b0 + nb, cap_blk);
+    if (off + cnt[e] > R * k) atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);  // more selections than k per row
+    off_s = off;
+    base_s = 0;
+  }
+  __syncthreads();
+  for (int r0 = 0; r0 < R; r0 += 1024) {
+    const int r = r0 + t;
+    const int sp = r < R ? sel_pos[(size_t)r * E + e] : -1;
+    const bool f = sp >= 0;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) wsum[wid] = __popc(bal);
+    __syncthreads();
+    if (t < 32) {  // exclusive prefix of the warps' counts
+      const int v = wsum[t];
+      int incl = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (t >= o) incl += u;
+      }
+      wsum[t] = incl - v;
+      if (t == 31) chunk_s = incl;
+    }
+    __syncthreads();
+    if (f) {
+      const int q = off_s + base_s + wsum[wid] + __popc(bal & ((1u << lane) - 1u));
+      if (q < R * k && sp < k) {
+        perm[q] = r;
+        pos[(size_t)r * k + sp] = q;
+      } else {
+        atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+      }
+    }
+    __syncthreads();
+    if (t == 0) base_s += chunk_s;
+    __syncthreads();
+  }
+}
+
+// One warp per gathered row q: the source row's norm operand (bf16, d) and its sums of squares.
+__global__ void moe_gather_kernel(int rows, int R, int d, const __nv_bfloat16* x, const float* ss, int ss_ld,
+                                  const int32_t* perm, __nv_bfloat16* xg, float* ssg, int32_t* status) {
+  const int q = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (q >= rows) return;
+  const int r = perm[q];
+  uint4* dst = reinterpret_cast<uint4*>(xg + (size_t)q * d);
+  if (r < 0 || r >= R) {  // a row list that does not cover every gathered row: zeros, and the error
+    for (int i = lane; i < d / 8; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)r * d);
+  for (int i = lane; i < d / 8; i += 32) dst[i] = src[i];
+  for (int i = lane; i < ss_ld; i += 32) ssg[(size_t)q * ss_ld + i] = ss[(size_t)r * ss_ld + i];
+}
+
+// grid (R, ceil(d / 512)), 128 threads, 4 features each: row r's experts' outputs (gathered rows
+// pos[r][j]) mixed in set order, y = sum_j w_j Y[pos[r][j]], h[r] += y; with g_next the next norm's
+// operand x_next = bf16(h (*) g_next) and ss[r * ss_ld + chunk] = sum of h^2 over the chunk. The
+// same arithmetic, in the same order, as the decode step's combine for the primary flow.
+__global__ void moe_combine_rows_kernel(const float* yg, int R, int d, int E, int k, const int32_t* sel_pos,
+                                        const float* sel_w, const int32_t* pos, float* h,
+                                        const __nv_bfloat16* g_next, __nv_bfloat16* x_next, float* ss, int ss_ld,
+                                        int32_t* status) {
+  __shared__ int qrow[32];
+  __shared__ float wts[32];
+  __shared__ int nsel;
+  __shared__ float red[4];
+  const int r = blockIdx.x, chunk = blockIdx.y, t = threadIdx.x;
+  if (t < 32) {
+    if (t == 0) nsel = 0;
+    __syncwarp();
+    if (t < E) {
+      const int p = sel_pos[(size_t)r * E + t];
+      if (p >= 0 && p < k) {
+        const int q = pos[(size_t)r * k + p];
+        if (q < 0 || q >= R * k) {
+          atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+        } else {
+          qrow[p] = q;
+          wts[p] = sel_w[(size_t)r * E + t];
+          atomicAdd(&nsel, 1);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int i = chunk * 512 + 4 * t;
+  const bool live = i < d;  // d is a multiple of 4
+  float s = 0.f;
+  if (live) {
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < nsel; ++j) {
+      const float w = wts[j];
+      const float4 v = *reinterpret_cast<const float4*>(yg + (size_t)qrow[j] * d + i);
+      y = make_float4(__fmaf_rn(w, v.x, y.x), __fmaf_rn(w, v.y, y.y), __fmaf_rn(w, v.z, y.z), __fmaf_rn(w, v.w, y.w));
+    }
+    float4* hp = reinterpret_cast<float4*>(h + (size_t)r * d + i);
+    float4 hv = *hp;
+    hv = make_float4(__fadd_rn(hv.x, y.x), __fadd_rn(hv.y, y.y), __fadd_rn(hv.z, y.z), __fadd_rn(hv.w, y.w));
+    *hp = hv;
+    if (g_next) {
+      const uint2 gu = *reinterpret_cast<const uint2*>(g_next + i);
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gu.x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gu.y));
+      __nv_bfloat162 a = __floats2bfloat162_rn(__fmul_rn(hv.x, g01.x), __fmul_rn(hv.y, g01.y));
+      __nv_bfloat162 bb = __floats2bfloat162_rn(__fmul_rn(hv.z, g23.x), __fmul_rn(hv.w, g23.y));
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&a);
+      u.y = *reinterpret_cast<uint32_t*>(&bb);
+      *reinterpret_cast<uint2*>(x_next + (size_t)r * d + i) = u;
+      s = __fmaf_rn(hv.w, hv.w, __fmaf_rn(hv.z, hv.z, __fmaf_rn(hv.y, hv.y, __fmul_rn(hv.x, hv.x))));
+    }
+  }
+  if (g_next) {
+    const int w = t >> 5, lane = t & 31;
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) red[w] = s;
+    __syncthreads();
+    if (t == 0) ss[(size_t)r * ss_ld + chunk] = ((red[0] + red[1]) + red[2]) + red[3];
+  }
+}
+
 }  // namespace
+
+int launch_moe_route_rows(const dualflow_config& c, const float* rlog, int R, int32_t* sel_pos, float* sel_w,
+                          cudaStream_t s) {
+  const int kmax = c.topk_primary > c.topk_aux ? c.topk_primary : c.topk_aux;
+  moe_route_kernel<<<(R + 3) / 4, 128, 0, s>>>(rlog, R, c.n_experts, c.topk_primary, c.topk_aux, 0, sel_pos, sel_w,
+                                               nullptr, kmax);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_moe_plan(const dualflow_config& c, int R, const int32_t* sel_pos, int32_t* perm, int32_t* pos, int4* blk,
+                    int32_t* n_blk, int32_t* status, cudaStream_t s) {
+  if (c.n_experts > 32) return DF_ERR_UNSUPPORTED;
+  moe_plan_kernel<<<c.n_experts, 1024, 0, s>>>(R, c.n_experts, c.topk_primary, sel_pos, perm, pos, blk, n_blk,
+                                               status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_moe_gather(int rows, int R, int d, const void* x, const float* ss, int ss_ld, const int32_t* perm, void* xg,
+                      float* ssg, int32_t* status, cudaStream_t s) {
+  if (d % 8 != 0) return DF_ERR_SHAPE;
+  moe_gather_kernel<<<(rows + 3) / 4, 128, 0, s>>>(rows, R, d, static_cast<const __nv_bfloat16*>(x), ss, ss_ld, perm,
+                                                   static_cast<__nv_bfloat16*>(xg), ssg, status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
+
+int launch_moe_combine_rows(const dualflow_config& c, int R, const float* yg, const int32_t* sel_pos,
+                            const float* sel_w, const int32_t* pos, float* h, const void* g_next, void* x_next,
+                            float* ss, int ss_ld, int32_t* status, cudaStream_t s) {
+  moe_combine_rows_kernel<<<dim3(R, (c.d_model + 511) / 512, 1), 128, 0, s>>>(
+      yg, R, c.d_model, c.n_experts, c.topk_primary, sel_pos, sel_w, pos, h,
+      static_cast<const __nv_bfloat16*>(g_next), static_cast<__nv_bfloat16*>(x_next), ss, ss_ld, status);
+  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+}
 
 int launch_moe_route(dualflow_ctx* ctx, const float* rlog, int batch, int aux_on, int32_t* ids, cudaStream_t s,
                      int pdl) {

@@ -232,9 +232,11 @@ DF_API int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const
                              int32_t* n_free, int32_t aux_on, dualflow_stream stream);
 
 /* Workspace for dualflow_prefill / dualflow_prefill_slots: room for max_rows = prompt sequences *
- * prompt tokens activation rows (about (4 d + 4 Hq D + 2 F + 4 ss) bytes per row). Allocates (cold
- * call, not for a hot loop); a smaller request than the current room does nothing. bf16 dense
- * contexts only (DF_ERR_UNSUPPORTED otherwise); DF_ERR_OOM leaves no prefill room. */
+ * prompt tokens activation rows (about (4 d + 4 Hq D + 2 F + 4 ss) bytes per row; a MoE context
+ * adds about k (8 d + 2 F + 4 ss + 8) + 12 E bytes per row, k = topk_primary). Allocates (cold
+ * call, not for a hot loop); a smaller request than the current room does nothing. bf16 contexts,
+ * dense or MoE with at most 32 experts (DF_ERR_UNSUPPORTED otherwise); DF_ERR_OOM leaves no
+ * prefill room. */
 DF_API int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows);
 
 /* Primary-only prefill ("Custos de Inferencia vs. Treinamento", gist.science technical summary: the
@@ -244,9 +246,11 @@ DF_API int dualflow_prefill_reserve(dualflow_ctx* ctx, int32_t max_rows);
  * the keys/values of every prompt position are written into the cache, and each position attends
  * the cached positions 0 .. itself (causal). Then seq_len[b] += n_tok (device). No logits: the
  * caller runs the prompt's last token as the first decode step (dualflow_step / dualflow_generate),
- * where the auxiliary flow joins. Needs dualflow_prefill_reserve(ctx, >= batch * n_tok)
- * (DF_ERR_SHAPE otherwise); bf16 dense contexts with G = Hq / Hkv in {1, 2, 4}
- * (DF_ERR_UNSUPPORTED otherwise). A position seq_len[b] + t >= max_ctx latches
+ * where the auxiliary flow joins. A MoE layer routes every prompt row (top-k of its router
+ * logits, the decode step's rule for the primary flow), gathers each expert's rows and runs that
+ * expert's projections on them only. Needs dualflow_prefill_reserve(ctx, >= batch * n_tok)
+ * (DF_ERR_SHAPE otherwise); bf16 contexts (dense, or MoE with at most 32 experts) with
+ * G = Hq / Hkv in {1, 2, 4} (DF_ERR_UNSUPPORTED otherwise). A position seq_len[b] + t >= max_ctx latches
  * DF_ERR_DEVICE_BOUNDS; so does, with a paged cache, a prompt position whose page the table does
  * not map (this call takes no free list: see dualflow_prefill_slots). Asynchronous on `stream`,
  * launched eagerly (no graph). Same as dualflow_prefill_slots(ctx, w, kv, tokens, NULL, batch,

@@ -482,19 +482,22 @@ def prefill(hp: HParams, glob: dict, layers: Sequence[dict], caches: Sequence, p
             seq_len: np.ndarray, mirror: bool = True) -> dict:
     """Primary-only prefill (R13) of prompt [B, n]: token t of sequence b sits at position
     seq_len[b] + t; its key/value enter the cache there (caches written in place). Returns the
-    primary logits of every position [B, n, V] and the final seq_len."""
+    primary logits of every position [B, n, V], the final seq_len and, for MoE, the primary
+    router logits of every position [n_layers, B, n, E]."""
     prompt = np.asarray(prompt, dtype=np.int64)
     B, n = prompt.shape
     L = np.array(seq_len, dtype=np.int64)
     logits = np.zeros((B, n, hp.vocab))
+    rlog = np.full((len(layers), B, n, max(hp.n_experts, 1)), np.nan)
     for t in range(n):
         r = decode_step(hp, glob, layers, caches, prompt[:, t], L, aux_on=False, mirror=mirror)
         logits[:, t] = r["logits"][0]
+        rlog[:, :, t] = r["router_logits"][:, 0]
         for layer in range(len(layers)):
             for b in range(B):
                 append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])
         L = L + 1
-    return dict(logits=logits, seq_len=L)
+    return dict(logits=logits, seq_len=L, rlog=rlog)
 
 
 def sample_inverse_cdf(p: np.ndarray, u: float) -> int:
