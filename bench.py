@@ -85,7 +85,8 @@ def load_peaks() -> tuple[float, str]:
 def workload(name: str = "dense"):
     from dfsynth import workloads as W
     return {"dense": W.DENSE_24L_B32_L4096, "moe": W.MOE_16L_B64, "attn": W.ATTN_B8_L2048,
-            "paged": W.PAGED_RAGGED_B64, "prefill": W.DENSE_24L_B32_L4096, "dense_paged": W.DENSE_PAGED_RAGGED_B32}[name]
+            "paged": W.PAGED_RAGGED_B64, "prefill": W.DENSE_24L_B32_L4096, "dense_paged": W.DENSE_PAGED_RAGGED_B32,
+            "prefill_moe": W.MOE_16L_B64}[name]
 
 
 PREFILL_TOKENS = 512  # prompt tokens per sequence of the prefill workload (from an empty cache)
@@ -93,10 +94,14 @@ PREFILL_TOKENS = 512  # prompt tokens per sequence of the prefill workload (from
 
 def prefill_flops(w, n_tok: int) -> float:
     """Algorithmic FLOPs of the primary-only prefill of n_tok tokens per sequence from position 0:
-    2 per weight element per row for the four projections of every layer, and the causal attention
-    (2 x 2 x D per head per (query, attended key) pair)."""
+    2 per weight element per row for the projections of every layer (a MoE layer: the router and
+    the topk_primary experts each row chose), and the causal attention (2 x 2 x D per head per
+    (query, attended key) pair)."""
     qkv = (w.n_q_heads + 2 * w.n_kv_heads) * w.head_dim * w.d_model
-    layer = qkv + w.d_model * w.n_q_heads * w.head_dim + 3 * w.ffn_hidden * w.d_model
+    mlp = 3 * w.ffn_hidden * w.d_model
+    if w.n_experts > 0:
+        mlp = w.n_experts * w.d_model + w.topk_primary * mlp
+    layer = qkv + w.d_model * w.n_q_heads * w.head_dim + mlp
     rows = w.batch * n_tok
     pairs = w.batch * n_tok * (n_tok + 1) / 2
     return w.n_layers * (2.0 * layer * rows + 4.0 * w.head_dim * w.n_q_heads * pairs)
@@ -343,7 +348,7 @@ def run_reference(args, w) -> dict:
     rotating through the batch, over the first layer and the LM head; for an attention-only
     workload, one sequence's attention call)."""
     per = []
-    if args.workload == "prefill":
+    if args.workload in ("prefill", "prefill_moe"):
         samp = PrefillOracleSample(w, 8, PREFILL_TOKENS)
         for i in range(args.warmup + args.steps):
             t = samp.time()
@@ -509,7 +514,7 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
 
 def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     """Primary-only prefill of PREFILL_TOKENS tokens per sequence from an empty cache, on the dense
-    model (the positions are rewritten by every repetition)."""
+    or the MoE model (the positions are rewritten by every repetition)."""
     import torch
 
     import dual_flow_decode_dualflow_b300 as dfl
@@ -570,6 +575,7 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
     if rank != 0:
         return None
     flops = prefill_flops(w, n_tok)
+    launches = 1 + (10 if w.n_experts else 5) * w.n_layers + 1  # embedding + layers + length advance
     peak = None
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -589,7 +595,9 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
                    "batch_per_gpu": w.batch, "prompt_tokens": n_tok, "rows": w.batch * n_tok,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "compute-bound; weights re-read per 256-row block, no flush"},
-        "roofline": {"kernel": "whole prefill pass (24 x {QKV, causal attention, O, gate/up, down})",
+        "roofline": {"kernel": f"whole prefill pass ({w.n_layers} x {{QKV, causal attention, O, "
+                               + ("router, routing, gather, expert gate/up, expert down, combine})" if w.n_experts
+                                  else "gate/up, down})"),
                      "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_kind": kind, "flops_per_step": flops, "traffic": None},
         "cpu_baseline": {"value": w.batch * n_tok / cpu_s, "unit": "prefill tokens/s", "cores": blas_threads(),
@@ -597,7 +605,7 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
         "e2e": {"value": reps.rate(w.batch * n_tok, e2e_s), "unit": "prefill tokens/s", "h2d_bytes_per_step": int(prompt_np.nbytes),
                 "d2h_bytes_per_step": 0,
                 "api": "dualflow_prefill with the prompt copied from pinned host memory, stream sync per call"},
-        "gpu_launches": steps * (1 + 5 * w.n_layers + 1), "launches_per_step": 1 + 5 * w.n_layers + 1,
+        "gpu_launches": steps * launches, "launches_per_step": launches,
         "clocks": sampler.summary(),
     }
 
@@ -853,7 +861,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling captures only: run the workload with this many layers")
     ap.add_argument("--quick", action="store_true", help="profiling captures only: time the step, skip the rest")
-    ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged", "prefill", "dense_paged"], default="dense")
+    ap.add_argument("--workload", choices=["dense", "moe", "attn", "paged", "prefill", "prefill_moe", "dense_paged"],
+                    default="dense")
     ap.add_argument("--sweep-topk-aux", default="",
                     help="MoE only: comma-separated auxiliary fan-outs to time as well (cost side of the decode budget)")
     args = ap.parse_args()
@@ -871,7 +880,7 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    if args.workload == "prefill":
+    if args.workload in ("prefill", "prefill_moe"):
         res = run_ours_prefill(args, w, rank, world, local_rank)
     elif w.kind == "attention":
         res = run_ours_attention(args, w, rank, world, local_rank)
