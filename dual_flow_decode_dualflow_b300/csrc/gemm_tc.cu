@@ -42,7 +42,6 @@ namespace {
 constexpr int kStages = 4;                 // most pipeline stages (barrier arrays are sized for it)
 constexpr int kStageBudget = 96 * 1024;    // stage bytes that still let two CTAs share an SM
 constexpr int kStageBudget3 = 68 * 1024;   // ... three CTAs
-constexpr int kStageBudgetRows = 192 * 1024;  // ... one CTA (row-blocked launches)
 constexpr int kRowGroup = 8;               // row blocks per L2-resident group (row-blocked launches)
 constexpr int kThreads = 128;
 constexpr int kABytes = kGemmTileN * kGemmTileK * 2;  // 16 KB weight tile per stage
@@ -59,6 +58,7 @@ struct GemmParams {
   int region;    // bytes of the data region (pipeline stages, later the partial tiles)
   int row_blocks;  // > 1: grid y runs over blocks of 256 activation rows (splits == 1)
   float* part;     // S > 1: the split-K exchange area, [CTA of the launch][S slices][n_pad][2 nl]
+  int chunk;       // S == 1: accumulator rows drained to shared memory per epilogue pass
   int32_t* status;
 };
 
@@ -203,7 +203,9 @@ __device__ __forceinline__ void store4(const GemmArgs& a, int vec_ok, int n, int
 template <int EPI>
 constexpr int min_ctas_per_sm() { return (EPI == EPI_MOE_GATEUP || EPI == EPI_MOE_DOWN) ? 3 : 2; }
 
-template <int EPI>
+// RB: the row-blocked (prefill) instantiation, whose accumulator may be drained in passes; the
+// others drain it in one pass, with that loop resolved at compile time.
+template <int EPI, bool RB>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_pf, const GemmParams p) {
@@ -396,10 +398,27 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
   const int hf = tf & 63, dst_rank = hf / nl;  // split-K: the rank that owns feature tf
   const int fl = (tf >> 6) * nl + hf % nl;     // and its index there
-  float* dst = acc_s + tf;  // S == 1: acc[n][128]
+  float* dst = acc_s + tf;  // S == 1: acc[n][128 - row offset of the pass]
   float* gdst = S > 1 ? p.part + (tile_cta0 + split) * cta_floats + (size_t)dst_rank * p.n_pad * nfs + fl : nullptr;
+  RedSrc red;
+  red.base = acc_s;
+  red.g = S > 1 ? p.part + tile_cta0 * cta_floats + slice_off : nullptr;
+  red.gstride = (int)cta_floats;
+  red.S = S;
+  red.nl = nl;
+  const bool scaled = a.ss_in != nullptr;
+  const bool norm_out = (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD) && a.g_next != nullptr;
+  // units of work: (activation row, quad); paired epilogues take the primary row and its auxiliary row
+  const bool paired = EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV || EPI == EPI_MOE_GATEUP;
+  const int rows = (EPI == EPI_Q2) ? a.m_a : paired ? a.m_p : m;
+  // S == 1 with a tile larger than the pipeline bytes (row-blocked launches on a small budget): the
+  // accumulator is drained and its epilogue run in passes of `chunk` rows (no auxiliary rows there)
+  const int chunk = (RB && S == 1 && p.chunk > 0) ? p.chunk : p.n_pad;
+  const int n_pass = RB ? (p.n_pad + chunk - 1) / chunk : 1;
+  for (int pass = 0; pass < n_pass; ++pass) {
+  const int cb = RB ? pass * chunk : 0;
   // four 16-column TMEM loads in flight per wait
-  for (int c0 = 0; c0 < p.n_pad; c0 += 64) {
+  for (int c0 = cb; c0 < cb + chunk && c0 < p.n_pad; c0 += 64) {
     uint32_t v[4][16];
     const int nblk = (p.n_pad - c0) >= 64 ? 4 : (p.n_pad - c0) / 16;
 #pragma unroll
@@ -418,33 +437,26 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
       for (int q = 0; q < 4; ++q)
         if (q < nblk)
 #pragma unroll
-          for (int j = 0; j < 16; ++j) dst[(c0 + 16 * q + j) * kGemmTileN] = __uint_as_float(v[q][j]);
+          for (int j = 0; j < 16; ++j) dst[(c0 - cb + 16 * q + j) * kGemmTileN] = __uint_as_float(v[q][j]);
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, ncols);
-  griddep_wait();  // the epilogue reads and writes buffers of the preceding kernels
-  if (S > 1) {
-    cluster_arrive();  // this CTA's partial is written (release: its global stores included)
-    cluster_wait();    // and so are the other ranks'
+  if (cb + chunk >= p.n_pad && warp == 1) tmem_dealloc(tmem, ncols);
+  if (cb == 0) {
+    griddep_wait();  // the epilogue reads and writes buffers of the preceding kernels
+    if (S > 1) {
+      cluster_arrive();  // this CTA's partial is written (release: its global stores included)
+      cluster_wait();    // and so are the other ranks'
+    }
   }
-  RedSrc red;
-  red.base = acc_s;
-  red.g = S > 1 ? p.part + tile_cta0 * cta_floats + slice_off : nullptr;
-  red.gstride = (int)cta_floats;
-  red.S = S;
-  red.nl = nl;
-  const bool scaled = a.ss_in != nullptr;
-  const bool norm_out = (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD) && a.g_next != nullptr;
-  // units of work: (activation row, quad); paired epilogues take the primary row and its auxiliary row
-  const bool paired = EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV || EPI == EPI_MOE_GATEUP;
-  const int rows = (EPI == EPI_Q2) ? a.m_a : paired ? a.m_p : m;
-  const int units = rows * nq;
+  red.base = acc_s - (size_t)cb * kGemmTileN;  // row n of this pass at acc_s[(n - cb) * 128]
+  const int r_end = min(cb + chunk, rows);
+  const int units = r_end > cb ? (r_end - cb) * nq : 0;
   for (int base = 0; base < units; base += kThreads) {
     const int it = base + threadIdx.x;
     const bool live = it < units;
-    const int n = live ? it / nq : 0, qd = it % nq;
+    const int n = live ? cb + it / nq : 0, qd = it % nq;
     const int fa = lo0 + 4 * qd;        // tile feature of the low quad
     const int fg = tile * kGemmTileN + fa;
     float ss0 = 0.f, ss1 = 0.f;         // norm outputs: sum of h^2 of row n (and its auxiliary row)
@@ -675,12 +687,14 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
       }
     }
   }
+  if (cb + chunk < p.n_pad) __syncthreads();  // the next pass overwrites the drained rows
+  }
 }
 
-template <int EPI>
+template <int EPI, bool RB = false>
 int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& mpf, const GemmParams& p, size_t smem,
                cudaStream_t s) {
-  auto kern = gemm_tc_kernel<EPI>;
+  auto kern = gemm_tc_kernel<EPI, RB>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return DF_ERR_CUDA;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
@@ -802,9 +816,9 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   const bool grouped_epi = a.epi == EPI_MOE_GATEUP || a.epi == EPI_MOE_DOWN;  // built for three per SM
   const bool three = grouped_epi && ctas > 2 * ctx->num_sms && ctas <= 3 * ctx->num_sms && 3 * tcols <= 512 &&
                      2 * (kABytes + p.n_pad * 128) <= kStageBudget3 && 512 * p.n_pad <= kStageBudget3;
-  // row-blocked (prefill) launches hold a 128 KB accumulator tile: one CTA per SM, so the pipeline
-  // takes the room that leaves (the same bytes later hold the tile)
-  p.stages = (a.row_blocked ? kStageBudgetRows : three ? kStageBudget3 : kStageBudget) / (kABytes + p.n_pad * 128);
+  // row-blocked (prefill) launches take the two-CTA budget too: while one CTA drains its accumulator
+  // tile (in passes, through its pipeline bytes) the other streams its main loop
+  p.stages = (three ? kStageBudget3 : kStageBudget) / (kABytes + p.n_pad * 128);
   p.stages = p.stages > kStages ? kStages : (p.stages < 2 ? 2 : p.stages);
   const int pipe = p.stages * (kABytes + p.n_pad * 128);
   // split-K partials go to the exchange area (sized at init for the largest split launch)
@@ -814,9 +828,27 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
       return DF_ERR_UNSUPPORTED;
     p.part = ctx->gemm_part;
   }
-  const int parts = p.splits == 1 ? 512 * p.n_pad : 0;  // S == 1: the accumulator tile
+  // S == 1: the accumulator tile, drained in passes of as many 64-row groups as the pipeline bytes
+  // hold when the whole tile does not fit them
+  // (only the row-blocked instantiation drains in passes: every other launch holds the whole tile)
+  p.chunk = 0;
+  if (a.row_blocked && p.splits == 1 && 512 * p.n_pad > pipe) {
+    p.chunk = (pipe / (512 * 64)) * 64;
+    if (p.chunk < 64) return DF_ERR_UNSUPPORTED;
+  }
+  const int parts = p.splits == 1 ? 512 * (p.chunk > 0 ? p.chunk : p.n_pad) : 0;
   p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
   const size_t smem = 1024 + (size_t)p.region + 128 + kGemmMaxAct * 8;
+  if (a.row_blocked) {
+    switch (a.epi) {
+      case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, true>(mw, mx, mpf, p, smem, s);
+      case EPI_ADD_F32: return launch_epi<EPI_ADD_F32, true>(mw, mx, mpf, p, smem, s);
+      case EPI_COUPLE_ADD: return launch_epi<EPI_COUPLE_ADD, true>(mw, mx, mpf, p, smem, s);
+      case EPI_SWIGLU: return launch_epi<EPI_SWIGLU, true>(mw, mx, mpf, p, smem, s);
+      case EPI_PREFILL_QKV: return launch_epi<EPI_PREFILL_QKV, true>(mw, mx, mpf, p, smem, s);
+      default: return DF_ERR_UNSUPPORTED;
+    }
+  }
   switch (a.epi) {
     case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(mw, mx, mpf, p, smem, s);
     case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(mw, mx, mpf, p, smem, s);
@@ -827,7 +859,6 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
     case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(mw, mx, mpf, p, smem, s);
     case EPI_MOE_GATEUP: return launch_epi<EPI_MOE_GATEUP>(mw, mx, mpf, p, smem, s);
     case EPI_MOE_DOWN: return launch_epi<EPI_MOE_DOWN>(mw, mx, mpf, p, smem, s);
-    case EPI_PREFILL_QKV: return launch_epi<EPI_PREFILL_QKV>(mw, mx, mpf, p, smem, s);
     default: return DF_ERR_ARG;
   }
 }
