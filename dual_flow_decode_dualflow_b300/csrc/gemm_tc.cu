@@ -828,9 +828,9 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
       return DF_ERR_UNSUPPORTED;
     p.part = ctx->gemm_part;
   }
-  // S == 1: the accumulator tile, drained in passes of as many 64-row groups as the pipeline bytes
-  // hold when the whole tile does not fit them
-  // (only the row-blocked instantiation drains in passes: every other launch holds the whole tile)
+  // S == 1: the accumulator tile. The row-blocked instantiation drains it through the pipeline
+  // bytes in passes of as many 64-row groups as they hold when the whole tile does not fit; every
+  // other launch holds the whole tile after its main loop.
   p.chunk = 0;
   if (a.row_blocked && p.splits == 1 && 512 * p.n_pad > pipe) {
     p.chunk = (pipe / (512 * 64)) * 64;
