@@ -73,6 +73,14 @@ class Replicas:
         return self.world * units_per_rank / seconds
 
 
+def step_percentiles(times_ms) -> dict:
+    """p10 / p50 / p90 (nearest rank) of per-step times."""
+    t = sorted(float(x) for x in times_ms)
+    n = len(t)
+    pick = lambda q: t[min(n - 1, max(0, -(-q * n // 100) - 1))]  # noqa: E731  nearest-rank percentile
+    return {"n": n, "p10_ms": pick(10), "p50_ms": pick(50), "p90_ms": pick(90)}
+
+
 def load_peaks() -> tuple[float, str]:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -669,6 +677,21 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         return None
     ms_primary = timed(0, max(args.steps // 2, 3), 3)
 
+    # the distribution of single steps (an event between consecutive steps; outside the timed region)
+    dist_steps = None
+    try:
+        n_d = 50
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_d + 1)]
+        with torch.cuda.stream(stream):
+            evs[0].record(stream)
+            for i in range(n_d):
+                run.step(aux_on=1, stream=stream)
+                evs[i + 1].record(stream)
+        evs[-1].synchronize()
+        dist_steps = step_percentiles([evs[i].elapsed_time(evs[i + 1]) for i in range(n_d)])
+    except Exception as exc:  # the distribution is a report only: never lose the run over it
+        dist_steps = {"error": str(exc)[:200]}
+
     # per-kernel times inside the step (event pairs captured into the step's graph)
     dfl.dualflow_set_profiling(run.ctx, 1)
     fam_ms = [0.0] * dfl.DF_PROF_FAMILIES
@@ -772,6 +795,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
         "hbm": {"step_bytes": nb["total"], "achieved_gbs": step_gbs, "frac_of_8000": step_gbs / NOMINAL_HBM_GBS,
                 f"frac_of_{peak_kind}": step_gbs / peak},
         "primary_only": {"ms_per_step": ms_primary, "dual_over_primary": ms / ms_primary},
+        "step_distribution": dist_steps,
         "roofline": {"kernel": "attn_bf16_kernel (shared-KV decode attention)", "bound": "hbm",
                      "achieved": att_gbs, "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "bytes_per_launch": nb["attention_per_launch"],

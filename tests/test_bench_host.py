@@ -70,3 +70,12 @@ def test_replicas_single_process():
     assert reps.max(3.0, 1.5) == [3.0, 1.5]
     assert reps.rate(32, 0.002) == pytest.approx(16000.0)
     reps.barrier()  # a no-op without a process group
+
+
+def test_step_percentiles_nearest_rank():
+    t = list(range(1, 51))  # 1 .. 50 ms, shuffled below
+    import random
+    random.Random(3).shuffle(t)
+    got = bench.step_percentiles(t)
+    assert got == {"n": 50, "p10_ms": 5.0, "p50_ms": 25.0, "p90_ms": 45.0}
+    assert bench.step_percentiles([7.0]) == {"n": 1, "p10_ms": 7.0, "p50_ms": 7.0, "p90_ms": 7.0}
