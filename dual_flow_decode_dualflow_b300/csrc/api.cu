@@ -624,7 +624,7 @@ const char* dualflow_status_string(int st) {
     case DF_ERR_ARG: return "invalid argument";
     case DF_ERR_SHAPE: return "shape inconsistent with the config";
     case DF_ERR_DTYPE: return "unknown storage dtype";
-    case DF_ERR_UNSUPPORTED: return "configuration not supported by this build";
+    case DF_ERR_UNSUPPORTED: return "configuration not supported by this library";
     case DF_ERR_CUDA: return "CUDA runtime error";
     case DF_ERR_OOM: return "device allocation failed";
     case DF_ERR_DEVICE_BOUNDS: return "device-side bounds check failed (page id, token or cache slot)";

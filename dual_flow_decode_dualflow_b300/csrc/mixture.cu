@@ -2,7 +2,7 @@
 //
 // "Objetivo de Mistura" (gist.science technical summary, "Mecanismos Chave"): the next-token
 // distribution mixes both flows' predictions with a weight that grows with the primary flow's
-// confidence and never drops below one half. This build's reading: p_f = softmax(logits_f),
+// confidence and never drops below one half. The reading implemented here: p_f = softmax(logits_f),
 // alpha = 1/2 + 1/2 * sum_i p1_i^2 (the collision probability of p1 mapped to [1/2, 1]),
 // p_mix = alpha * p1 + (1 - alpha) * p2. The token is the argmax of p_mix (ties to the lower index)
 // or, given a uniform u in [0, 1), the smallest i whose cumulative p_mix exceeds u (inverse-transform

@@ -1,7 +1,7 @@
 // Mixture-of-experts MLP of the dual-flow decode step with router replay ("Replay de Roteador",
 // gist.science technical summary, "Mecanismos Chave"): the auxiliary flow reuses the experts the
 // primary router selects, with its own mixing weights; the two flows' expert fan-outs are set
-// independently ("Contribuicoes Principais", item 3). This build's reading: the primary takes the
+// independently ("Contribuicoes Principais", item 3). The reading implemented here: the primary takes the
 // top-k1 experts of its router logits r1 with softmax(r1) weights over them; the auxiliary flow takes
 // the top-k2 experts of the PRIMARY logits r1 (so its set contains the primary's when k2 >= k1) with
 // softmax weights from its own logits r2 over that set. Ties go to the lower expert index.

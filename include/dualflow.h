@@ -51,7 +51,7 @@ typedef enum {
   DF_ERR_ARG = 1,            /* null pointer, negative or zero size, bad flag */
   DF_ERR_SHAPE = 2,          /* sizes inconsistent with the config or beyond its max_* fields */
   DF_ERR_DTYPE = 3,          /* unknown storage dtype */
-  DF_ERR_UNSUPPORTED = 4,    /* a valid config this build has no kernel for (see dualflow_init) */
+  DF_ERR_UNSUPPORTED = 4,    /* a valid config this library has no kernel for (see dualflow_init) */
   DF_ERR_CUDA = 5,           /* a CUDA runtime call failed */
   DF_ERR_OOM = 6,            /* workspace allocation failed at init */
   DF_ERR_DEVICE_BOUNDS = 7,  /* device-side check failed: page id, token id or cache slot out of range */
