@@ -13,8 +13,10 @@
  *
  * Conventions for every call
  *  - Pointers named "device" are CUDA device addresses; all others are host addresses.
- *  - The caller owns every tensor (weights, cache, inputs, outputs). A context owns only its
- *    workspace, sized at dualflow_init from the config's max_* fields. Hot calls never allocate.
+ *  - The caller owns every tensor (weights, cache, page table, free list, inputs, outputs). A
+ *    context owns only its workspace, sized at dualflow_init from the config's max_* fields, plus
+ *    the prefill workspace that dualflow_prefill_reserve allocates (a cold call). Hot calls never
+ *    allocate.
  *  - Every compute call is asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and returns a dualflow_status. Argument and shape errors are detected on the host
  *    before any launch and leave every buffer untouched. Errors found on the device (an out-of-
@@ -53,7 +55,7 @@ typedef enum {
   DF_ERR_DTYPE = 3,          /* unknown storage dtype */
   DF_ERR_UNSUPPORTED = 4,    /* a valid config this library has no kernel for (see dualflow_init) */
   DF_ERR_CUDA = 5,           /* a CUDA runtime call failed */
-  DF_ERR_OOM = 6,            /* workspace allocation failed at init */
+  DF_ERR_OOM = 6,            /* workspace allocation failed (dualflow_init, dualflow_prefill_reserve) */
   DF_ERR_DEVICE_BOUNDS = 7,  /* device-side check failed: page id, token id or cache slot out of range */
   DF_ERR_TIMEOUT = 8         /* a bounded device wait expired; the kernel returned early */
 } dualflow_status;
@@ -122,7 +124,9 @@ typedef struct {
  *               physical page holding positions [j*page_size, (j+1)*page_size); -1 = unused
  *   seq_len     device int32 [batch]: positions cached BEFORE the call. A step writes the new
  *               primary key/value at slot seq_len[b] and both flows attend positions
- *               0..seq_len[b]; the caller advances seq_len afterwards. */
+ *               0..seq_len[b]; the caller advances seq_len afterwards (dualflow_generate and the
+ *               prefill calls advance it themselves). Calls that take cache slots
+ *               (dualflow_prefill_slots, dualflow_release_slots) index it by slot: [max_batch]. */
 typedef struct {
   void* const* k;
   void* const* v;
@@ -233,7 +237,7 @@ DF_API int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const
 
 /* Workspace for dualflow_prefill / dualflow_prefill_slots: room for max_rows = prompt sequences *
  * prompt tokens activation rows (about (4 d + 4 Hq D + 2 F + 4 ss) bytes per row; a MoE context
- * adds about k (8 d + 2 F + 4 ss + 8) + 12 E bytes per row, k = topk_primary). Allocates (cold
+ * adds about k (6 d + 2 F + 4 ss + 8) + 12 E bytes per row, k = topk_primary). Allocates (cold
  * call, not for a hot loop); a smaller request than the current room does nothing. bf16 contexts,
  * dense or MoE with at most 32 experts (DF_ERR_UNSUPPORTED otherwise); DF_ERR_OOM leaves no
  * prefill room. */
