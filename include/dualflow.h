@@ -29,6 +29,11 @@
  *    vectors and the KV cache as bf16 (round to nearest even); the residual stream, logits and all
  *    accumulations are fp32. DF_DTYPE_F32 stores everything as fp32 (no TF32 anywhere).
  *  - Matrices are row-major [out_features, in_features]; y = x . W^T.
+ *  - A context's workspace (activations, split-KV partials and merge counters, the split-K
+ *    exchange area, the prefill buffers) is shared by all of its calls: calls on one context must
+ *    not overlap on the GPU (issue them on one stream, or order the streams). Independent
+ *    contexts may run concurrently. The library keeps no other global state (except the
+ *    context-free attention call at the end of this header).
  */
 #ifndef DUALFLOW_H
 #define DUALFLOW_H
