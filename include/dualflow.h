@@ -32,8 +32,8 @@
  *  - A context's workspace (activations, split-KV partials and merge counters, the split-K
  *    exchange area, the prefill buffers) is shared by all of its calls: calls on one context must
  *    not overlap on the GPU (issue them on one stream, or order the streams). Independent
- *    contexts may run concurrently. The library keeps no other global state (except the
- *    context-free attention call at the end of this header).
+ *    contexts may run concurrently: apart from the static scratch of the context-free attention
+ *    call (end of this header), every buffer a call writes belongs to its context or its caller.
  */
 #ifndef DUALFLOW_H
 #define DUALFLOW_H
