@@ -562,6 +562,21 @@ def pin_prefill(O):
         assert np.array_equal(got["seq_len"], start + prompt.shape[1])
 
 
+def pin_prefill_moe(O):
+    """Prefill of a MoE model with one expert and top-1 routing equals the torch causal pass of the
+    dense model whose MLP is that expert (the routing weight of a single chosen expert is 1), at
+    every position; its router logits are reported for every position and layer."""
+    hp = tiny_hp(O, n_experts=1, topk_primary=1, topk_aux=1)
+    glob, layers, caches, _, L = tiny_model(O, hp, n_layers=2, seed=33)
+    dense = [dict({k: v for k, v in P.items() if k not in ("Wr", "We_gu", "We_d")}, Wgu=P["We_gu"][0], Wd=P["We_d"][0])
+             for P in layers]
+    prompt = np.random.default_rng(34).integers(0, hp.vocab, size=(2, 3))
+    ref = torch_prefill(tiny_hp(O), glob, dense, caches, prompt, L)
+    got = O.prefill(hp, glob, layers, _writable_caches(O, caches), prompt, L, mirror=False)
+    close(got["logits"], ref, 1e-11, "one-expert MoE prefill logits")
+    assert got["rlog"].shape == (2, 2, 3, 1) and np.all(np.isfinite(got["rlog"]))
+
+
 def _writable_caches(O, caches):
     return [O.DenseCache(K=np.array(c.K, copy=True), V=np.array(c.V, copy=True)) for c in caches]
 
@@ -600,4 +615,4 @@ def pin_generate(O):
 ALL_PINS = [pin_round_bf16, pin_rmsnorm, pin_rope, pin_attention_closed_forms, pin_attention_gqa_vs_sdpa,
             pin_small_ops, pin_primary_is_standard_decoder, pin_flow_invariants, pin_coupling_special_cases, pin_query_coupling_source,
             pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mirror_tracks_exact, pin_mixture_head,
-            pin_sampling, pin_generate, pin_prefill]
+            pin_sampling, pin_generate, pin_prefill, pin_prefill_moe]
