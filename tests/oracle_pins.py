@@ -612,7 +612,44 @@ def pin_generate(O):
     assert np.array_equal(got["tokens"], prim)
 
 
+def pin_generate_paged(O):
+    """Generation through a shuffled paged cache (pages of 4) that holds every position the
+    sequences reach, so the entries each step appends land in pages mapped ahead of time, gives the
+    tokens of the torch-built generator, which keeps its own dense key/value lists; every slot the
+    loop appends to holds a finite entry afterwards and every other unused slot is still unwritten."""
+    hp = tiny_hp(O, vocab=11)
+    n, ps = 5, 4
+    glob, layers, caches, tokens, L = tiny_model(O, hp, n_layers=2, seed=25, couple=False, tie_emb=True)
+    ref = torch_generate(hp, glob, layers, caches, tokens, L, n)
+    B, Hkv, D = len(tokens), hp.n_kv_heads, hp.head_dim
+    need = (L + n + ps - 1) // ps  # pages covering positions 0 .. L_b + n - 1
+    perm = np.random.default_rng(26).permutation(int(need.sum()))
+    table = np.full((B, int(need.max()) + 1), -1)
+    off = 0
+    for b in range(B):
+        table[b, : need[b]] = perm[off: off + need[b]]
+        off += int(need[b])
+    paged = []
+    for c in caches:
+        K = np.full((int(need.sum()), Hkv, ps, D), np.nan)
+        V = np.full_like(K, np.nan)
+        for b in range(B):
+            for pos in range(int(L[b])):
+                pid = table[b, pos // ps]
+                K[pid][:, pos % ps] = c.K[b][:, pos]
+                V[pid][:, pos % ps] = c.V[b][:, pos]
+        paged.append(O.PagedCache(K, V, table, ps))
+    got = O.generate(hp, glob, layers, paged, tokens, L, n, mirror=False)
+    assert np.array_equal(got["tokens"], ref), (got["tokens"], ref)
+    for c in paged:
+        for b in range(B):
+            for pos in range(int(need[b]) * ps):
+                pid = table[b, pos // ps]
+                written = np.all(np.isfinite(c.K[pid][:, pos % ps])) and np.all(np.isfinite(c.V[pid][:, pos % ps]))
+                assert written == (pos < L[b] + n), f"sequence {b} position {pos}: written {written}"
+
+
 ALL_PINS = [pin_round_bf16, pin_rmsnorm, pin_rope, pin_attention_closed_forms, pin_attention_gqa_vs_sdpa,
             pin_small_ops, pin_primary_is_standard_decoder, pin_flow_invariants, pin_coupling_special_cases, pin_query_coupling_source,
             pin_paged_equals_dense, pin_empty_cache, pin_moe_special_cases, pin_mirror_tracks_exact, pin_mixture_head,
-            pin_sampling, pin_generate, pin_prefill, pin_prefill_moe]
+            pin_sampling, pin_generate, pin_generate_paged, pin_prefill, pin_prefill_moe]

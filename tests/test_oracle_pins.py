@@ -63,6 +63,9 @@ MUTANTS = {
     "prefill_no_append": ('                append_entry(caches[layer], b, int(L[b]), r["k_new"][layer, b], r["v_new"][layer, b])\n        L = L + 1\n    return dict(logits=logits',
                           '                pass\n        L = L + 1\n    return dict(logits=logits'),
     "generate_primary_choice": ("    if logits2 is None:\n        p = softmax", "    if True:\n        p = softmax"),
+    "paged_append_wrong_slot": ("cache.K[pid][:, L % cache.page_size, :] = k",
+                                "cache.K[pid][:, (L + 1) % cache.page_size, :] = k"),
+    "paged_append_first_page": ("pid = int(cache.table[b, L // cache.page_size])", "pid = int(cache.table[b, 0])"),
 }
 
 
