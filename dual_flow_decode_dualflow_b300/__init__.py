@@ -25,8 +25,10 @@ C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dual
                "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
                "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head",
                "dualflow_generate", "dualflow_generate_host", "dualflow_prefill_reserve", "dualflow_prefill",
-               "dualflow_prefill_slots", "dualflow_release_slots")
+               "dualflow_prefill_slots", "dualflow_release_slots", "dualflow_set_nvtx", "dualflow_set_wait_limit",
+               "dualflow_router_logits", "dualflow_cuda_error_string")
 DF_PROF_FAMILIES = 8
+DF_NOALLOC_MAX_PAIRS = 512  # the header's limit of batch * n_kv_heads for the context-free attention
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
 
 
@@ -53,7 +55,8 @@ class dualflow_kv(ctypes.Structure):
 
 class DualFlowError(RuntimeError):
     def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn}: {dualflow_status_string(code)} (status {code})")
+        detail = f": {dualflow_cuda_error_string()}" if code == DF_ERR_CUDA else ""
+        super().__init__(f"{fn}: {dualflow_status_string(code)} (status {code}){detail}")
         self.code = code
 
 
@@ -96,6 +99,10 @@ def load_library(path: str = LIB_PATH):
         "dualflow_release_slots": ([vp, POINTER(dualflow_kv), vp, i32, vp, vp, vp], i32),
         "dualflow_generate_host": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, i32, vp],
                                    i32),
+        "dualflow_set_nvtx": ([vp, i32], i32),
+        "dualflow_set_wait_limit": ([vp, ctypes.c_int64], i32),
+        "dualflow_router_logits": ([vp, vp, i32, vp], i32),
+        "dualflow_cuda_error_string": ([], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -130,6 +137,11 @@ def _check(fn: str, rc: int) -> None:
 
 def dualflow_status_string(code: int) -> str:
     return load_library().dualflow_status_string(code).decode()
+
+
+def dualflow_cuda_error_string() -> str:
+    """The last CUDA runtime error the library met in this host thread (diagnoses DF_ERR_CUDA)."""
+    return load_library().dualflow_cuda_error_string().decode()
 
 
 def dualflow_init(cfg: dualflow_config) -> int:
@@ -191,8 +203,25 @@ def dualflow_set_graphs(ctx, enabled: int) -> None:
     _check("dualflow_set_graphs", load_library().dualflow_set_graphs(ctx, enabled))
 
 
-def dualflow_set_profiling(ctx, enabled: int) -> None:
-    _check("dualflow_set_profiling", load_library().dualflow_set_profiling(ctx, enabled))
+def dualflow_set_profiling(ctx, mode: int) -> None:
+    """0: off; 1: CUDA event pair around every launch (serialising); 2: in-graph end stamps, each
+    launch's share of the step (no serialisation)."""
+    _check("dualflow_set_profiling", load_library().dualflow_set_profiling(ctx, mode))
+
+
+def dualflow_set_nvtx(ctx, enabled: int) -> None:
+    _check("dualflow_set_nvtx", load_library().dualflow_set_nvtx(ctx, enabled))
+
+
+def dualflow_set_wait_limit(ctx, limit_ns: int) -> None:
+    """Limit of the kernels' bounded pipeline waits in ns (0: default); failure-path tests only."""
+    _check("dualflow_set_wait_limit", load_library().dualflow_set_wait_limit(ctx, limit_ns))
+
+
+def dualflow_router_logits(ctx, logits, batch: int, stream=None) -> None:
+    """Router logits of the last MoE computation: device fp32 [n_layers, 2, batch, n_experts]."""
+    _check("dualflow_router_logits", load_library().dualflow_router_logits(ctx, _ptr(logits), batch,
+                                                                            _stream(stream)))
 
 
 def dualflow_profile_read(ctx) -> tuple[list[float], list[int]]:

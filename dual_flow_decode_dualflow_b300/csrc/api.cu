@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "internal.h"
 
@@ -18,6 +19,28 @@ namespace df {
 namespace {
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
+}  // namespace
+thread_local char t_driver_error[96] = "";  // last driver call of this library that failed here
+namespace {
+thread_local int t_context_bound = -1;      // device whose primary context this thread made current
+
+// The tensor-map encoder is a driver call: it needs the device's context current in the calling
+// thread, which a host thread that has made no runtime call yet does not have. cudaSetDevice makes
+// the device's primary context current (creating nothing once the device is initialised).
+int bind_context() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DF_ERR_CUDA;
+  if (dev != t_context_bound) {
+    if (cudaSetDevice(dev) != cudaSuccess) return DF_ERR_CUDA;
+    t_context_bound = dev;
+  }
+  return DF_OK;
+}
+
+int encode_failed(CUresult r) {
+  snprintf(t_driver_error, sizeof(t_driver_error), "cuTensorMapEncodeTiled returned CUresult %d", (int)r);
+  return DF_ERR_CUDA;
+}
 
 int get_encoder() {
   std::call_once(g_encode_once, [] {
@@ -32,9 +55,27 @@ int get_encoder() {
 }
 }  // namespace
 
+int set_smem_attrs_once(const void* kernel) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;  // (kernel, device) already set
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DF_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const auto& e : done)
+    if (e.first == kernel && e.second == dev) return DF_OK;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || optin <= 0)
+    return DF_ERR_CUDA;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) != cudaSuccess ||
+      cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+    return DF_ERR_CUDA;
+  done.emplace_back(kernel, dev);
+  return DF_OK;
+}
+
 int encode_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
                        uint32_t box_inner, uint32_t box_rows) {
-  if (get_encoder() != DF_OK) return DF_ERR_CUDA;
+  if (get_encoder() != DF_OK || bind_context() != DF_OK) return DF_ERR_CUDA;
   if ((reinterpret_cast<uintptr_t>(base) & 15u) || (row_stride_bytes & 15u)) return DF_ERR_ARG;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {row_stride_bytes};
@@ -43,12 +84,12 @@ int encode_map_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint6
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DF_OK : DF_ERR_CUDA;
+  return r == CUDA_SUCCESS ? DF_OK : encode_failed(r);
 }
 
 int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1_bytes,
                        uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
-  if (get_encoder() != DF_OK) return DF_ERR_CUDA;
+  if (get_encoder() != DF_OK || bind_context() != DF_OK) return DF_ERR_CUDA;
   if ((reinterpret_cast<uintptr_t>(base) & 15u) || (stride1_bytes & 15u) || (stride2_bytes & 15u)) return DF_ERR_ARG;
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
@@ -57,7 +98,7 @@ int encode_map_3d_bf16(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DF_OK : DF_ERR_CUDA;
+  return r == CUDA_SUCCESS ? DF_OK : encode_failed(r);
 }
 
 }  // namespace df
@@ -177,10 +218,14 @@ int check_weights(const dualflow_ctx* ctx, const dualflow_weights* w) {
 }
 
 // ------------------------------------------------------------------ launch bookkeeping
-// Counts every kernel the step launches by family and, when profiling is on, brackets it with a
-// CUDA event pair on the launching stream. The records are external event nodes when the step is
-// being captured, so the replayed graph records them (a plain record during capture would only
-// become an internal dependency, with no timestamp).
+const char* const kFamNames[DF_PROF_FAMILIES] = {"norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head",
+                                                 "other"};
+
+// Counts every kernel the step launches by family. Profiling mode 1 brackets each launch with a
+// CUDA event pair on the launching stream (external event nodes when the step is being captured,
+// so the replayed graph records them; this serialises the launches). Mode 2 gives each launch a
+// stamp slot that its CTAs raise to the globaltimer value at their end (no serialisation). With
+// NVTX on, each launch is a named range (host side: eager launches, or the capture).
 struct Launcher {
   dualflow_ctx* ctx;
   cudaStream_t s;
@@ -188,21 +233,48 @@ struct Launcher {
   int operator()(int fam, F&& f) {
     ctx->step_launches[fam]++;
     ProfRec* r = nullptr;
-    if (ctx->profiling && ctx->prof_n < (int)ctx->prof.size()) {
+    if (ctx->profiling == 1 && ctx->prof_n < (int)ctx->prof.size()) {
       r = &ctx->prof[ctx->prof_n++];
       r->fam = fam;
       if (cudaEventRecordWithFlags(r->a, s, cudaEventRecordExternal) != cudaSuccess) return DF_ERR_CUDA;
+    } else if (ctx->profiling == 2 && ctx->prof_n < (int)ctx->prof_fam.size()) {
+      ctx->prof_fam[ctx->prof_n] = fam;
+      ctx->cur_stamp = ctx->stamps + 1 + ctx->prof_n;
+      ctx->prof_n++;
     }
+    if (ctx->nvtx) nvtxRangePushA(kFamNames[fam]);
     const int rc = f();
+    if (ctx->nvtx) nvtxRangePop();
+    ctx->cur_stamp = nullptr;
     if (r && cudaEventRecordWithFlags(r->b, s, cudaEventRecordExternal) != cudaSuccess) return DF_ERR_CUDA;
     return rc;
   }
 };
 
-void reset_counts(dualflow_ctx* ctx) {
+int reset_counts(dualflow_ctx* ctx, cudaStream_t s) {
   for (int& n : ctx->step_launches) n = 0;
   ctx->prof_n = 0;
+  ctx->cur_stamp = nullptr;
+  // mode 2: the step's start slot is lowered by its first kernel from the largest value
+  if (ctx->profiling == 2 && cudaMemsetAsync(ctx->stamps, 0xff, sizeof(unsigned long long), s) != cudaSuccess)
+    return DF_ERR_CUDA;
+  return DF_OK;
 }
+
+// NVTX range for one layer of the step (host side), closed on scope exit.
+struct LayerRange {
+  bool on;
+  LayerRange(const dualflow_ctx* ctx, int l) : on(ctx->nvtx != 0) {
+    if (on) {
+      char name[32];
+      snprintf(name, sizeof(name), "layer %d", l);
+      nvtxRangePushA(name);
+    }
+  }
+  ~LayerRange() {
+    if (on) nvtxRangePop();
+  }
+};
 
 // ------------------------------------------------------------------ the MoE MLP (bf16)
 // x (the norm-fed operand, rows scaled by 1 / rms from ss_parts partials) -> router logits ->
@@ -221,6 +293,8 @@ int run_moe(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int b
     g.eps = c.rms_eps;
     g.pdl = pdl;
   };
+  // this layer's router logits, kept per layer for dualflow_router_logits
+  float* rlog = ctx->rlog + (size_t)l * mrows * E;
   GemmArgs r = gemm_args(ctx);
   r.x = ctx->x;
   r.W = w->Wr[l];
@@ -229,11 +303,11 @@ int run_moe(dualflow_ctx* ctx, float* h, const dualflow_weights* w, int l, int b
   r.m_p = mp;
   r.m_a = ma;
   r.epi = EPI_STORE_F32;
-  r.y = ctx->rlog;
+  r.y = rlog;
   r.ldy = E;
   normed(r);
   DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_gemm_tc(ctx, r, s); }));
-  DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_moe_route(ctx, ctx->rlog, batch, aux_on, ids, s, pdl); }));
+  DF_TRY(L(DF_PROF_GATEUP, [&] { return launch_moe_route(ctx, rlog, batch, aux_on, ids, s, pdl); }));
   GemmArgs g = gemm_args(ctx);
   g.x = ctx->x;
   g.W = w->We_gu[l];
@@ -381,6 +455,7 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
     gemm_prefetch_next(ctx, cur, nx);
   };
   for (int l = 0; l < c.n_layers; ++l) {
+    LayerRange range(ctx, l);
     GemmArgs g = gemm_args(ctx);
     g.x = ctx->x;
     g.W = w->Wqkv[l];
@@ -470,7 +545,7 @@ int run_step_bf16(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_k
 int run_step(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens, int batch,
              float* logits, int aux_on, cudaStream_t s) {
   const dualflow_config& c = ctx->cfg;
-  reset_counts(ctx);
+  DF_TRY(reset_counts(ctx, s));
   if (c.dtype == DF_DTYPE_BF16) return run_step_bf16(ctx, w, kv, tokens, batch, logits, aux_on, s);
   const int mp = batch, ma = aux_on ? batch : 0, M = mp + ma;
   const int qkv_n = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim, qd = c.n_q_heads * c.head_dim;
@@ -515,6 +590,7 @@ void graph_key(std::vector<uint64_t>& k, const dualflow_ctx* ctx, const dualflow
   k.push_back((uint64_t)batch);
   k.push_back((uint64_t)aux_on);
   k.push_back((uint64_t)ctx->profiling);
+  k.push_back((uint64_t)ctx->wait_ns);
   P(w->E1), P(w->E2), P(w->W_lm), P(w->g_final);
   P(kv->seq_len), P(kv->page_table);
   for (int l = 0; l < L; ++l) {
@@ -618,6 +694,12 @@ void free_prefill_moe(dualflow_ctx* ctx) {
 // ================================================================== C ABI
 extern "C" {
 
+const char* dualflow_cuda_error_string(void) {
+  const cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess || df::t_driver_error[0] == 0) return cudaGetErrorString(e);
+  return df::t_driver_error;
+}
+
 const char* dualflow_status_string(int st) {
   switch (st) {
     case DF_OK: return "ok";
@@ -695,7 +777,7 @@ int dualflow_init(const dualflow_config* cfg, dualflow_ctx** out) {
   if (dalloc(&ctx->ss, (size_t)ctx->ss_ld * MB * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
   if (c.n_experts > 0) {
     const size_t E = c.n_experts, kmax = std::max(c.topk_primary, c.topk_aux);
-    if (dalloc(&ctx->rlog, MB * E * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
+    if (dalloc(&ctx->rlog, (size_t)std::max(c.n_layers, 1) * MB * E * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
     if (dalloc(&ctx->sel_pos, MB * E * sizeof(int32_t)) != DF_OK) return fail(DF_ERR_OOM);
     if (dalloc(&ctx->sel_w, MB * E * sizeof(float)) != DF_OK) return fail(DF_ERR_OOM);
     if (dalloc(&ctx->moe_u, E * MB * c.ffn_hidden * es) != DF_OK) return fail(DF_ERR_OOM);
@@ -723,6 +805,7 @@ int dualflow_free(dualflow_ctx* ctx) {
     if (r.a) cudaEventDestroy(r.a);
     if (r.b) cudaEventDestroy(r.b);
   }
+  if (ctx->stamps) cudaFree(ctx->stamps);
   void* ptrs[] = {ctx->status, ctx->rope, ctx->attn_part, ctx->attn_cnt, ctx->h,
                   ctx->x,      ctx->q,    ctx->o,         ctx->u,        ctx->raw,       ctx->tokens_dev, ctx->logits_dev, ctx->ss,
                   ctx->rlog, ctx->sel_pos, ctx->sel_w, ctx->moe_u, ctx->moe_y, ctx->moe_ids, ctx->gen_tokens, ctx->gen_out_dev, ctx->gen_u_dev,
@@ -822,7 +905,7 @@ int dualflow_coupled_mlp(dualflow_ctx* ctx, float* h, const dualflow_weights* w,
   if (batch <= 0 || batch > ctx->cfg.max_batch) return DF_ERR_SHAPE;
   if (layer < 0 || layer >= ctx->cfg.n_layers) return DF_ERR_ARG;
   DF_TRY(check_weights(ctx, w));
-  reset_counts(ctx);
+  DF_TRY(reset_counts(ctx, S(stream)));
   DF_TRY(run_mlp(ctx, h, w, layer, batch, aux_on, S(stream)));
   const dualflow_config& c = ctx->cfg;
   if (expert_ids_out && c.n_experts > 0) {
@@ -1159,16 +1242,22 @@ int dualflow_set_graphs(dualflow_ctx* ctx, int32_t enabled) {
   return DF_OK;
 }
 
-int dualflow_set_profiling(dualflow_ctx* ctx, int32_t enabled) {
-  if (!ctx || (enabled != 0 && enabled != 1)) return DF_ERR_ARG;
-  if (enabled && ctx->prof.empty()) {
-    const int n = 8 * std::max(ctx->cfg.n_layers, 1) + 16;
+int dualflow_set_profiling(dualflow_ctx* ctx, int32_t mode) {
+  if (!ctx || mode < 0 || mode > 2) return DF_ERR_ARG;
+  if (mode == 2 && ctx->cfg.dtype != DF_DTYPE_BF16) return DF_ERR_UNSUPPORTED;
+  const int n = 8 * std::max(ctx->cfg.n_layers, 1) + 16;
+  if (mode == 1 && ctx->prof.empty()) {
     ctx->prof.resize(n);
     for (auto& r : ctx->prof)
       if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return DF_ERR_CUDA;
   }
-  if (ctx->profiling != enabled) drop_graphs(ctx);
-  ctx->profiling = enabled;
+  if (mode == 2 && ctx->stamps == nullptr) {
+    if (dalloc(&ctx->stamps, (size_t)(n + 1) * sizeof(unsigned long long)) != DF_OK) return DF_ERR_OOM;
+    if (cudaMemset(ctx->stamps, 0, (size_t)(n + 1) * sizeof(unsigned long long)) != cudaSuccess) return DF_ERR_CUDA;
+    ctx->prof_fam.assign(n, 0);
+  }
+  if (ctx->profiling != mode) drop_graphs(ctx);
+  ctx->profiling = mode;
   return DF_OK;
 }
 
@@ -1180,14 +1269,56 @@ int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches, int32
     for (int f = 0; f < n; ++f) launches[f] = ctx->step_launches[f];
   if (ms) {
     for (int f = 0; f < n; ++f) ms[f] = 0.f;
-    if (ctx->profiling)
+    if (ctx->profiling == 1)
       for (int i = 0; i < ctx->prof_n; ++i) {
         float t = 0.f;
         if (cudaEventElapsedTime(&t, ctx->prof[i].a, ctx->prof[i].b) != cudaSuccess) return DF_ERR_CUDA;
         if (ctx->prof[i].fam < n) ms[ctx->prof[i].fam] += t;
       }
+    if (ctx->profiling == 2 && ctx->prof_n > 0) {
+      // each launch's share of the step: from the end of the launch before it (the step's start
+      // for the first) to its own end
+      std::vector<unsigned long long> st((size_t)ctx->prof_n + 1);
+      if (cudaMemcpy(st.data(), ctx->stamps, st.size() * sizeof(unsigned long long), cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
+        return DF_ERR_CUDA;
+      unsigned long long prev = st[0];
+      for (int i = 0; i < ctx->prof_n; ++i) {
+        const unsigned long long e = st[1 + (size_t)i];
+        const double dt = e > prev ? (double)(e - prev) * 1e-6 : 0.0;
+        if (ctx->prof_fam[i] < n) ms[ctx->prof_fam[i]] += (float)dt;
+        prev = e > prev ? e : prev;
+      }
+    }
   }
   return DF_OK;
+}
+
+int dualflow_set_nvtx(dualflow_ctx* ctx, int32_t enabled) {
+  if (!ctx || (enabled != 0 && enabled != 1)) return DF_ERR_ARG;
+  ctx->nvtx = enabled;
+  return DF_OK;
+}
+
+int dualflow_set_wait_limit(dualflow_ctx* ctx, int64_t limit_ns) {
+  if (!ctx || limit_ns < 0) return DF_ERR_ARG;
+  if ((unsigned long long)limit_ns != ctx->wait_ns) drop_graphs(ctx);
+  ctx->wait_ns = (unsigned long long)limit_ns;
+  return DF_OK;
+}
+
+int dualflow_router_logits(dualflow_ctx* ctx, float* logits, int32_t batch, dualflow_stream stream) {
+  if (!ctx || !logits) return DF_ERR_ARG;
+  const dualflow_config& c = ctx->cfg;
+  if (c.n_experts == 0 || c.dtype != DF_DTYPE_BF16) return DF_ERR_UNSUPPORTED;
+  if (batch <= 0 || batch > c.max_batch) return DF_ERR_SHAPE;
+  if (c.n_layers == 0) return DF_OK;
+  const size_t row = (size_t)2 * batch * c.n_experts * sizeof(float);
+  const size_t pitch = (size_t)2 * c.max_batch * c.n_experts * sizeof(float);
+  return cudaMemcpy2DAsync(logits, row, ctx->rlog, pitch, row, (size_t)c.n_layers, cudaMemcpyDeviceToDevice,
+                           S(stream)) == cudaSuccess
+             ? DF_OK
+             : DF_ERR_CUDA;
 }
 
 int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream) {

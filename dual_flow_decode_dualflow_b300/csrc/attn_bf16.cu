@@ -41,17 +41,21 @@ struct AttnParams {
   int32_t* cnt;      // [pairs] CTAs done with each pair (zero between launches)
   int32_t* status;
   float scale_log2;  // log2(e) / sqrt(D)
+  unsigned long long wait_ns;  // limit of the pipeline's bounded waits
 };
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
 
-__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* err, int32_t* status) {
+// A pipeline wait that gives up after `limit` ns, or at once when another warp of the CTA already
+// gave up (err), so that one expired wait ends the CTA's main loop without further waiting.
+__device__ __forceinline__ bool wait_or_fail(uint64_t* bar, uint32_t parity, volatile int* err, int32_t* status,
+                                             uint64_t limit) {
   if (*err) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
     if (*err) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) {
+    if (globaltimer() - t0 > limit) {
       *err = 1;
       set_status(status, DF_ERR_TIMEOUT);
       return false;
@@ -207,6 +211,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
                     reinterpret_cast<const __nv_bfloat16*>(a.q) + (((size_t)f * B + b) * Hq + g * G) * kHeadDim,
                     (uint32_t)(G * kHeadDim * 2), &full[s]);
       };
+      int issued = 0;
       for (int i = 0; i < n_my; ++i) {
         const int s = (int)(i % kStagesA);
         const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
@@ -218,7 +223,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
           for (int k = 0; k < npend; ++k) issue_q(pend_s[k], pend_b[k], pend_g[k]);
           npend = 0;
         }
-        if (!wait_or_fail(&empty[s], ph ^ 1u, err, P.status)) break;
+        if (!wait_or_fail(&empty[s], ph ^ 1u, err, P.status, P.wait_ns)) break;
         const bool seg_start = (w.j == 0) || (i == 0);
         uint8_t* Kst = smem + s * kStageBytes;
         uint8_t* Vst = Kst + kTileBytes;
@@ -268,11 +273,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
           }
         }
         walker_next(w, sched, B, Hkv);
+        ++issued;
       }
       if (!waited) {
         griddep_wait();
         for (int k = 0; k < npend; ++k) issue_q(pend_s[k], pend_b[k], pend_g[k]);
       }
+      // Every copy issued into the stages has landed before this warp exits, so that none writes
+      // into the CTA's shared memory after the CTA is gone (after a wait gave up, the consumers
+      // stop reading the stages and may exit first).
+      if (!mbar_drain(full, kStagesA, issued)) set_status(P.status, DF_ERR_TIMEOUT);
     }
     return;
   }
@@ -288,7 +298,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
       for (int i = threadIdx.x; i < Hq * kHeadDim; i += kConsumers * 32)
         o[((size_t)f * B + b) * Hq * kHeadDim + i] = __float2bfloat16_rn(0.f);
   }
-  if (n_my <= 0) return;
+  if (n_my <= 0) {
+    if (a.stamp != nullptr && threadIdx.x == 0) atomicMax(a.stamp, (unsigned long long)globaltimer());
+    return;
+  }
 
   const int kw = 16 * warp;
   const int qn = lane >> 2;          // query row this lane feeds into the B fragment
@@ -308,7 +321,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
     const int Leff = lens[w.b];
     const int s = (int)(i % kStagesA);
     const uint32_t ph = (uint32_t)(i / kStagesA) & 1u;
-    const bool ok = wait_or_fail(&full[s], ph, err, P.status);
+    const bool ok = wait_or_fail(&full[s], ph, err, P.status, P.wait_ns);
     if (new_seg) {
       // this group's 2G query rows (primary heads, then auxiliary heads) as B fragments, from the
       // stage's query area
@@ -551,62 +564,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
     }
     walker_next(w, sched, B, Hkv);
   }
+  if (a.stamp != nullptr && threadIdx.x == 0) atomicMax(a.stamp, (unsigned long long)globaltimer());
 }
 
 }  // namespace
 
 int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl) {
-  const dualflow_config& cfg = ctx->cfg;
-  if (a.batch <= 0) return DF_OK;
-  if (reinterpret_cast<uintptr_t>(a.q) & 15u) return DF_ERR_ARG;  // bulk copies of query rows
-  CUtensorMap mk, mv;
-  int rc;
-  if (!a.paged) {
-    const uint64_t rows = (uint64_t)cfg.max_batch * cfg.n_kv_heads;
-    rc = encode_map_3d_bf16(&mk, a.k_cache, kHeadDim, (uint64_t)cfg.max_ctx, rows, kHeadDim * 2,
-                            (uint64_t)cfg.max_ctx * kHeadDim * 2, 64, kAttnTileKeys, 1);
-    if (rc == DF_OK)
-      rc = encode_map_3d_bf16(&mv, a.v_cache, kHeadDim, (uint64_t)cfg.max_ctx, rows, kHeadDim * 2,
-                              (uint64_t)cfg.max_ctx * kHeadDim * 2, 64, kAttnTileKeys, 1);
-  } else {
-    const uint64_t rows = (uint64_t)cfg.max_pages * cfg.n_kv_heads;
-    rc = encode_map_3d_bf16(&mk, a.k_cache, kHeadDim, (uint64_t)cfg.page_size, rows, kHeadDim * 2,
-                            (uint64_t)cfg.page_size * kHeadDim * 2, 64, (uint32_t)cfg.page_size, 1);
-    if (rc == DF_OK)
-      rc = encode_map_3d_bf16(&mv, a.v_cache, kHeadDim, (uint64_t)cfg.page_size, rows, kHeadDim * 2,
-                              (uint64_t)cfg.page_size * kHeadDim * 2, 64, (uint32_t)cfg.page_size, 1);
-  }
-  if (rc != DF_OK) return rc;
-  AttnParams p;
-  p.a = a;
-  p.part = ctx->attn_part;
-  p.cnt = ctx->attn_cnt;
-  p.status = ctx->status;
-  p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
-  const size_t smem = 1024 + (size_t)kStagesA * (kStageBytes + kQBytes) + kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
-                      (size_t)(2 * a.batch + 1) * 4;
-  if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-    return DF_ERR_CUDA;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(ctx->attn_ctas, 1, 1);
-  lc.blockDim = dim3(kAttnThreads, 1, 1);
-  lc.dynamicSmemBytes = smem;
-  lc.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&lc, attn_bf16_kernel, mk, mv, p) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  AttnArgs at = a;
+  if (at.stamp == nullptr) at.stamp = ctx->cur_stamp;
+  return launch_attention_bf16_ws(ctx->cfg, at, ctx->attn_part, ctx->attn_cnt, ctx->status, ctx->attn_ctas, s, pdl,
+                                  ctx->wait_ns);
 }
 
-}  // namespace df
-
-namespace df {
-
 int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, float* part, int32_t* cnt,
-                             int32_t* status, int ctas, cudaStream_t s) {
+                             int32_t* status, int ctas, cudaStream_t s, int pdl, unsigned long long wait_ns) {
   if (a.batch <= 0) return DF_OK;
   if (ctas <= 0 || !part || !cnt || !status) return DF_ERR_ARG;
   if (reinterpret_cast<uintptr_t>(a.q) & 15u) return DF_ERR_ARG;  // bulk copies of query rows
@@ -636,13 +607,21 @@ int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, floa
   p.cnt = cnt;
   p.status = status;
   p.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+  p.wait_ns = wait_ns ? wait_ns : kWaitLimitNs;
   const size_t smem = 1024 + (size_t)kStagesA * (kStageBytes + kQBytes) + kMergeFloats * 4 + 2 * kStagesA * 8 + 16 +
                       (size_t)(2 * a.batch + 1) * 4;
-  if (cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
-      cudaFuncSetAttribute(attn_bf16_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-    return DF_ERR_CUDA;
-  attn_bf16_kernel<<<ctas, kAttnThreads, smem, s>>>(mk, mv, p);
-  return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
+  if (set_smem_attrs_once(reinterpret_cast<const void*>(attn_bf16_kernel)) != DF_OK) return DF_ERR_CUDA;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)ctas, 1, 1);
+  lc.blockDim = dim3(kAttnThreads, 1, 1);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, attn_bf16_kernel, mk, mv, p) == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
 }  // namespace df

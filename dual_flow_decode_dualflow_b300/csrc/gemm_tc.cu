@@ -60,6 +60,7 @@ struct GemmParams {
   float* part;     // S > 1: the split-K exchange area, [CTA of the launch][S slices][n_pad][2 nl]
   int chunk;       // S == 1: accumulator rows drained to shared memory per epilogue pass
   int32_t* status;
+  unsigned long long wait_ns;  // limit of the pipeline's bounded waits
 };
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
@@ -319,10 +320,11 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     griddep_wait();
     for (int i = 0; i < npre; ++i)
       tma_load_2d_hint(sB + i * b_bytes, &map_x, &full[i], (kb0 + i) * kGemmTileK, xrow, pol_x);
+    int issued = npre;
     for (int i = npre; i < nkb; ++i) {
       const int s = i % nst;
       const uint32_t ph = (uint32_t)(i / nst) & 1u;
-      if (!mbar_wait(&empty[s], ph ^ 1u)) {
+      if (!mbar_wait(&empty[s], ph ^ 1u, p.wait_ns)) {
         set_status(p.status, DF_ERR_TIMEOUT);
         break;
       }
@@ -331,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
       tma_load_2d_hint(sA + s * kABytes, &map_w, &full[s], kc, row0, pol_w);
       tma_load_2d_hint(sA + s * kABytes + kABytes / 2, &map_w, &full[s], kc, row1, pol_w);
       tma_load_2d_hint(sB + s * b_bytes, &map_x, &full[s], kc, xrow, pol_x);
+      ++issued;
     }
     if (a.pf_W != nullptr && a.pf_depth > 0) {
       // every tile of this launch is requested: warm L2 with the next launch's first k-blocks
@@ -347,13 +350,17 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
         }
       }
     }
+    // Every load issued into the stages lands before they are reused for the accumulator tile or
+    // the CTA exits. After a normal main loop the MMA thread has consumed all of them already; after
+    // a wait that gave up this is what keeps an asynchronous copy from writing into freed memory.
+    if (!mbar_drain(full, nst, issued)) set_status(p.status, DF_ERR_TIMEOUT);
   } else if (warp == 1 && lane == 0) {
     // MMA issuer: 4 x (M=128, N=n_pad, K=16) per stage, accumulate in TMEM.
     const uint32_t idesc = idesc_bf16_f32(kGemmTileN, p.n_pad);
     for (int i = 0; i < nkb; ++i) {
       const int s = i % nst;
       const uint32_t ph = (uint32_t)(i / nst) & 1u;
-      if (!mbar_wait(&full[s], ph)) {
+      if (!mbar_wait(&full[s], ph, p.wait_ns)) {
         set_status(p.status, DF_ERR_TIMEOUT);
         break;
       }
@@ -376,13 +383,23 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
       const float* row = a.ss_in + (size_t)n * a.ss_ld;
       float ss = 0.f;
       int q = 0;
+      // up to 16 vector loads in flight, summed in partial order afterwards
       if ((a.ss_ld & 3) == 0)
-        for (; q + 4 <= a.ss_parts; q += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(row + q);
-          ss += v.x;
-          ss += v.y;
-          ss += v.z;
-          ss += v.w;
+        while (q + 4 <= a.ss_parts) {
+          float4 v[16];
+          const int nv = min(16, (a.ss_parts - q) / 4);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < nv) v[j] = *reinterpret_cast<const float4*>(row + q + 4 * j);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (j < nv) {
+              ss += v[j].x;
+              ss += v[j].y;
+              ss += v[j].z;
+              ss += v[j].w;
+            }
+          q += 4 * nv;
         }
       for (; q < a.ss_parts; ++q) ss += row[q];
       rstd_s[n] = 1.0f / sqrtf(ss * a.inv_d + a.eps);
@@ -689,16 +706,17 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   }
   if (cb + chunk < p.n_pad) __syncthreads();  // the next pass overwrites the drained rows
   }
+  if (a.stamp != nullptr) {  // in-graph timing: this launch's end
+    __syncthreads();
+    if (threadIdx.x == 0) atomicMax(a.stamp, (unsigned long long)globaltimer());
+  }
 }
 
 template <int EPI, bool RB = false>
 int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& mpf, const GemmParams& p, size_t smem,
                cudaStream_t s) {
   auto kern = gemm_tc_kernel<EPI, RB>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return DF_ERR_CUDA;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-    return DF_ERR_CUDA;
+  if (set_smem_attrs_once(reinterpret_cast<const void*>(kern)) != DF_OK) return DF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_tiles, p.row_blocks > 1 ? p.row_blocks : p.splits,
                      (p.a.n_groups > 0 && !p.a.blk_info) ? p.a.n_groups : 1);
@@ -789,6 +807,8 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   p.n_tiles = gemm_tiles(a.n_out, a.epi);
   p.splits = a.row_blocked ? 1 : gemm_splits(ctx, a.n_out, a.k, a.epi, groups);
   p.status = ctx->status;
+  p.wait_ns = ctx->wait_ns ? ctx->wait_ns : kWaitLimitNs;
+  if (p.a.stamp == nullptr) p.a.stamp = ctx->cur_stamp;
   const uintptr_t align = (a.epi == EPI_STORE_BF16 || a.epi == EPI_SWIGLU || a.epi == EPI_MOE_GATEUP) ? 8 : 16;
   p.vec_ok = a.y != nullptr && (reinterpret_cast<uintptr_t>(a.y) % align == 0) && (a.ldy % 4 == 0) ? 1 : 0;
   if (a.g_next != nullptr && !p.vec_ok) return DF_ERR_ARG;

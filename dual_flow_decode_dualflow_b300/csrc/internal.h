@@ -96,6 +96,9 @@ struct GemmArgs {
   // *n_blk do nothing. m_p is the capacity in rows (the x tensor map's extent).
   const int4* blk_info;
   const int32_t* n_blk;
+  // In-graph timing (profiling mode 2): the CTAs raise *stamp to the globaltimer value at their end
+  // (nullable).
+  unsigned long long* stamp;
 };
 
 struct AttnArgs {
@@ -109,6 +112,7 @@ struct AttnArgs {
   int paged, page_size, max_ctx, max_pages, pages_per_seq;
   int extra;                // 1 when the step appended slot seq_len[b] (attend 0..seq_len[b])
   int aux_on;
+  unsigned long long* stamp;  // in-graph timing: raised to the globaltimer value at the end (nullable)
 };
 
 struct ProfRec {
@@ -184,6 +188,14 @@ struct dualflow_ctx {
   std::vector<df::ProfRec> prof;
   int prof_n = 0;
   int step_launches[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  // in-graph timing (profiling mode 2): stamps[0] = start of the step's first kernel, stamps[1 + i]
+  // = end of its i-th launch; prof_fam[i] = that launch's family
+  unsigned long long* stamps = nullptr;
+  std::vector<int> prof_fam;
+  unsigned long long* cur_stamp = nullptr;  // the slot of the launch being recorded (nullptr: none)
+  // limit of the bounded pipeline waits (ns); 0 = the library default. Failure-path tests only.
+  unsigned long long wait_ns = 0;
+  int nvtx = 0;  // NVTX ranges around the step's layers and launches
 };
 
 namespace df {
@@ -204,9 +216,16 @@ void gemm_prefetch_next(const dualflow_ctx* ctx, GemmArgs& cur, const GemmArgs& 
 int launch_attention_bf16(dualflow_ctx* ctx, const AttnArgs& a, cudaStream_t s, int pdl = 0);
 // The same kernel with caller-chosen workspace: split partials (>= pairs + ctas slots of
 // kAttnPartFloats), per-pair merge counters (zero on entry), the status word, and a grid of `ctas`
-// CTAs; cache geometry is taken from `cfg`. Used by the allocation-free entry point.
+// CTAs; cache geometry is taken from `cfg`; wait_ns = limit of the pipeline waits (0: default).
+// Used by the allocation-free entry point and, with the context's workspace, by the one above.
 int launch_attention_bf16_ws(const dualflow_config& cfg, const AttnArgs& a, float* part, int32_t* cnt,
-                             int32_t* status, int ctas, cudaStream_t s);
+                             int32_t* status, int ctas, cudaStream_t s, int pdl = 0,
+                             unsigned long long wait_ns = 0);
+// Sets a kernel's shared-memory attributes once per device: the device's largest opt-in dynamic
+// shared memory and the full shared-memory carveout. Launches never change them again, so
+// concurrent launches of the same kernel with different sizes cannot race on a process-wide
+// attribute. Thread-safe.
+int set_smem_attrs_once(const void* kernel);
 
 int launch_embed_rmsnorm(dualflow_ctx* ctx, const void* E1, const void* E2, const int32_t* tokens, const void* g,
                          int batch, int aux_on, cudaStream_t s);

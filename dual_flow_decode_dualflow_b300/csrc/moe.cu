@@ -42,10 +42,12 @@ __device__ __forceinline__ float masked_softmax(float v, bool sel) {
 // -1 if not selected), sel_w[row][e] (mixing weight), ids[f][b][kmax] (experts in set order, -1
 // padded; nullable).
 __global__ void moe_route_kernel(const float* rlog, int B, int E, int k1, int k2, int aux_on, int32_t* sel_pos,
-                                 float* sel_w, int32_t* ids, int kmax) {
+                                 float* sel_w, int32_t* ids, int kmax, unsigned long long* stamp) {
   griddep_launch_dependents();
   griddep_wait();
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), e = threadIdx.x & 31;
+  // in-graph timing (nullable): raised by every warp as it finishes
+  if (stamp != nullptr && e == 0 && b >= B) atomicMax(stamp, (unsigned long long)globaltimer());
   if (b >= B) return;
   const bool live = e < E;
   const float r1 = live ? rlog[(size_t)b * E + e] : -INFINITY;
@@ -61,6 +63,7 @@ __global__ void moe_route_kernel(const float* rlog, int B, int E, int k1, int k2
   if (ids && in1) ids[(size_t)b * kmax + rank] = e;
   if (!aux_on) {
     if (ids && e < kmax) ids[((size_t)B + b) * kmax + e] = -1;
+    if (stamp != nullptr && e == 0) atomicMax(stamp, (unsigned long long)globaltimer());
     return;
   }
   // auxiliary flow: the primary logits choose the set (replay), its own logits weight it
@@ -74,6 +77,7 @@ __global__ void moe_route_kernel(const float* rlog, int B, int E, int k1, int k2
   if (ids && e < kmax) ids[((size_t)B + b) * kmax + e] = -1;
   __syncwarp();
   if (ids && in2) ids[((size_t)B + b) * kmax + rank] = e;
+  if (stamp != nullptr && e == 0) atomicMax(stamp, (unsigned long long)globaltimer());
 }
 
 // grid (B, ceil(d / 512)), 128 threads, 4 features each. For sequence b and both flows:
@@ -81,7 +85,8 @@ __global__ void moe_route_kernel(const float* rlog, int B, int E, int k1, int k2
 // With g_next: x_next = bf16(h (*) g_next) and ss[row * ss_ld + chunk] = sum of h^2 over the chunk.
 __global__ void moe_combine_kernel(const float* Y, int mrows, int d, int B, int E, int aux_on, const int32_t* sel_pos,
                                    const float* sel_w, const __nv_bfloat16* c, float* h, const __nv_bfloat16* g_next,
-                                   __nv_bfloat16* x_next, float* ss, int ss_ld, int32_t* status) {
+                                   __nv_bfloat16* x_next, float* ss, int ss_ld, int32_t* status,
+                                   unsigned long long* stamp) {
   griddep_launch_dependents();
   griddep_wait();
   __shared__ int order[2][32];
@@ -168,6 +173,10 @@ __global__ void moe_combine_kernel(const float* Y, int mrows, int d, int B, int 
       const float v = ((red[t][0] + red[t][1]) + red[t][2]) + red[t][3];
       ss[(size_t)(t * B + b) * ss_ld + chunk] = v;
     }
+  }
+  if (stamp != nullptr) {  // in-graph timing: this launch's end
+    __syncthreads();
+    if (t == 0) atomicMax(stamp, (unsigned long long)globaltimer());
   }
   (void)status;
 }
@@ -333,7 +342,7 @@ int launch_moe_route_rows(const dualflow_config& c, const float* rlog, int R, in
                           cudaStream_t s) {
   const int kmax = c.topk_primary > c.topk_aux ? c.topk_primary : c.topk_aux;
   moe_route_kernel<<<(R + 3) / 4, 128, 0, s>>>(rlog, R, c.n_experts, c.topk_primary, c.topk_aux, 0, sel_pos, sel_w,
-                                               nullptr, kmax);
+                                               nullptr, kmax, nullptr);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
@@ -376,7 +385,7 @@ int launch_moe_route(dualflow_ctx* ctx, const float* rlog, int batch, int aux_on
   lc.attrs = attr;
   lc.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&lc, moe_route_kernel, rlog, batch, c.n_experts, c.topk_primary, c.topk_aux, aux_on,
-                            ctx->sel_pos, ctx->sel_w, ids, kmax) == cudaSuccess
+                            ctx->sel_pos, ctx->sel_w, ids, kmax, ctx->cur_stamp) == cudaSuccess
              ? DF_OK
              : DF_ERR_CUDA;
 }
@@ -396,7 +405,7 @@ int launch_moe_combine(dualflow_ctx* ctx, float* h, int batch, int aux_on, const
   return cudaLaunchKernelEx(&lc, moe_combine_kernel, (const float*)ctx->moe_y, 2 * c.max_batch, c.d_model, batch,
                             c.n_experts, aux_on, (const int32_t*)ctx->sel_pos, (const float*)ctx->sel_w,
                             (const __nv_bfloat16*)c_vec, h, (const __nv_bfloat16*)g_next, (__nv_bfloat16*)ctx->x,
-                            ctx->ss, ctx->ss_ld, ctx->status) == cudaSuccess
+                            ctx->ss, ctx->ss_ld, ctx->status, ctx->cur_stamp) == cudaSuccess
              ? DF_OK
              : DF_ERR_CUDA;
 }

@@ -52,14 +52,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false when the limit expired.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false when the limit (ns) expired.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
   return true;
+}
+
+// After a pipeline gave up on a wait: waits (with the full limit) for the loads this thread issued
+// into its last min(stages, issued) iterations, so that no asynchronous copy still writes into the
+// stages when they are reused or when the CTA exits. Iteration i used stage i % stages with phase
+// parity (i / stages) & 1. False if one of them did not land within the limit.
+__device__ __forceinline__ bool mbar_drain(uint64_t* full, int stages, int issued) {
+  bool ok = true;
+  for (int i = issued > stages ? issued - stages : 0; i < issued; ++i)
+    ok = mbar_wait(&full[i % stages], (uint32_t)(i / stages) & 1u) && ok;
+  return ok;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -97,9 +97,11 @@ __global__ void rmsnorm_rows_kernel(float* h, const T* E1, const T* E2, const in
 // written to the fp32 residual. d must be a multiple of 4.
 __global__ void norm_prep_kernel(float* h, const __nv_bfloat16* E1, const __nv_bfloat16* E2, const int32_t* tokens,
                                  const __nv_bfloat16* g, __nv_bfloat16* x, float* ss, int ss_ld, int rows, int B, int d,
-                                 int V, int32_t* status) {
+                                 int V, int32_t* status, unsigned long long* t_start, unsigned long long* t_end) {
   griddep_launch_dependents();
   const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  // in-graph timing (nullable): the step's start and this launch's end
+  if (t_start != nullptr && threadIdx.x == 0) atomicMin(t_start, (unsigned long long)globaltimer());
   if (n >= rows) return;
   const __nv_bfloat16* src = nullptr;
   if (E1 != nullptr) {
@@ -123,6 +125,7 @@ __global__ void norm_prep_kernel(float* h, const __nv_bfloat16* E1, const __nv_b
   }
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (lane == 0) ss[(size_t)n * ss_ld] = s;
+  if (t_end != nullptr && lane == 0) atomicMax(t_end, (unsigned long long)globaltimer());
 }
 
 // Attention-only call without the auxiliary flow: q[0, b, h] = RoPE(q1[b, h]) at position seq_len[b].
@@ -362,7 +365,8 @@ int launch_embed_prep(dualflow_ctx* ctx, const void* E1, const void* E2, const i
   const int rows = aux_on ? 2 * batch : batch;
   norm_prep_kernel<<<(rows + 3) / 4, 128, 0, s>>>(ctx->h, (const __nv_bfloat16*)E1, (const __nv_bfloat16*)E2, tokens,
                                                   (const __nv_bfloat16*)g, (__nv_bfloat16*)ctx->x, ctx->ss, ctx->ss_ld,
-                                                  rows, batch, c.d_model, c.vocab, ctx->status);
+                                                  rows, batch, c.d_model, c.vocab, ctx->status,
+                                                  ctx->cur_stamp ? ctx->stamps : nullptr, ctx->cur_stamp);
   return ok_launch();
 }
 
@@ -371,7 +375,7 @@ int launch_norm_prep(dualflow_ctx* ctx, float* h, const void* g, int batch, int 
   const int rows = aux_on ? 2 * batch : batch;
   norm_prep_kernel<<<(rows + 3) / 4, 128, 0, s>>>(h, nullptr, nullptr, nullptr, (const __nv_bfloat16*)g,
                                                   (__nv_bfloat16*)ctx->x, ctx->ss, ctx->ss_ld, rows, batch,
-                                                  c.d_model, 0, ctx->status);
+                                                  c.d_model, 0, ctx->status, nullptr, ctx->cur_stamp);
   return ok_launch();
 }
 

@@ -153,6 +153,12 @@ DF_API int dualflow_free(dualflow_ctx* ctx);
 /* Static description of a status code; never NULL. */
 DF_API const char* dualflow_status_string(int status);
 
+/* Description of the last CUDA error that a call of this library met in the calling host thread: a
+ * pending CUDA runtime error of the library's own runtime state, else the last failed driver call
+ * of the library (tensor-map encoding), else "no error". Meant for diagnosing a DF_ERR_CUDA status
+ * right after the call that returned it. Never fails; the string is static or thread-local. */
+DF_API const char* dualflow_cuda_error_string(void);
+
 /* Attention-only dual-flow decode of one layer ("Atencao de KV Compartilhada Assimetrica"):
  *   q2 = Wq . h2 + a (*) q1;  RoPE(q1), RoPE(q2) at position seq_len[b];
  *   o_f = softmax(q_f K1^T / sqrt(D)) V1 over the cached positions 0..seq_len[b]-1 of layer `layer`.
@@ -338,15 +344,46 @@ enum {
   DF_PROF_FAMILIES = 8
 };
 
-/* Enables (1) or disables (0, default) per-kernel timing in dualflow_step: every kernel the step
- * launches is bracketed by a CUDA event pair on the launching stream (captured into the step's
- * CUDA graph when graphs are on). Toggling drops the cached graphs. */
-DF_API int dualflow_set_profiling(dualflow_ctx* ctx, int32_t enabled);
+/* Per-kernel timing of dualflow_step (mode 0: off, the default).
+ *   mode 1: every kernel the step launches is bracketed by a CUDA event pair on the launching
+ *           stream (captured into the step's CUDA graph when graphs are on). The event records
+ *           serialise the launches, so a kernel's time includes its full start-up: a stand-alone
+ *           duration, not its share of the pipelined step.
+ *   mode 2: every kernel raises a per-launch device slot to the globaltimer value at which its
+ *           CTAs finish (the step's first kernel also records the step's start); nothing is
+ *           serialised. A launch's time is then its share of the step: from the end of the launch
+ *           before it to its own end, and the shares of one step add up to the step. bf16 storage
+ *           only (DF_ERR_UNSUPPORTED for fp32).
+ * Changing the mode drops the cached graphs. DF_ERR_ARG for another mode. */
+DF_API int dualflow_set_profiling(dualflow_ctx* ctx, int32_t mode);
 
 /* Synchronizes the device and reports the last dualflow_step: launches[f] = kernels of family f
- * it launched (always available) and ms[f] = their summed device time (0 unless profiling was on).
- * Either array may be NULL; n_families entries are written (at most DF_PROF_FAMILIES). */
+ * it launched (always available) and ms[f] = their summed time in the current profiling mode
+ * (all 0 in mode 0). Either array may be NULL; n_families entries are written (at most
+ * DF_PROF_FAMILIES). With graphs on, the last step is the last replay of the last captured graph. */
 DF_API int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches, int32_t n_families);
+
+/* Enables (1) or disables (0, default) NVTX ranges: one per layer of dualflow_step and one per
+ * kernel launch, named after the families above. They are host-side ranges around the launches,
+ * so they show up for eager launches (dualflow_set_graphs(ctx, 0)) and for the capture of a step's
+ * graph, not for its replays. */
+DF_API int dualflow_set_nvtx(dualflow_ctx* ctx, int32_t enabled);
+
+/* Limit, in nanoseconds, of the kernels' bounded pipeline waits (0 restores the default of one
+ * second). Meant for tests of the failure path only: with a limit far below a copy's latency the
+ * waits expire, the step reports DF_ERR_TIMEOUT through dualflow_sync_status and its outputs are
+ * garbage, while every asynchronous copy a kernel issued is still awaited (with the default limit)
+ * before its CTA exits. Changing the limit drops the cached graphs. DF_ERR_ARG if negative. */
+DF_API int dualflow_set_wait_limit(dualflow_ctx* ctx, int64_t limit_ns);
+
+/* Router logits of the context's last MoE computation ("Replay de Roteador", gist.science technical
+ * summary, "Mecanismos Chave": the shared router scores every expert for both flows; the primary
+ * flow's scores choose the experts). Copies device fp32 [n_layers, 2, batch, n_experts] (flow-major
+ * rows as in the step) into the device buffer `logits`: layer l of the last dualflow_step, or of
+ * the last dualflow_coupled_mlp call on layer l. The flow-1 rows of a layer are stale when that
+ * layer last ran with aux_on = 0. batch must equal the one of those calls. DF_ERR_UNSUPPORTED for
+ * dense configurations. Asynchronous on `stream`. */
+DF_API int dualflow_router_logits(dualflow_ctx* ctx, float* logits, int32_t batch, dualflow_stream stream);
 
 /* Synchronizes `stream`, then returns and clears the device status word: DF_OK, or the first
  * DF_ERR_DEVICE_BOUNDS / DF_ERR_TIMEOUT latched by a kernel since the last call. After
@@ -377,11 +414,14 @@ DF_API int dualflow_sync_status(dualflow_ctx* ctx, dualflow_stream stream);
  *   kv      host struct of device pointers, as for dualflow_decode_attention; layer selects k/v
  *   o       device bf16 [2, batch, Hq, D]: o_f = softmax(q_f K1^T / sqrt(D)) V1 over the cached
  *           positions 0..seq_len[b]-1; seq_len[b] == 0 gives o = 0; flow 1 written only if aux_on
- *   status  device int32 or NULL: a device-side bounds error (out-of-range page id or length) is
- *           latched there (set only if it holds 0; the caller clears it). With NULL the code is
- *           latched in the library's array, where the caller cannot read it.
+ *   status  device int32 or NULL: a device-side bounds error (out-of-range page id or length) or
+ *           an expired bounded wait is latched there (set only if it holds 0; the caller clears
+ *           it). With NULL the code is latched in the library's array, where the caller cannot
+ *           read it.
  * The first call on a device (with that device current) looks up the array's device address;
- * make that first call before any stream capture. Every call clears the merge counters it uses
+ * make that first call before any stream capture. The address is kept for the life of the
+ * process: after cudaDeviceReset (or any reset of the device's primary context) the array is
+ * loaded anew, so this call must not be used across such a reset. Every call clears the merge counters it uses
  * with cudaMemsetAsync on `stream`, then launches one kernel there. All calls on a device share
  * the one array, so calls that may overlap on the GPU (other streams, other host threads) race on
  * it and must be serialised by the caller. */

@@ -81,3 +81,33 @@ def test_null_arguments_rejected():
     assert lib.dualflow_prefill(None, None, None, None, 1, 1, None) == dfl.DF_ERR_ARG
     assert lib.dualflow_prefill_slots(None, None, None, None, None, 1, 1, None, None, None) == dfl.DF_ERR_ARG
     assert lib.dualflow_release_slots(None, None, None, 1, None, None, None) == dfl.DF_ERR_ARG
+    assert lib.dualflow_set_nvtx(None, 1) == dfl.DF_ERR_ARG
+    assert lib.dualflow_set_wait_limit(None, 0) == dfl.DF_ERR_ARG
+    assert lib.dualflow_router_logits(None, None, 1, None) == dfl.DF_ERR_ARG
+
+
+def test_noalloc_limit_constant_matches_header():
+    m = re.search(r"#define\s+DF_NOALLOC_MAX_PAIRS\s+(\d+)", open(HEADER).read())
+    assert m and int(m.group(1)) == dfl.DF_NOALLOC_MAX_PAIRS
+
+
+@pytest.mark.parametrize("batch,kv_heads,code", [
+    (65, 8, dfl.DF_ERR_SHAPE),    # 520 pairs: above the static array's limit of 512
+    (513, 1, dfl.DF_ERR_SHAPE),   # 513 pairs
+    (5, 4, dfl.DF_ERR_SHAPE),     # batch above cfg.max_batch
+    (0, 4, dfl.DF_ERR_SHAPE),
+])
+def test_noalloc_rejects_sizes_on_host(batch, kv_heads, code):
+    """The allocation-free attention rejects a batch beyond its static scratch (or the config)
+    before touching the device: the pointers below are never dereferenced."""
+    lib = dfl.load_library()
+    cfg = _good(n_q_heads=2 * kv_heads, n_kv_heads=kv_heads, max_batch=max(batch, 1) if batch != 5 else 4)
+    fake = ctypes.c_void_p(0x1000)  # 16-byte aligned, never read
+    kv = dfl.dualflow_kv()
+    arr = (ctypes.c_void_p * 1)(0x2000)
+    kv.k = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    kv.v = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    kv.seq_len = 0x3000
+    kv.n_layers = 1
+    rc = lib.dualflow_decode_attention_noalloc(ctypes.byref(cfg), fake, ctypes.byref(kv), 0, batch, fake, 1, None, None)
+    assert rc == code

@@ -227,3 +227,153 @@ def test_generate_host_matches_device(cuda_device):
             dfl.dualflow_generate_host(run.ctx, run.weights, run.kv, tok_h, w.batch, 257, out_h, stream=s)
     finally:
         run.close()
+
+
+PEAKED_SIGMA = 0.4  # LM-head weights: logits of a few units, so the next-token distribution is peaked
+
+
+def _peaked_lm(w, dev):
+    """A peaked LM head drawn by the seeded generator: (device bf16 [V, d], host fp64 [V, d])."""
+    import dfsynth
+    t = torch.empty((w.vocab, w.d_model), dtype=torch.bfloat16, device=dev)
+    dfsynth.cuda_normal_(t.data_ptr(), w.seed, "W_lm_peaked", t.numel(), PEAKED_SIGMA, w.dtype)
+    host = O.widen(dfsynth.host_normal(w.seed, "W_lm_peaked", (w.vocab, w.d_model), PEAKED_SIGMA, w.dtype), w.dtype)
+    return t, host.reshape(w.vocab, w.d_model)
+
+
+def _derived_override(gpu_tok, gpu_logits, u, counts):
+    """Token check with a near-tie window derived from the two distributions themselves: the GPU's
+    mixture distribution (from its own logits, in fp64) and the oracle's differ in their cumulative
+    sums by at most dC, so wherever u is farther than dC from both ends of the oracle's interval (or,
+    for argmax, the oracle's top-2 gap exceeds twice the largest probability difference) the GPU's
+    token must equal the oracle's. The slack 1e-5 covers the GPU computing its mixture in fp32."""
+
+    def f(t, b, tok, p):
+        g = int(gpu_tok[t, b])
+        lg = gpu_logits[t, :, b]
+        pg = O.choice_distribution(lg[0], lg[1])
+        if u is None:
+            dp = float(np.max(np.abs(pg - p))) + 1e-5
+            srt = np.sort(p)
+            if srt[-1] - srt[-2] > 2 * dp:
+                counts[0] += 1
+                assert g == tok, f"step {t} row {b}: GPU token {g}, oracle {tok}"
+                return tok
+            assert p[g] >= srt[-1] - 2 * dp, f"step {t} row {b}: GPU token {g} is not a near tie"
+            return g
+        C, Cg = np.cumsum(p), np.cumsum(pg)
+        dC = float(np.max(np.abs(Cg - C))) + 1e-5
+        uu = float(u[t, b])
+        lo = C[g - 1] if g > 0 else 0.0
+        assert lo <= uu + dC and C[g] >= uu - dC, f"step {t} row {b}: GPU sample {g} off the interval"
+        olo = C[tok - 1] if tok > 0 else 0.0
+        if uu - olo > dC and C[tok] - uu > dC:
+            counts[0] += 1
+            assert g == tok, f"step {t} row {b}: GPU sample {g}, oracle {tok}"
+            return tok
+        return g
+    return f
+
+
+@pytest.mark.parametrize("mode", ["greedy", "sampled"])
+def test_generate_peaked_bf16(cuda_device, mode):
+    """bf16 generation with a peaked next-token distribution: every step's logits against the oracle
+    at 2e-2, and the tokens compared exactly outside the derived near-tie window -- at least half of
+    the sampled choices are."""
+    w = CASES["dense_small_g4"][0].replace(batch=4)
+    n = 5
+    dev = cuda_device
+    W_lm_d, W_lm_h = _peaked_lm(w, dev)
+    run = H.DeviceRun(w, dev, overrides={"W_lm": W_lm_d})
+    try:
+        run.rebuild_structs()
+        u = _uniforms(n, w.batch, seed=13) if mode == "sampled" else None
+        gpu_tok, logits_all = _run_gpu(run, w, n, u)
+        assert run.status() == 0
+        got = H.to_f64(logits_all)
+        counts = [0]
+        glob = {"E1": H.LazyRows(w, "E1"), "E2": H.LazyRows(w, "E2"), "W_lm": W_lm_h,
+                "g_final": H.host_f64(w, "g_final")}
+        ref = O.generate(H.hparams(w), glob, H.LazyLayers(w), _oracle_caches(w), run.tokens_np, run.seq_len_np, n,
+                         u=u, aux_on=True, mirror=True, token_override=_derived_override(gpu_tok, got, u, counts))
+        assert np.array_equal(ref["tokens"], gpu_tok)
+        total = n * w.batch
+        print(f"[generate peaked {mode}] tokens compared exactly: {counts[0]}/{total}")
+        assert counts[0] >= total // 2, f"only {counts[0]} of {total} choices compared exactly"
+        for t in range(n):
+            for f in range(2):
+                err = H.rel_err(got[t, f], ref["logits"][t, f])
+                assert err <= 2e-2, f"step {t} flow {f + 1}: rel err {err:.3e}"
+    finally:
+        run.close()
+
+
+def test_generate_paged_matches_oracle(cuda_device):
+    """The decode loop through a shuffled paged cache that grows over the steps, against the
+    oracle's decode loop on a paged cache with the same table: logits at 2e-2, tokens exact outside
+    the near-tie window, and the pages the loop took from the free list."""
+    w = CASES["dense_small_g4"][0]
+    tol, tie = CASES["dense_small_g4"][1:]
+    n = 20
+    run = H.DeviceRun(w, cuda_device)
+    ctx_p = None
+    try:
+        Ks, Vs, table, free, total = _paged_copy(run, w, n, extra=3)
+        cfg = H.config_for(w)
+        cfg.paged, cfg.page_size, cfg.max_pages = 1, 16, total
+        ctx_p = dfl.dualflow_init(cfg)
+        seq_p = torch.from_numpy(run.seq_len_np.copy()).to(cuda_device)
+        table_d = torch.from_numpy(table.copy()).to(cuda_device)
+        kv_p = dfl.make_kv(Ks, Vs, seq_p, table_d)
+        free_d = torch.from_numpy(free.copy()).to(cuda_device)
+        n_free = torch.tensor([len(free)], dtype=torch.int32, device=cuda_device)
+        tok_p = torch.full((n, w.batch), -7, dtype=torch.int32, device=cuda_device)
+        log_p = torch.full((n, 2, w.batch, w.vocab), float("nan"), device=cuda_device)
+        logits = torch.empty((2, w.batch, w.vocab), device=cuda_device)
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            dfl.dualflow_generate(ctx_p, run.weights, kv_p, run.tokens, w.batch, n, tok_p, logits, logits_all=log_p,
+                                  free_pages=free_d, n_free=n_free, stream=s)
+        s.synchronize()
+        assert dfl.dualflow_sync_status(ctx_p) == 0
+        gpu_tok = tok_p.cpu().numpy()
+        # the table the loop must end with, replayed on the host from the documented order (the
+        # page a sequence opens is popped from the top of the free list, sequences in index order)
+        exp_table, exp_free = table.copy(), list(free)
+        L = run.seq_len_np.astype(np.int64).copy()
+        for _ in range(n):
+            for b in range(w.batch):
+                L[b] += 1
+                if L[b] % 16 == 0 and exp_table[b, L[b] // 16] < 0:
+                    exp_table[b, L[b] // 16] = exp_free.pop()
+        assert np.array_equal(table_d.cpu().numpy(), exp_table)
+        # the oracle's paged caches: the cached positions in the pages the table maps, every other
+        # slot unwritten (NaN); the oracle's own appends fill the growth pages of exp_table
+        caches = []
+        for l in range(w.n_layers):
+            Kh = H.host_f64(w, f"L{l}.K").reshape(w.cache_shape())
+            Vh = H.host_f64(w, f"L{l}.V").reshape(w.cache_shape())
+            pk = np.full((total, w.n_kv_heads, 16, w.head_dim), np.nan)
+            pv = np.full_like(pk, np.nan)
+            for b in range(w.batch):
+                for pos in range(int(run.seq_len_np[b])):
+                    pid = int(table[b, pos // 16])
+                    pk[pid][:, pos % 16] = Kh[b][:, pos]
+                    pv[pid][:, pos % 16] = Vh[b][:, pos]
+            caches.append(O.PagedCache(pk, pv, exp_table, 16))
+        counts = [0]
+        glob = {"E1": H.LazyRows(w, "E1"), "E2": H.LazyRows(w, "E2"), "W_lm": H.host_f64(w, "W_lm"),
+                "g_final": H.host_f64(w, "g_final")}
+        ref = O.generate(H.hparams(w), glob, H.LazyLayers(w), caches, run.tokens_np, run.seq_len_np, n,
+                         aux_on=True, mirror=True, token_override=_override(gpu_tok, None, tie, counts))
+        assert np.array_equal(ref["tokens"], gpu_tok)
+        assert counts[0] > 0
+        got = H.to_f64(log_p)
+        for t in range(n):
+            for f in range(2):
+                err = H.rel_err(got[t, f], ref["logits"][t, f])
+                assert err <= tol, f"step {t} flow {f + 1}: rel err {err:.3e}"
+    finally:
+        if ctx_p:
+            dfl.dualflow_free(ctx_p)
+        run.close()

@@ -1,11 +1,24 @@
 """The MoE dual-flow decode step on the GPU against the oracle (router replay, independent fan-outs).
 
-Expert ids are compared bit-exactly with the oracle's own top-k wherever the decision is not a near
-tie. A near tie is two router logits of the primary flow (the k-th and (k+1)-th for the set, two
-neighbours within the top-k for the order) closer than 2e-2 of the largest magnitude: the bf16
-parity tolerance, since the GPU's router logits carry the same bf16-storage error as any other
-output and two logits that close may legitimately swap. The oracle then follows the GPU's ids, so
-that a near tie decided the other way cannot derail the comparison of the logits (tolerance 2e-2)."""
+Routing is checked in three parts, none of which exempts a decision by a chosen threshold:
+
+1. The decision itself, bit-exactly. Every expert id the GPU chose (every layer, row and flow) equals
+   the top-k of the GPU's own fp32 router logits (dualflow_router_logits), ties to the lower index;
+   the auxiliary flow's set is the top-k_aux of the primary logits (replay). The integer decision is
+   taken on the values the kernel decided from, in the kernel's precision.
+2. The logits it is taken from. Each GPU router logit lies within drift_bound(l) * max|r| of the
+   mirrored oracle's for the same row (max|r| = the largest magnitude among that row's oracle
+   logits). The bound grows with the layer index l: the mirrored oracle rounds to bf16 where the GPU
+   stores bf16, but cannot follow a one-ulp rounding flip of a stored operand whose fp32 value sits
+   on a rounding boundary, and those flips accumulate along the residual stream. The bound is the
+   measured growth on B300 (from about 1.4e-3 at the first layer to 4e-2 at the sixteenth of the
+   full workload) with a margin of at least 1.5.
+3. Agreement with the oracle's own decision. Given 2., two experts whose oracle logits differ by more
+   than 2 * drift_bound(l) * max|r| are ordered the same way by the GPU, so outside that window the
+   GPU's ids equal the oracle's own top-k; the share of decisions compared that way is reported.
+
+The oracle then follows the GPU's ids, so that a near tie decided the other way cannot derail the
+comparison of the logits (tolerance 2e-2, against the mirrored and the plain fp64 oracle)."""
 import numpy as np
 import pytest
 import torch
@@ -18,7 +31,17 @@ from tests import gpu_harness as H
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
-TIE = 2e-2
+# Against the plain fp64 oracle (no intermediate bf16 rounding) the error is the bf16 storage error
+# accumulated over the depth: measured on B300 at <= 2.8e-3 for the 1-2 layer cases and 2.4e-2 for
+# the 16-layer workload; the bounds leave a factor of about 1.7 or more.
+TOL_PLAIN = 1e-2
+TOL_PLAIN_DEEP = 4e-2
+DRIFT_PER_LAYER = 5e-3  # drift_bound(l) = DRIFT_PER_LAYER * (l + 1), l = 0-based layer index
+
+
+def drift_bound(l: int) -> float:
+    return DRIFT_PER_LAYER * (l + 1)
+
 
 SMALL = dict(n_layers=2, d_model=256, n_q_heads=4, n_kv_heads=1, ffn_hidden=128, vocab=1000, batch=5, n_experts=6,
              topk_primary=2, topk_aux=3, ctx_len=0, ctx_lo=5, ctx_hi=200, gain_sigma=0.1)
@@ -30,41 +53,67 @@ CASES = {
 }
 
 
-def _ambiguous(r1: np.ndarray, k: int) -> tuple[bool, bool]:
-    """(set, order) ambiguity of the top-k of r1: the k-th and (k+1)-th largest logits are closer
-    than the tie threshold (the set is a near tie), or two neighbours among the first k are (their
-    order is)."""
+def _drift(gpu_r: np.ndarray, ref_r: np.ndarray) -> float:
+    """max_e |gpu_e - ref_e| / max_e |ref_e| of one row of router logits."""
+    return float(np.max(np.abs(gpu_r - ref_r)) / max(np.max(np.abs(ref_r)), 1e-30))
+
+
+def _topk_gpu(r: np.ndarray, k: int) -> list:
+    """Top-k of fp32 logits, largest first, ties to the lower index (the decision the kernel takes)."""
+    r32 = np.asarray(r, dtype=np.float32)
+    return sorted(range(len(r32)), key=lambda i: (-float(r32[i]), i))[:k]
+
+
+def _window_clear(r1: np.ndarray, k: int, tie: float) -> bool:
+    """True when the oracle's top-k of r1 (set and order) is decided by gaps wider than tie * max|r|."""
     s = np.sort(r1)[::-1]
-    thr = TIE * np.abs(r1).max()
-    set_amb = k < len(r1) and s[k - 1] - s[k] < thr
-    order_amb = bool(np.any(s[: k - 1] - s[1:k] < thr)) if k > 1 else False
-    return set_amb, order_amb
+    thr = tie * np.abs(r1).max()
+    if k < len(r1) and s[k - 1] - s[k] <= thr:
+        return False
+    return not (k > 1 and bool(np.any(s[: k - 1] - s[1:k] <= thr)))
 
 
-def _same_ids(gpu: np.ndarray, r1: np.ndarray, k: int) -> bool:
-    """The GPU's k experts agree with the oracle's top-k of r1 where the decision is not a near tie:
-    as an ordered list, or as a set when only the order is a near tie. Near-tie sets pass."""
-    set_amb, order_amb = _ambiguous(r1, k)
-    ref = list(O.topk_lower_index(r1, k))
-    if set_amb:
-        return True
-    if order_amb:
-        return sorted(gpu[:k]) == sorted(ref)
-    return list(gpu[:k]) == ref
-
-
-def _check_ids(w, gpu_ids, ref, rows):
-    """gpu_ids [nL, 2, B, kmax]; ref: oracle step result (router logits [nL, 2, R, E], ids). Returns
-    how many (layer, row) decisions were unambiguous and compared exactly."""
+def _check_decisions(w, gid, grl, ref_rlog, rows, layer_of=lambda l: l):
+    """gid [nL, 2, B, kmax] GPU ids; grl [nL, 2, B, E] GPU router logits; ref_rlog [nL, 2, R, E]
+    oracle router logits for rows[i]. Asserts parts 1-3 of the module docstring; returns (largest
+    drift relative to its bound, decisions compared with the oracle's own, all decisions)."""
     k1, k2 = w.topk_primary, w.topk_aux
-    exact = 0
-    for l in range(w.n_layers):
+    worst, agreed, total = 0.0, 0, 0
+    for l in range(gid.shape[0]):
+        lb = layer_of(l)
         for i, b in enumerate(rows):
-            r1 = ref["router_logits"][l, 0, i]
-            assert _same_ids(gpu_ids[l, 0, b], r1, k1), f"layer {l} row {b} primary ids {gpu_ids[l, 0, b]}"
-            assert _same_ids(gpu_ids[l, 1, b], r1, k2), f"layer {l} row {b} aux ids {gpu_ids[l, 1, b]}"
-            exact += not any(_ambiguous(r1, k1) + _ambiguous(r1, k2))
-    return exact
+            g1 = _topk_gpu(grl[l, 0, b], max(k1, k2))
+            assert list(gid[l, 0, b, :k1]) == g1[:k1], f"layer {lb} row {b}: primary ids {gid[l, 0, b]} vs {g1[:k1]}"
+            assert list(gid[l, 1, b, :k2]) == g1[:k2], f"layer {lb} row {b}: auxiliary ids {gid[l, 1, b]} vs {g1[:k2]}"
+            d = max(_drift(grl[l, f, b], ref_rlog[l, f, i]) for f in range(2))
+            assert d <= drift_bound(lb), f"layer {lb} row {b}: router logits drift {d:.3e} > {drift_bound(lb):.3e}"
+            worst = max(worst, d / drift_bound(lb))
+            r1 = ref_rlog[l, 0, i]
+            total += 1
+            if _window_clear(r1, k1, 2 * drift_bound(lb)) and _window_clear(r1, k2, 2 * drift_bound(lb)):
+                agreed += 1
+                assert list(gid[l, 0, b, :k1]) == list(O.topk_lower_index(r1, k1)), f"layer {lb} row {b} primary"
+                assert list(gid[l, 1, b, :k2]) == list(O.topk_lower_index(r1, k2)), f"layer {lb} row {b} auxiliary"
+    return worst, agreed, total
+
+
+def _check_routing(run, w, gid, ref, rows, label):
+    """The routing checks (module docstring) on a whole step's decisions."""
+    rlog = torch.full((w.n_layers, 2, w.batch, w.n_experts), float("nan"), device=run.dev)
+    dfl.dualflow_router_logits(run.ctx, rlog, w.batch)
+    worst, agreed, total = _check_decisions(w, gid, rlog.cpu().numpy(), ref["router_logits"], rows)
+    print(f"[moe {label}] routing: every id = top-k of the GPU's router logits; drift at most {worst:.2f} of its "
+          f"bound; {agreed}/{total} decisions also compared with the oracle's own")
+
+
+def _check_plain(w, got, rows, override, label, tol=TOL_PLAIN):
+    """The GPU's logits (got [2, len(rows), V]) against the unmirrored oracle: the plain fp64
+    definition with the same expert ids."""
+    plain = H.oracle_step(w, rows=rows, mirror=False, ids_override=override)
+    for f in range(2):
+        err = H.rel_err(got[f], plain["logits"][f])
+        print(f"[moe {label}] flow {f + 1} logits vs unmirrored oracle: rel err {err:.3e}")
+        assert err <= tol, f"flow {f + 1} vs the unmirrored oracle: rel err {err:.3e} > {tol:.0e}"
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -84,12 +133,14 @@ def test_moe_step_parity(cuda_device, name):
         for l in range(w.n_layers):
             for b in rows:
                 assert set(gid[l, 0, b, :w.topk_primary]) <= set(gid[l, 1, b, :w.topk_aux])
-        ref = H.oracle_step(w, rows=rows, ids_override=lambda l, b: (gid[l, 0, b], gid[l, 1, b]))
-        assert _check_ids(w, gid, ref, rows) > 0
+        override = lambda l, b: (gid[l, 0, b], gid[l, 1, b])  # noqa: E731
+        ref = H.oracle_step(w, rows=rows, ids_override=override)
+        _check_routing(run, w, gid, ref, rows, name)
         got = H.to_f64(run.logits)
         for f in range(2):
             err = H.rel_err(got[f], ref["logits"][f])
             assert err <= TOL, f"flow {f + 1}: rel err {err:.3e}"
+        _check_plain(w, got, rows, override, name)
         # primary-only step (it rewrites the same primary entry at slot L_b): primary logits and
         # primary expert ids bit-identical
         dual = run.logits.clone()
@@ -117,19 +168,26 @@ def test_moe_coupled_mlp_parity(cuda_device):
         dfl.dualflow_coupled_mlp(run.ctx, h, run.weights, 1, B, 1, ids)
         assert run.status() == 0
         gid = ids.cpu().numpy()
+        rl = torch.full((w.n_layers, 2, B, w.n_experts), float("nan"), device=cuda_device)
+        dfl.dualflow_router_logits(run.ctx, rl, B)
+        grl = rl.cpu().numpy()[1:2]  # layer 1
         got = H.to_f64(h) - h0.astype(np.float64)
         hp = H.hparams(w)
         P = H.LazyLayers(w)[1]
-        checked = 0
+        ref_rlog = np.zeros((1, 2, B, w.n_experts))
         for b in range(B):
             x = [O.dualflow_oracle._normed(h0[f, b].astype(np.float64), P["g_mlp"], hp, True) for f in range(2)]
-            y, oid, (r1, _) = O.dualflow_oracle._moe_mlp(hp, P, x, True, True, (gid[0, b], gid[1, b]))
-            assert _same_ids(gid[0, b], r1, w.topk_primary) and _same_ids(gid[1, b], r1, w.topk_aux), f"row {b} ids"
-            checked += not any(_ambiguous(r1, w.topk_primary) + _ambiguous(r1, w.topk_aux))
+            y, oid, (r1, r2) = O.dualflow_oracle._moe_mlp(hp, P, x, True, True, (gid[0, b], gid[1, b]))
+            ref_rlog[0, 0, b], ref_rlog[0, 1, b] = r1, r2
             for f in range(2):
                 err = H.rel_err(got[f, b], y[f])
                 assert err <= TOL, f"row {b}, flow {f + 1}: rel err {err:.3e}"
-        assert checked > 0
+        # the same inputs on both sides: the router logits agree to fp32 accumulation order
+        drift = max(_drift(grl[0, f, b], ref_rlog[0, f, b]) for f in range(2) for b in range(B))
+        assert drift <= 1e-5, f"router logits drift {drift:.3e} on identical inputs"
+        worst, agreed, total = _check_decisions(w, gid[None], grl, ref_rlog, list(range(B)), layer_of=lambda l: 0)
+        print(f"[moe coupled_mlp] router-logit drift {drift:.3e}; {agreed}/{total} decisions compared with the "
+              f"oracle's own")
     finally:
         run.close()
 
@@ -156,7 +214,7 @@ def test_moe_full_16l_b64_sampled(cuda_device):
     """The full MoE workload (16 layers, 16 experts, top-2 / top-4, B = 64, L = 4096) in the launch
     configuration of the benchmark (captured graph on a stream), on sampled sequences."""
     w = W.MOE_16L_B64
-    rows = [0, 21, 63]
+    rows = [0, 21, 40, 63]
     run = H.DeviceRun(w, cuda_device)
     try:
         s = torch.cuda.Stream()
@@ -169,11 +227,13 @@ def test_moe_full_16l_b64_sampled(cuda_device):
         dfl.dualflow_expert_ids(run.ctx, ids, w.batch)
         torch.cuda.synchronize()
         gid = ids.cpu().numpy()
-        ref = H.oracle_step(w, rows=rows, ids_override=lambda l, b: (gid[l, 0, b], gid[l, 1, b]))
-        _check_ids(w, gid, ref, rows)
+        override = lambda l, b: (gid[l, 0, b], gid[l, 1, b])  # noqa: E731
+        ref = H.oracle_step(w, rows=rows, ids_override=override)
+        _check_routing(run, w, gid, ref, rows, "full_16l_b64")
         got = H.to_f64(run.logits)[:, rows]
         for f in range(2):
             err = H.rel_err(got[f], ref["logits"][f])
             assert err <= TOL, f"flow {f + 1}: rel err {err:.3e}"
+        _check_plain(w, got, rows, override, "full_16l_b64", TOL_PLAIN_DEEP)
     finally:
         run.close()

@@ -1,6 +1,14 @@
 """The whole dual-flow decode step (dualflow_step) against the oracle, plus the method's invariants
 checked on the GPU: primary bit-identical with and without the auxiliary flow, cache untouched
-outside slot L_b, auxiliary == primary when the flows are uncoupled and share the embedding."""
+outside slot L_b, auxiliary == primary when the flows are uncoupled and share the embedding.
+
+The parity bar is taken against the oracle's mirror mode, which rounds to bf16 exactly where the
+GPU path stores bf16. The error against the plain fp64 definition (no intermediate rounding) is
+also reported and bounded: for bf16 storage it is the storage error accumulated over the depth
+(measured on B300 at <= 2.8e-3 for the 1-2 layer cases and 1.7e-2 for the 24-layer workload; bounds
+1e-2 and 4e-2), for fp32 storage it stays within the fp32 bar of 1e-5."""
+TOL_PLAIN_BF16 = 1e-2
+TOL_PLAIN_DEEP = 4e-2
 import numpy as np
 import pytest
 import torch
@@ -29,6 +37,16 @@ def _check_logits(run, w, rows, tol, ref):
         if w.dtype == "f32":
             r = ref["logits"][f]
             assert np.all(np.abs(got[f] - r) <= 1e-5 * np.abs(r) + 1e-6 * np.abs(r).max())
+
+
+def _check_plain(run, w, rows, tol, label):
+    """Logits against the unmirrored oracle: the plain fp64 definition of the step."""
+    plain = H.oracle_step(w, rows=rows, mirror=False)
+    got = H.to_f64(run.logits)[:, rows]
+    for f in range(2):
+        err = H.rel_err(got[f], plain["logits"][f])
+        print(f"[step {label}] flow {f + 1} logits vs unmirrored oracle: rel err {err:.3e}")
+        assert err <= tol, f"flow {f + 1} vs the unmirrored oracle: rel err {err:.3e}"
 
 
 def _check_cache(run, w, rows, tol, ref, before):
@@ -60,6 +78,7 @@ def test_step_parity(cuda_device, name):
         ref = H.oracle_step(w, rows=rows)
         _check_logits(run, w, rows, tol, ref)
         _check_cache(run, w, rows, tol, ref, before)
+        _check_plain(run, w, rows, tol if w.dtype == "f32" else TOL_PLAIN_BF16, name)
         logits_dual = run.logits.clone()
         caches_dual = {k: run.t[k].clone() for k in before}
         # primary-only step on the same inputs: primary logits and cache bit-identical
@@ -155,6 +174,7 @@ def test_step_full_dense_24l_sampled(cuda_device):
         ref = H.oracle_step(w, rows=rows)
         _check_logits(run, w, rows, 2e-2, ref)
         _check_cache(run, w, rows, 2e-2, ref, None)
+        _check_plain(run, w, rows, TOL_PLAIN_DEEP, "full_24l_b32")
     finally:
         run.close()
 

@@ -2,11 +2,12 @@
 memory (their own pool owns it all, or cudaMalloc's device-wide synchronisation is not allowed on
 their path), so cannot create a context. Its scratch lives in a static device array of the library.
 
-Each case calls the allocation-free entry point twice in a row, through the C ABI, on the queries
-that dualflow_decode_attention forms internally (q2 = Wq.h2 + a (*) q1, both rotated to position
-seq_len[b] and stored bf16), and compares both outputs with that entry point's output at the bf16
-tolerance of the other attention tests. The file sorts last so that a stop at the first failure
-has already run every other test."""
+Each case calls the allocation-free entry point twice in a row, through the C ABI, on both flows'
+queries as the oracle forms them (q2 = Wq.h2 + a (*) q1, both rotated to position seq_len[b] and
+rounded to bf16), and compares both outputs with the oracle's attention at the bf16 tolerance of the
+other attention tests, and with the context entry point's output on the same workload. One case fills
+the array's limit (batch * n_kv_heads = 512 pairs). The file sorts last so that a stop at the first
+failure has already run every other test."""
 import numpy as np
 import pytest
 import torch
@@ -23,6 +24,8 @@ SMALL = dict(d_model=256, n_q_heads=8, n_kv_heads=2, batch=6, ctx_len=0, ctx_lo=
 CASES = {
     "contiguous_ragged": W.ATTN_B8_L2048.replace(**SMALL),
     "paged16_ragged": W.PAGED_RAGGED_B64.replace(**dict(SMALL, ctx_lo=1, ctx_hi=700, d_model=512)),
+    # the limit of the static array: 64 sequences x 8 KV heads = 512 (sequence, KV head) pairs
+    "paged16_512_pairs": W.PAGED_RAGGED_B64.replace(**dict(ctx_lo=1, ctx_hi=200)),
 }
 
 
@@ -40,13 +43,15 @@ def _rotated_queries(w, dev) -> torch.Tensor:
 
 
 @pytest.mark.parametrize("name", list(CASES))
-def test_noalloc_matches_context_entry_point(cuda_device, name):
+def test_noalloc_matches_oracle(cuda_device, name):
     w = CASES[name]
+    assert w.batch * w.n_kv_heads <= dfl.DF_NOALLOC_MAX_PAIRS
     run = H.DeviceRun(w, cuda_device)
     try:
+        ref = H.oracle_attention(w)  # [2, B, Hq, D], mirrored bf16 storage points
         run.attention(aux_on=1)
         assert run.status() == 0
-        ref = H.to_f64(run.o)
+        ctx_out = H.to_f64(run.o)
         q = _rotated_queries(w, cuda_device)
         cfg = H.config_for(w)
         status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
@@ -58,6 +63,8 @@ def test_noalloc_matches_context_entry_point(cuda_device, name):
             got = H.to_f64(o)
             for f in range(2):
                 err = H.rel_err(got[f], ref[f])
-                assert err <= TOL_BF16, f"call {call}, flow {f + 1}: rel err {err:.3e}"
+                assert err <= TOL_BF16, f"call {call}, flow {f + 1}: rel err {err:.3e} vs the oracle"
+                err = H.rel_err(got[f], ctx_out[f])
+                assert err <= TOL_BF16, f"call {call}, flow {f + 1}: rel err {err:.3e} vs the context entry point"
     finally:
         run.close()
