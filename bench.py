@@ -143,6 +143,41 @@ def step_bytes(w, experts_touched=None) -> dict:
                 kv_write=kv_write, attention_per_launch=attn)
 
 
+def family_bytes(w, experts_touched=None) -> dict:
+    """Algorithmic HBM bytes per step of each kernel family of the decode step (the unit a family's
+    roofline is taken on): its weights once (for MoE, the router and every touched expert's
+    weights), the activations it reads and writes once, and for attention every cached K1/V1 entry
+    once. Sums to at least step_bytes()['total'] (the activations are counted here only)."""
+    es = 2
+    B, d, F, V = w.batch, w.d_model, w.ffn_hidden, w.vocab
+    M = 2 * B
+    qd, kvd = w.q_dim, w.kv_dim
+    nL = w.n_layers
+    sb = step_bytes(w, experts_touched)
+    out = {
+        "norm": M * d * es + M * d * 4 + M * d * es,  # embedding rows, residual, first norm operand
+        "qkv": nL * ((qd + 2 * kvd) * d * es + M * d * es + M * qd * es + B * 2 * kvd * es),
+        "attention": nL * sb["attention_per_launch"],
+        "o_proj": nL * (d * qd * es + M * qd * es + 2 * M * d * 4 + M * d * es),
+        "lm_head": V * d * es + M * d * es + M * V * 4,
+    }
+    if w.n_experts == 0:
+        out["gate_up"] = nL * (2 * F * d * es + M * d * es + M * F * es)
+        out["down"] = nL * (d * F * es + M * F * es + 2 * M * d * 4 + M * d * es)
+    else:
+        E = w.n_experts
+        touched = list(experts_touched) if experts_touched is not None else [E] * nL
+        kmax = max(w.topk_primary, w.topk_aux)
+        out["gate_up"] = sum(E * d * es + M * E * 4 + t_ * 2 * F * d * es + M * d * es + M * kmax * F * es
+                             for t_ in touched)
+        out["down"] = sum(t_ * d * F * es + M * kmax * F * es + M * kmax * d * 4 + 2 * M * d * 4 + M * d * es
+                          for t_ in touched)
+    return out
+
+
+FAMILY_LAUNCHES = {"norm": 1, "lm_head": 1}  # per step; the per-layer families launch once per layer
+
+
 def call_bytes(w) -> dict:
     """Algorithmic HBM bytes of one attention-only call: Wq once, K1/V1 of the cached positions
     once, q1 and h2 read, both flows' outputs written."""
@@ -306,13 +341,86 @@ class OracleSample:
                 f"full step by sequences and by (layers + 1)")
 
 
-def blas_threads() -> int:
+def host_cpu() -> dict:
+    """The host's CPU model and the cores this process may run on."""
+    model = "unknown"
     try:
-        from threadpoolctl import threadpool_info
-        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
-        return int(max(n)) if n else 1
-    except Exception:
-        return 1
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    return {"model": model, "cores": cores}
+
+
+def _openblas_calls():
+    """(set_num_threads, get_num_threads) of the OpenBLAS that numpy loaded, found through its
+    exported C entry points (the symbol names carry a suffix in numpy's own build), or None."""
+    import ctypes
+    paths = set()
+    try:
+        with open("/proc/self/maps") as f:
+            for line in f:
+                if "openblas" in line.lower() and ".so" in line:
+                    paths.add(line.split()[-1])
+    except OSError:
+        return None
+    names = ("scipy_openblas_set_num_threads64_", "openblas_set_num_threads64_", "scipy_openblas_set_num_threads",
+             "openblas_set_num_threads")
+    for path in sorted(paths):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for n in names:
+            if hasattr(lib, n):
+                getter = getattr(lib, n.replace("set_num_threads", "get_num_threads"), None)
+                setter = getattr(lib, n)
+                setter.argtypes, setter.restype = [ctypes.c_int], None
+                if getter is not None:
+                    getter.argtypes, getter.restype = [], ctypes.c_int
+                return setter, getter
+    return None
+
+
+class OracleThreads:
+    """Runs the oracle with its BLAS library on every core this process may use (the oracle's
+    matrix products are where its time goes); `threads` is the count in effect inside, read back
+    from the library."""
+
+    def __enter__(self):
+        np.zeros(1) @ np.zeros(1)  # numpy's BLAS is loaded
+        self.cores = host_cpu()["cores"]
+        self._restore = None
+        calls = _openblas_calls()
+        if calls is not None:
+            setter, getter = calls
+            before = getter() if getter is not None else None
+            setter(self.cores)
+            self.threads = getter() if getter is not None else self.cores
+            if before is not None:
+                self._restore = lambda: setter(before)
+        else:
+            self.threads = 1
+        return self
+
+    def __exit__(self, *exc):
+        if self._restore is not None:
+            self._restore()
+        return False
+
+
+def cpu_baseline_entry(value: float, unit: str, threads: int, sample: str, sample_s: float) -> dict:
+    cpu = host_cpu()
+    return {"value": value, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample,
+            "sample_seconds": sample_s, "host_cpu": cpu["model"], "host_cores": cpu["cores"],
+            "parallelism": f"the oracle's BLAS calls on {threads} threads (numpy fp64); its Python loops on one"}
 
 
 class AttentionOracleSample:
@@ -352,55 +460,59 @@ class AttentionOracleSample:
 
 
 def run_reference(args, w) -> dict:
-    """The reference arm: the CPU oracle, as it stands, on a bounded sample per step (one sequence,
-    rotating through the batch, over the first layer and the LM head; for an attention-only
-    workload, one sequence's attention call)."""
-    per = []
-    if args.workload in ("prefill", "prefill_moe"):
-        samp = PrefillOracleSample(w, 8, PREFILL_TOKENS)
-        for i in range(args.warmup + args.steps):
-            t = samp.time()
-            if i >= args.warmup:
-                per.append(samp.full(t))
-        s = statistics.median(per)
-        value = w.batch * PREFILL_TOKENS / s
-        unit = "prefill tokens/s"
-        return {"impl": "reference", "metric": "primary-only prefill tokens/s at 1 B300", "value": value, "unit": unit,
-                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3,
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": f"prefill_{w.name}", "batch": w.batch, "prompt_tokens": PREFILL_TOKENS,
-                           "layers": w.n_layers},
-                "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle",
-                                 "sample": samp.describe()},
-                "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    if w.kind == "attention":
-        lens = w.seq_lens()
-        order = [int(b) for b in np.argsort(lens)[: max(1, min(8, w.batch))]]  # the shortest: bounded time
-        samp = AttentionOracleSample(w, order)
-        for i in range(args.warmup + args.steps):
-            rows = [order[i % len(order)]]
-            t = samp.time_rows(rows)
-            if i >= args.warmup:
-                per.append(samp.full_call(t, rows))
-        desc = samp.describe(order)
-    else:
-        rows = list(range(min(8, w.batch)))
-        samp = OracleSample(w, rows, 1)
-        for i in range(args.warmup + args.steps):
-            t = samp.time_step([rows[i % len(rows)]])
-            if i >= args.warmup:
-                per.append(samp.full_step(t, 1))
-        desc = samp.describe(1)
+    """The reference arm: the CPU oracle, as it stands, on the host's cores (its BLAS calls on every
+    usable core), one bounded sample per step -- one sequence, rotating through the batch, over the
+    first layer and the LM head; for an attention-only workload one sequence's attention call; for
+    prefill one sequence's first prompt tokens over one layer. Each sample's seconds are measured;
+    the line's time per step is those seconds scaled to the whole workload (extrapolated, stated as
+    such in the line)."""
+    per, raw = [], []
+    with OracleThreads() as th:
+        if args.workload in ("prefill", "prefill_moe"):
+            samp = PrefillOracleSample(w, 8, PREFILL_TOKENS)
+            for i in range(args.warmup + args.steps):
+                t = samp.time()
+                if i >= args.warmup:
+                    raw.append(t)
+                    per.append(samp.full(t))
+            desc = samp.describe()
+        elif w.kind == "attention":
+            lens = w.seq_lens()
+            order = [int(b) for b in np.argsort(lens)[: max(1, min(8, w.batch))]]  # the shortest: bounded time
+            samp = AttentionOracleSample(w, order)
+            for i in range(args.warmup + args.steps):
+                rows = [order[i % len(order)]]
+                t = samp.time_rows(rows)
+                if i >= args.warmup:
+                    raw.append(t)
+                    per.append(samp.full_call(t, rows))
+            desc = samp.describe(order)
+        else:
+            rows = list(range(min(8, w.batch)))
+            samp = OracleSample(w, rows, 1)
+            for i in range(args.warmup + args.steps):
+                t = samp.time_step([rows[i % len(rows)]])
+                if i >= args.warmup:
+                    raw.append(t)
+                    per.append(samp.full_step(t, 1))
+            desc = samp.describe(1)
     s = statistics.median(per)
-    value = w.batch / s
-    cores = blas_threads()
-    unit = "tokens/s" if w.kind == "step" else "sequence-steps/s (one layer)"
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch, "ctx": w.ctx_len or f"{w.ctx_lo}-{w.ctx_hi}",
-                       "layers": w.n_layers},
-            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": desc},
+    if args.workload in ("prefill", "prefill_moe"):
+        metric, unit, value = "primary-only prefill tokens/s at 1 B300", "prefill tokens/s", w.batch * PREFILL_TOKENS / s
+        config = {"workload": f"prefill_{w.name}", "batch": w.batch, "prompt_tokens": PREFILL_TOKENS, "layers": w.n_layers}
+    else:
+        metric, value = METRIC, w.batch / s
+        unit = "tokens/s" if w.kind == "step" else "sequence-steps/s (one layer)"
+        config = {"workload": w.name, "batch": w.batch, "ctx": w.ctx_len or f"{w.ctx_lo}-{w.ctx_hi}",
+                  "layers": w.n_layers}
+    return {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": s * 1e3,
+            "ms_per_step_kind": "extrapolated: the median timed sample scaled to the whole workload's step",
+            "sample_ms": {"median": statistics.median(raw) * 1e3, "min": min(raw) * 1e3, "max": max(raw) * 1e3,
+                          "n": len(raw)},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config,
+            "cpu_baseline": cpu_baseline_entry(value, unit, th.threads, desc, statistics.median(raw)),
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -490,7 +602,9 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
     lens = w.seq_lens()
     rows = [int(b) for b in np.argsort(lens)[:2]]
     samp = AttentionOracleSample(w, rows)
-    cpu_s = samp.full_call(samp.time_rows(rows), rows)
+    with OracleThreads() as th:
+        raw_s = statistics.median(samp.time_rows(rows) for _ in range(3))
+    cpu_s = samp.full_call(raw_s, rows)
     unit = "sequence-steps/s (one layer)"
     return {
         "metric": METRIC, "value": reps.rate(w.batch, ms * 1e-3), "unit": unit, "n_gpus": world,
@@ -509,8 +623,7 @@ def run_ours_attention(args, w, rank: int, world: int, local_rank: int) -> dict 
                      "bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "bytes_per_launch": nb["total"],
                      "avg_launch_ms": ms, "traffic": None},
-        "cpu_baseline": {"value": w.batch / cpu_s, "unit": unit, "cores": blas_threads(), "kind": "oracle",
-                         "sample": samp.describe(rows)},
+        "cpu_baseline": cpu_baseline_entry(w.batch / cpu_s, unit, th.threads, samp.describe(rows), raw_s),
         "e2e": {"value": reps.rate(w.batch, e2e_s), "unit": unit,
                 "h2d_bytes_per_step": int((q1_h.numel() + h2_h.numel()) * 2), "d2h_bytes_per_step": int(o_h.numel() * 2),
                 "api": "dualflow_decode_attention with q1, h2 copied from pinned host memory and o copied back, "
@@ -592,7 +705,9 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
         peak, kind = 1400.0, "fallback sustained bf16"
     tflops = flops / (ms * 1e-3) / 1e12
     samp = PrefillOracleSample(w, 8, n_tok)
-    cpu_s = samp.full(samp.time())
+    with OracleThreads() as th:
+        raw_s = statistics.median(samp.time() for _ in range(3))
+    cpu_s = samp.full(raw_s)
     return {
         "metric": "primary-only prefill tokens/s at 1 B300", "value": reps.rate(w.batch * n_tok, ms * 1e-3),
         "unit": "prefill tokens/s",
@@ -608,8 +723,8 @@ def run_ours_prefill(args, w, rank: int, world: int, local_rank: int) -> dict | 
                                   else "gate/up, down})"),
                      "bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
                      "peak_kind": kind, "flops_per_step": flops, "traffic": None},
-        "cpu_baseline": {"value": w.batch * n_tok / cpu_s, "unit": "prefill tokens/s", "cores": blas_threads(),
-                         "kind": "oracle", "sample": samp.describe()},
+        "cpu_baseline": cpu_baseline_entry(w.batch * n_tok / cpu_s, "prefill tokens/s", th.threads, samp.describe(),
+                                           raw_s),
         "e2e": {"value": reps.rate(w.batch * n_tok, e2e_s), "unit": "prefill tokens/s", "h2d_bytes_per_step": int(prompt_np.nbytes),
                 "d2h_bytes_per_step": 0,
                 "api": "dualflow_prefill with the prompt copied from pinned host memory, stream sync per call"},
@@ -692,19 +807,27 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     except Exception as exc:  # the distribution is a report only: never lose the run over it
         dist_steps = {"error": str(exc)[:200]}
 
-    # per-kernel times inside the step (event pairs captured into the step's graph)
-    dfl.dualflow_set_profiling(run.ctx, 1)
-    fam_ms = [0.0] * dfl.DF_PROF_FAMILIES
-    fam_n = [0] * dfl.DF_PROF_FAMILIES
+    # per-kernel times inside the step: mode 2 = each launch's share of the pipelined step (device
+    # end stamps, nothing serialised); mode 1 = CUDA event pairs around every launch (serialising:
+    # each kernel's stand-alone duration, start-up included)
     nprof = max(min(args.steps, 50), 3)
-    with torch.cuda.stream(stream):
-        for i in range(3 + nprof):
-            run.step(aux_on=1, stream=stream)
-            t, n = dfl.dualflow_profile_read(run.ctx)
-            if i >= 3:
-                fam_ms = [a + b for a, b in zip(fam_ms, t)]
-                fam_n = [a + b for a, b in zip(fam_n, n)]
-    dfl.dualflow_set_profiling(run.ctx, 0)
+
+    def profile(mode):
+        dfl.dualflow_set_profiling(run.ctx, mode)
+        fm = [0.0] * dfl.DF_PROF_FAMILIES
+        fn = [0] * dfl.DF_PROF_FAMILIES
+        with torch.cuda.stream(stream):
+            for i in range(3 + nprof):
+                run.step(aux_on=1, stream=stream)
+                tt, nn = dfl.dualflow_profile_read(run.ctx)
+                if i >= 3:
+                    fm = [a + b for a, b in zip(fm, tt)]
+                    fn = [a + b for a, b in zip(fn, nn)]
+        dfl.dualflow_set_profiling(run.ctx, 0)
+        return fm, fn
+
+    fam_ms_graph, _ = profile(2)
+    fam_ms, fam_n = profile(1)
 
     # end to end through the host-buffer decode call a user makes: the step's input tokens copied in
     # from pinned host memory, one decode step (step, mixture head, token choice, length advance),
@@ -776,9 +899,26 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
     att_ms = fam_ms[dfl.PROF_NAMES.index("attention")] / max(fam_n[dfl.PROF_NAMES.index("attention")], 1)
     att_gbs = nb["attention_per_launch"] / (att_ms * 1e-3) / 1e9
     prof_total = sum(fam_ms) / nprof
-    samp = OracleSample(w, [0, 1, 2, 3], 6)
-    cpu_s = samp.full_step(samp.time_step([0, 1, 2, 3]), 4)
-    cpu_desc = samp.describe(4)
+    graph_total = sum(fam_ms_graph) / nprof
+    fb = family_bytes(w, experts_touched)
+    families = {}
+    for i, name in enumerate(dfl.PROF_NAMES):
+        if not fam_n[i] or name not in fb:
+            continue
+        per_step = fam_n[i] // nprof
+        ms_g, ms_s = fam_ms_graph[i] / nprof, fam_ms[i] / nprof
+        gbs_g, gbs_s = fb[name] / (ms_g * 1e-3) / 1e9, fb[name] / (ms_s * 1e-3) / 1e9
+        families[name] = {"launches_per_step": per_step, "bytes_per_step": fb[name],
+                          "bytes_per_launch": fb[name] / per_step,
+                          "in_graph": {"ms_per_step": ms_g, "share": ms_g / graph_total, "achieved_gbs": gbs_g,
+                                       "frac": gbs_g / peak},
+                          "serialised": {"ms_per_step": ms_s, "achieved_gbs": gbs_s, "frac": gbs_s / peak}}
+    cpu_rows = list(range(min(8, w.batch)))
+    samp = OracleSample(w, cpu_rows, min(6, w.n_layers))
+    with OracleThreads() as th:
+        raw_s = statistics.median(samp.time_step(cpu_rows) for _ in range(3))
+    cpu_s = samp.full_step(raw_s, len(cpu_rows))
+    cpu_desc = samp.describe(len(cpu_rows)) + " (median of 3 timings)"
     launches_per_step = int(sum(launches))
     res = {
         "metric": METRIC, "value": reps.rate(w.batch, ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
@@ -800,12 +940,20 @@ def run_ours(args, w, rank: int, world: int, local_rank: int) -> dict | None:
                      "achieved": att_gbs, "peak": peak, "unit": "GB/s", "frac": att_gbs / peak,
                      "peak_kind": f"{peak_kind} copy bandwidth", "bytes_per_launch": nb["attention_per_launch"],
                      "avg_launch_ms": att_ms,
+                     "timing": "CUDA event pair around every launch in the replayed graph (serialising)",
+                     "in_graph_achieved": families["attention"]["in_graph"]["achieved_gbs"],
+                     "in_graph_frac": families["attention"]["in_graph"]["frac"],
                      # the committed ncu capture is of the dense workload's attention launch
                      "traffic": attention_traffic() if w.name == workload("dense").name else None},
-        "kernel_ms_per_step": {n: fam_ms[i] / nprof for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
-        "kernel_share": {n: fam_ms[i] / nprof / prof_total for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
-        "cpu_baseline": {"value": w.batch / cpu_s, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                         "sample": cpu_desc},
+        "roofline_families": {
+            "note": ("per kernel family, against the measured copy bandwidth: in_graph = the family's share of the "
+                     "pipelined step (device end stamps, dualflow_set_profiling mode 2; shares add up to the step), "
+                     "serialised = CUDA event pairs around every launch (mode 1; each launch's stand-alone time)"),
+            "peak_gbs": peak, "families": families},
+        "kernel_ms_per_step": {n: fam_ms_graph[i] / nprof for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
+        "kernel_ms_per_step_serialised": {n: fam_ms[i] / nprof for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
+        "kernel_share": {n: fam_ms_graph[i] / nprof / graph_total for i, n in enumerate(dfl.PROF_NAMES) if fam_n[i]},
+        "cpu_baseline": cpu_baseline_entry(w.batch / cpu_s, "tokens/s", th.threads, cpu_desc, raw_s),
         "e2e": {"value": reps.rate(w.batch, e2e_s), "unit": "tokens/s", "h2d_bytes_per_step": int(tok.numel() * 4),
                 "d2h_bytes_per_step": int((out if w.paged else tok_out).numel() * 4),
                 "api": ("dualflow_step_host (pinned host tokens in, host logits out, sync per step)" if w.paged else

@@ -79,3 +79,42 @@ def test_step_percentiles_nearest_rank():
     got = bench.step_percentiles(t)
     assert got == {"n": 50, "p10_ms": 5.0, "p50_ms": 25.0, "p90_ms": 45.0}
     assert bench.step_percentiles([7.0]) == {"n": 1, "p10_ms": 7.0, "p50_ms": 7.0, "p90_ms": 7.0}
+
+
+def test_dense_family_bytes_by_hand():
+    """Each kernel family's roofline numerator: its weights once, its activations in and out once,
+    and for attention the KV of every layer; the weights of the families add up to the step's."""
+    w = W.DENSE_24L_B32_L4096
+    d, Hq, Hkv, D, F, V, nL, B = 2048, 16, 4, 128, 8192, 32000, 24, 32
+    M, es = 2 * B, 2
+    fb = bench.family_bytes(w)
+    assert fb["qkv"] == nL * ((Hq + 2 * Hkv) * D * d * es + M * d * es + M * Hq * D * es + B * 2 * Hkv * D * es)
+    assert fb["o_proj"] == nL * (d * Hq * D * es + M * Hq * D * es + 2 * M * d * 4 + M * d * es)
+    assert fb["gate_up"] == nL * (2 * F * d * es + M * d * es + M * F * es)
+    assert fb["down"] == nL * (d * F * es + M * F * es + 2 * M * d * 4 + M * d * es)
+    assert fb["lm_head"] == V * d * es + M * d * es + M * V * 4
+    assert fb["attention"] == nL * bench.step_bytes(w)["attention_per_launch"]
+    weights = nL * ((Hq + 2 * Hkv) * D * d + d * Hq * D + 2 * F * d + d * F) * es + V * d * es
+    activations = (nL * (M * d * es + M * Hq * D * es + B * 2 * Hkv * D * es)
+                   + nL * (M * Hq * D * es + 2 * M * d * 4 + M * d * es) + nL * (M * d * es + M * F * es)
+                   + nL * (M * F * es + 2 * M * d * 4 + M * d * es) + M * d * es + M * V * 4)
+    assert sum(fb[k] for k in ("qkv", "o_proj", "gate_up", "down", "lm_head")) == weights + activations
+    # weights read per step by the families = the step's weight bytes except gains and coupling vectors
+    small = nL * (2 * d + Hq * D + F + d) * es + d * es
+    assert bench.step_bytes(w)["weights"] == weights + small
+
+
+def test_moe_family_bytes_count_touched_experts():
+    w = W.MOE_16L_B64
+    full = bench.family_bytes(w)
+    half = bench.family_bytes(w, experts_touched=[w.n_experts // 2] * w.n_layers)
+    F, d = w.ffn_hidden, w.d_model
+    assert full["gate_up"] - half["gate_up"] == w.n_layers * (w.n_experts // 2) * 2 * F * d * 2
+    assert full["down"] - half["down"] == w.n_layers * (w.n_experts // 2) * d * F * 2
+
+
+def test_host_cpu_reports_cores():
+    cpu = bench.host_cpu()
+    assert cpu["cores"] >= 1 and isinstance(cpu["model"], str)
+    with bench.OracleThreads() as th:
+        assert 1 <= th.threads <= max(cpu["cores"], 1)
