@@ -171,13 +171,20 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
     }
   }
   // This CTA's tiles. Contiguous: global tiles [t0, t1). Per pair: CTA c takes tiles j0, j0 + kpp,
-  // ... of pair c / kpp (j0 = c % kpp), so the pair's first tiles are every CTA's first tiles. The
-  // owners of a pair's partials are the same CTAs in both cases (owner_of below).
+  // ... of pair c % pairs (j0 = c / pairs), so the pair's first tiles are every CTA's first tiles,
+  // and the CTAs that share a pair are far apart in launch order: the CTAs that become resident
+  // first (while the preceding kernel still holds SMs) are spread over the pairs instead of making
+  // up whole pairs (measured on B300: -9 us per 24-layer dense step). c_eff = pair * kpp + j0 is
+  // the CTA's place in the order of the contiguous cut, which numbers the pair's partial slots and
+  // its merge order (owner_of below) in both cases.
   const long long t0 = (c < C) ? T * c / C : 0, t1 = (c < C) ? T * (c + 1) / C : 0;
   int n_my = (int)(t1 - t0);
+  int c_eff = c;
   Walker w0;
   if (kpp > 0) {
-    const int pr = c / kpp, j0 = c % kpp, per = (c < C) ? tiles_of(sched, pr / Hkv, Hkv) : 0;
+    const int pairs = B * Hkv;
+    const int pr = c % pairs, j0 = c / pairs, per = (c < C) ? tiles_of(sched, pr / Hkv, Hkv) : 0;
+    c_eff = pr * kpp + j0;
     n_my = (c < C && j0 < per) ? (per - j0 + kpp - 1) / kpp : 0;
     w0.b = pr / Hkv;
     w0.g = pr % Hkv;
@@ -489,7 +496,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
             }
           }
         } else {
-          float* slot = P.part + (size_t)(p + c) * kAttnPartFloats;
+          float* slot = P.part + (size_t)(p + c_eff) * kAttnPartFloats;
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
