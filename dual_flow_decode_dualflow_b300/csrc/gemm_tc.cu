@@ -121,6 +121,19 @@ __device__ __forceinline__ void rope4(const float2* cs, float4 x, float4 xp, flo
                    rot_hi(x.w, xp.w, c1.z, c1.w));
 }
 
+// Epilogue operands of one (row, quad) unit loaded before the accumulator is ready (see the kernel).
+struct EpiPre {
+  float4 y1[2], y2[2], c[2], g[2];  // residual rows / rotary angles (QKV: y1 = cos/sin pairs), coupling, gain
+  int pos;                          // QKV: the row's position
+};
+
+__device__ __forceinline__ void rope4_pre(float4 c0, float4 c1, float4 x, float4 xp, float4& lo, float4& hi) {
+  lo = make_float4(rot_lo(x.x, xp.x, c0.x, c0.y), rot_lo(x.y, xp.y, c0.z, c0.w), rot_lo(x.z, xp.z, c1.x, c1.y),
+                   rot_lo(x.w, xp.w, c1.z, c1.w));
+  hi = make_float4(rot_hi(x.x, xp.x, c0.x, c0.y), rot_hi(x.y, xp.y, c0.z, c0.w), rot_hi(x.z, xp.z, c1.x, c1.y),
+                   rot_hi(x.w, xp.w, c1.z, c1.w));
+}
+
 __device__ __forceinline__ size_t cache_slot(const GemmArgs& a, int b, int hk, int pos, int32_t* status, bool* ok) {
   *ok = true;
   if (pos < 0 || pos >= a.max_ctx) {
@@ -424,6 +437,63 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   }
   __syncwarp();
 
+  const bool scaled = a.ss_in != nullptr;
+  const bool norm_out = (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD) && a.g_next != nullptr;
+  // units of work: (activation row, quad); paired epilogues take the primary row and its auxiliary row
+  const bool paired = EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV || EPI == EPI_MOE_GATEUP;
+  const int rows = (EPI == EPI_Q2) ? a.m_a : paired ? a.m_p : m;
+
+  // ---- epilogue operands that do not depend on the accumulator ----
+  // When every thread has at most one (row, quad) unit (the decode launches), its operands -- residual
+  // rows, the next norm's gain, the coupling vector, the rotary angles -- are final once the preceding
+  // kernel has completed, so they are loaded now, while the MMAs finish, instead of after the split-K
+  // exchange; the epilogue then waits for the partials alone.
+  EpiPre pre;
+  const bool pre_ok = !RB && rows * nq <= kThreads &&
+                      (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV);
+  if (pre_ok && (int)threadIdx.x < rows * nq) {
+    griddep_wait();  // the operands were written by preceding kernels
+    const int n = threadIdx.x / nq, qd = threadIdx.x % nq;
+    const int fa = lo0 + 4 * qd, fg = tile * kGemmTileN + fa;
+    if (EPI == EPI_ADD_F32 && norm_out) {
+      const float* y = reinterpret_cast<const float*>(a.y) + (size_t)n * a.ldy;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        if (fg + 64 * hh < a.n_out) {
+          pre.y1[hh] = *reinterpret_cast<const float4*>(y + fg + 64 * hh);
+          pre.g[hh] = ld_bf16x4(a.g_next, fg + 64 * hh);
+        }
+    } else if (EPI == EPI_COUPLE_ADD) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int f = fg + 64 * hh;
+        if (p.vec_ok && f + 3 < a.n_out) {
+          pre.y1[hh] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.y) + (size_t)n * a.ldy + f);
+          if (a.m_a > 0) {
+            pre.y2[hh] =
+                *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.y) + (size_t)(a.m_p + n) * a.ldy + f);
+            pre.c[hh] = ld_bf16x4(a.vec, f);
+          }
+          if (norm_out) pre.g[hh] = ld_bf16x4(a.g_next, f);
+        }
+      }
+    } else if (EPI == EPI_SWIGLU) {
+      if (a.m_a > 0) pre.c[0] = ld_bf16x4(a.vec, tile * 64 + fa);
+    } else if (EPI == EPI_QKV) {
+      const int pos = a.seq_len[n];
+      pre.pos = pos;
+      if (pos >= 0 && pos <= a.max_ctx) {
+        const float2* cs = a.rope + (size_t)pos * 64 + fa;
+        pre.y1[0] = *reinterpret_cast<const float4*>(cs);
+        pre.y1[1] = *reinterpret_cast<const float4*>(cs + 2);
+      }
+      if (tile < a.n_q_heads && a.m_a > 0) {
+        pre.c[0] = ld_bf16x4(a.vec, tile * kHeadDim + fa);
+        pre.c[1] = ld_bf16x4(a.vec, tile * kHeadDim + fa + 64);
+      }
+    }
+  }
+
   // ---- accumulator: TMEM -> registers -> shared memory (S == 1) or the exchange area ----
   const bool acc_ok = mbar_wait(done, 0);
   tc_fence_after();
@@ -440,11 +510,6 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   red.gstride = (int)cta_floats;
   red.S = S;
   red.nl = nl;
-  const bool scaled = a.ss_in != nullptr;
-  const bool norm_out = (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD) && a.g_next != nullptr;
-  // units of work: (activation row, quad); paired epilogues take the primary row and its auxiliary row
-  const bool paired = EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV || EPI == EPI_MOE_GATEUP;
-  const int rows = (EPI == EPI_Q2) ? a.m_a : paired ? a.m_p : m;
   // S == 1 with a tile larger than the pipeline bytes (row-blocked launches on a small budget): the
   // accumulator is drained and its epilogue run in passes of `chunk` rows (no auxiliary rows there)
   const int chunk = (RB && S == 1 && p.chunk > 0) ? p.chunk : p.n_pad;
@@ -512,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
         for (int hh = 0; hh < 2; ++hh) {
           const int f = fg + 64 * hh;
           if (f >= a.n_out) continue;
-          const float4 hv = f4_add(*reinterpret_cast<const float4*>(y + f), hh ? hi : lo);
+          const float4 hv = f4_add(pre_ok ? pre.y1[hh] : *reinterpret_cast<const float4*>(y + f), hh ? hi : lo);
           *reinterpret_cast<float4*>(y + f) = hv;
-          st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(hv, ld_bf16x4(a.g_next, f)));
+          st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(hv, pre_ok ? pre.g[hh] : ld_bf16x4(a.g_next, f)));
           ss0 = f4_sumsq_acc(ss0, hv);
         }
       } else if (EPI == EPI_COUPLE_ADD) {
@@ -534,16 +599,17 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
           const float4 z2 = hh ? z2hi : z2lo;
           if (p.vec_ok && f + 3 < a.n_out) {
             float* y1 = reinterpret_cast<float*>(a.y) + (size_t)n * a.ldy + f;
-            const float4 h1 = f4_add(*reinterpret_cast<const float4*>(y1), z1);
+            const float4 h1 = f4_add(pre_ok ? pre.y1[hh] : *reinterpret_cast<const float4*>(y1), z1);
             *reinterpret_cast<float4*>(y1) = h1;
             float4 h2 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (a.m_a > 0) {
               float* y2 = reinterpret_cast<float*>(a.y) + (size_t)(a.m_p + n) * a.ldy + f;
-              h2 = f4_add(*reinterpret_cast<const float4*>(y2), f4_fma(ld_bf16x4(a.vec, f), z1, z2));
+              h2 = f4_add(pre_ok ? pre.y2[hh] : *reinterpret_cast<const float4*>(y2),
+                          f4_fma(pre_ok ? pre.c[hh] : ld_bf16x4(a.vec, f), z1, z2));
               *reinterpret_cast<float4*>(y2) = h2;
             }
             if (norm_out) {
-              const float4 g = ld_bf16x4(a.g_next, f);
+              const float4 g = pre_ok ? pre.g[hh] : ld_bf16x4(a.g_next, f);
               st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(h1, g));
               ss0 = f4_sumsq_acc(ss0, h1);
               if (a.m_a > 0) {
@@ -602,19 +668,22 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
             g2 = f4_scale(g2, r);
             p2 = f4_scale(p2, r);
           }
-          st_bf16x4(a.y, (size_t)(a.m_p + n) * a.ldy + j, f4_fma(ld_bf16x4(a.vec, j), u1, f4_silu_mul(g2, p2)));
+          st_bf16x4(a.y, (size_t)(a.m_p + n) * a.ldy + j,
+                    f4_fma(pre_ok && base == 0 ? pre.c[0] : ld_bf16x4(a.vec, j), u1, f4_silu_mul(g2, p2)));
         }
       } else if (EPI == EPI_QKV) {
         const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, B = a.m_p, b = n;
-        const int pos = a.seq_len[b];
+        const int pos = pre_ok ? pre.pos : a.seq_len[b];
         if (pos < 0 || pos > a.max_ctx) {
           set_status(p.status, DF_ERR_DEVICE_BOUNDS);
         } else {
           const float2* cs = a.rope + (size_t)pos * 64 + fa;
+          const float4 cs0 = pre_ok ? pre.y1[0] : *reinterpret_cast<const float4*>(cs);
+          const float4 cs1 = pre_ok ? pre.y1[1] : *reinterpret_cast<const float4*>(cs + 2);
           float4 r_lo, r_hi;
           if (tile < Hq) {
             const int h = tile;
-            rope4(cs, lo, hi, r_lo, r_hi);
+            rope4_pre(cs0, cs1, lo, hi, r_lo, r_hi);
             const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
             st_bf16x4(a.q_out, o1 + fa, r_lo);
             st_bf16x4(a.q_out, o1 + fa + 64, r_hi);
@@ -626,9 +695,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
                 x2 = f4_scale(x2, r);
                 x2p = f4_scale(x2p, r);
               }
-              x2 = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa), lo, x2);
-              x2p = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa + 64), hi, x2p);
-              rope4(cs, x2, x2p, r_lo, r_hi);
+              x2 = f4_fma(pre_ok ? pre.c[0] : ld_bf16x4(a.vec, h * kHeadDim + fa), lo, x2);
+              x2p = f4_fma(pre_ok ? pre.c[1] : ld_bf16x4(a.vec, h * kHeadDim + fa + 64), hi, x2p);
+              rope4_pre(cs0, cs1, x2, x2p, r_lo, r_hi);
               const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
               st_bf16x4(a.q_out, o2 + fa, r_lo);
               st_bf16x4(a.q_out, o2 + fa + 64, r_hi);
@@ -641,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
             if (ok) {
               void* cache = is_k ? a.k_cache : a.v_cache;
               if (is_k) {
-                rope4(cs, lo, hi, r_lo, r_hi);
+                rope4_pre(cs0, cs1, lo, hi, r_lo, r_hi);
               } else {
                 r_lo = lo;
                 r_hi = hi;

@@ -42,8 +42,11 @@ CASES = {
 }
 
 
-def _check_logits(run, w, rows, tol, ref):
+def _check_logits(run, w, rows, tol, ref, label=""):
     got = H.to_f64(run.logits)[:, rows]
+    if label:
+        print(f"[step {label}] logits vs mirrored oracle: rel err "
+              + " / ".join(f"{H.rel_err(got[f], ref['logits'][f]):.3e}" for f in range(2)))
     for f in range(2):
         err = H.rel_err(got[f], ref["logits"][f])
         assert err <= tol, f"flow {f + 1} logits: rel err {err:.3e}"
@@ -191,7 +194,7 @@ def test_step_full_dense_24l_sampled(cuda_device):
         s.synchronize()
         assert run.status() == 0
         ref = H.oracle_step(w, rows=rows)
-        _check_logits(run, w, rows, 2e-2, ref)
+        _check_logits(run, w, rows, 2e-2, ref, "full_24l_b32")
         _check_cache(run, w, rows, CACHE_DRIFT, ref, None, "full_24l_b32")
         _check_plain(run, w, rows, TOL_PLAIN_DEEP, "full_24l_b32")
     finally:
