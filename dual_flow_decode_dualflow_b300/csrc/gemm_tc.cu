@@ -551,7 +551,40 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   }
   red.base = acc_s - (size_t)cb * kGemmTileN;  // row n of this pass at acc_s[(n - cb) * 128]
   const int r_end = min(cb + chunk, rows);
-  const int units = r_end > cb ? (r_end - cb) * nq : 0;
+  int units = r_end > cb ? (r_end - cb) * nq : 0;
+  if (EPI == EPI_SWIGLU && !RB && S > 1 && units <= 2 * kThreads) {
+    // gate/up of a split launch with up to two units per thread: every partial load of both units
+    // is issued before any of their arithmetic, so the exchange costs one round trip to L2
+    float4 lo[2], hi[2], g2[2], p2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int it = u * kThreads + threadIdx.x, n = it / nq, qd = it % nq;
+      if (it < units) {
+        reduce_pair(red, lo0, n, qd, lo[u], hi[u]);
+        if (a.m_a > 0) reduce_pair(red, lo0, a.m_p + n, qd, g2[u], p2[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int it = u * kThreads + threadIdx.x, n = it / nq, qd = it % nq;
+      if (it >= units) continue;
+      const int j = tile * 64 + lo0 + 4 * qd;  // hidden unit: gate at tile feature fa, up at fa + 64
+      if (scaled) {
+        lo[u] = f4_scale(lo[u], rstd_s[n]);
+        hi[u] = f4_scale(hi[u], rstd_s[n]);
+      }
+      const float4 u1 = f4_silu_mul(lo[u], hi[u]);
+      st_bf16x4(a.y, (size_t)n * a.ldy + j, u1);
+      if (a.m_a > 0) {
+        if (scaled) {
+          g2[u] = f4_scale(g2[u], rstd_s[a.m_p + n]);
+          p2[u] = f4_scale(p2[u], rstd_s[a.m_p + n]);
+        }
+        st_bf16x4(a.y, (size_t)(a.m_p + n) * a.ldy + j, f4_fma(ld_bf16x4(a.vec, j), u1, f4_silu_mul(g2[u], p2[u])));
+      }
+    }
+    units = 0;  // done: the loop below has nothing left
+  }
   for (int base = 0; base < units; base += kThreads) {
     const int it = base + threadIdx.x;
     const bool live = it < units;
