@@ -829,8 +829,12 @@ int dualflow_decode_attention(dualflow_ctx* ctx, const void* q1, const void* h2,
   const dualflow_config& c = ctx->cfg;
   cudaStream_t s = S(stream);
   if (c.dtype == DF_DTYPE_BF16) {
+    // On a caller's stream the two launches are chained by programmatic dependent launch, as in
+    // the step: the attention requests its first K/V stages while the query projection runs.
+    const int pdl = s != nullptr ? 1 : 0;
     if (aux_on) {
       GemmArgs g = gemm_args(ctx);
+      g.pdl = pdl;
       g.x = h2;
       g.W = Wq;
       g.n_out = c.n_q_heads * c.head_dim;
@@ -848,7 +852,7 @@ int dualflow_decode_attention(dualflow_ctx* ctx, const void* q1, const void* h2,
     }
     AttnArgs at = attn_args(ctx, kv, layer, batch, 0, aux_on);
     at.o = o;
-    return launch_attention_bf16(ctx, at, s);
+    return launch_attention_bf16(ctx, at, s, pdl);
   }
   if (aux_on)
     DF_TRY(launch_linear_f32(ctx, (const float*)h2, batch, (const float*)Wq, c.n_q_heads * c.head_dim, c.d_model,
