@@ -239,6 +239,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(prod_done + 1);
   float* rstd_s = reinterpret_cast<float*>(tmem_slot + 4);  // [256] 1 / rms of each activation row
   int* sel_s = reinterpret_cast<int*>(rstd_s + kGemmMaxAct);  // [256] grouped: row selected this expert
+  // grouped: the rows whose epilogue has work (the expert's rows), in row order; their count is
+  // tmem_slot[3]
+  int* sel_list = sel_s + kGemmMaxAct;
   // S == 1: after the main loop the pipeline bytes hold the accumulator tile acc[n][128]
   float* acc_s = reinterpret_cast<float*>(smem);
 
@@ -407,8 +410,27 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     // idle during the main loop: which rows selected this launch's expert (grouped launches) and
     // 1 / rms of every activation row, from the producer's partials
     griddep_wait();
-    if (a.sel_pos != nullptr)
+    if (a.sel_pos != nullptr) {
       for (int n = threadIdx.x - 64; n < m; n += 64) sel_s[n] = a.sel_pos[(size_t)n * a.n_groups + grp] >= 0;
+      if (warp == 2) {
+        // the epilogue's rows: gate/up pairs primary row n with auxiliary row m_p + n and has work
+        // when either selected the expert; down has one unit row per activation row
+        const int nr = EPI == EPI_MOE_GATEUP ? a.m_p : m;
+        int cnt = 0;
+        for (int b0 = 0; b0 < nr; b0 += 32) {
+          const int n = b0 + lane;
+          bool s = false;
+          if (n < nr) {
+            s = a.sel_pos[(size_t)n * a.n_groups + grp] >= 0;
+            if (EPI == EPI_MOE_GATEUP && a.m_a > 0) s = s || a.sel_pos[(size_t)(a.m_p + n) * a.n_groups + grp] >= 0;
+          }
+          const unsigned bal = __ballot_sync(0xffffffffu, s);
+          if (s) sel_list[cnt + __popc(bal & ((1u << lane) - 1u))] = n;
+          cnt += __popc(bal);
+        }
+        if (lane == 0) tmem_slot[3] = (uint32_t)cnt;
+      }
+    }
     for (int n = threadIdx.x - 64; a.ss_in != nullptr && n < m; n += 64) {
       const float* row = a.ss_in + (size_t)n * a.ss_ld;
       float ss = 0.f;
@@ -552,6 +574,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   red.base = acc_s - (size_t)cb * kGemmTileN;  // row n of this pass at acc_s[(n - cb) * 128]
   const int r_end = min(cb + chunk, rows);
   int units = r_end > cb ? (r_end - cb) * nq : 0;
+  // grouped expert launches (one pass, no split): only the rows that selected the expert
+  constexpr bool kListed = EPI == EPI_MOE_GATEUP || EPI == EPI_MOE_DOWN;
+  const bool listed = kListed && !RB && S == 1 && a.sel_pos != nullptr;
+  if (listed) units = (int)tmem_slot[3] * nq;
   if (EPI == EPI_SWIGLU && !RB && S > 1 && units <= 2 * kThreads) {
     // gate/up of a split launch with up to two units per thread: every partial load of both units
     // is issued before any of their arithmetic, so the exchange costs one round trip to L2
@@ -588,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   for (int base = 0; base < units; base += kThreads) {
     const int it = base + threadIdx.x;
     const bool live = it < units;
-    const int n = live ? cb + it / nq : 0, qd = it % nq;
+    const int n = live ? (listed ? sel_list[it / nq] : cb + it / nq) : 0, qd = it % nq;
     const int fa = lo0 + 4 * qd;        // tile feature of the low quad
     const int fg = tile * kGemmTileN + fa;
     float ss0 = 0.f, ss1 = 0.f;         // norm outputs: sum of h^2 of row n (and its auxiliary row)
@@ -985,7 +1011,7 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
   }
   const int parts = p.splits == 1 ? 512 * (p.chunk > 0 ? p.chunk : p.n_pad) : 0;
   p.region = ((pipe > parts ? pipe : parts) + 1023) & ~1023;
-  const size_t smem = 1024 + (size_t)p.region + 256 + kGemmMaxAct * 8;  // barriers, TMEM slot, row arrays
+  const size_t smem = 1024 + (size_t)p.region + 256 + kGemmMaxAct * 12;  // barriers, TMEM slot, row arrays
   if (a.row_blocked) {
     switch (a.epi) {
       case EPI_STORE_F32: return launch_epi<EPI_STORE_F32, true>(mw, mx, mpf, p, smem, s);
