@@ -221,8 +221,10 @@ template <int EPI>
 constexpr int min_ctas_per_sm() { return (EPI == EPI_MOE_GATEUP || EPI == EPI_MOE_DOWN) ? 3 : 2; }
 
 // RB: the row-blocked (prefill) instantiation, whose accumulator may be drained in passes; the
-// others drain it in one pass, with that loop resolved at compile time.
-template <int EPI, bool RB>
+// others drain it in one pass, with that loop resolved at compile time. PRE2: the O and QKV
+// projections of a batch of 64, whose epilogue has two units per thread, preload both units'
+// operands (a separate instantiation: the registers it takes slow the one-unit launches).
+template <int EPI, bool RB, bool PRE2 = false>
 __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_pf, const GemmParams p) {
@@ -470,48 +472,53 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   // rows, the next norm's gain, the coupling vector, the rotary angles -- are final once the preceding
   // kernel has completed, so they are loaded now, while the MMAs finish, instead of after the split-K
   // exchange; the epilogue then waits for the partials alone.
-  EpiPre pre;
-  const bool pre_ok = !RB && rows * nq <= kThreads &&
+  EpiPre pre[2];
+  constexpr int pre_units = (PRE2 && (EPI == EPI_ADD_F32 || EPI == EPI_QKV)) ? 2 : 1;
+  const bool pre_ok = !RB && rows * nq <= pre_units * kThreads &&
                       (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV);
-  if (pre_ok && (int)threadIdx.x < rows * nq) {
-    griddep_wait();  // the operands were written by preceding kernels
-    const int n = threadIdx.x / nq, qd = threadIdx.x % nq;
+  if (pre_ok && (int)threadIdx.x < rows * nq) griddep_wait();  // the operands were written by preceding kernels
+#pragma unroll
+  for (int u = 0; u < pre_units; ++u) {
+    const int it = u * kThreads + threadIdx.x;
+    if (!pre_ok || it >= rows * nq) continue;
+    EpiPre& pre_w = pre[u];
+    const int n = it / nq, qd = it % nq;
     const int fa = lo0 + 4 * qd, fg = tile * kGemmTileN + fa;
     if (EPI == EPI_ADD_F32 && norm_out) {
       const float* y = reinterpret_cast<const float*>(a.y) + (size_t)n * a.ldy;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
         if (fg + 64 * hh < a.n_out) {
-          pre.y1[hh] = *reinterpret_cast<const float4*>(y + fg + 64 * hh);
-          pre.g[hh] = ld_bf16x4(a.g_next, fg + 64 * hh);
+          pre_w.y1[hh] = *reinterpret_cast<const float4*>(y + fg + 64 * hh);
+          pre_w.g[hh] = ld_bf16x4(a.g_next, fg + 64 * hh);
         }
     } else if (EPI == EPI_COUPLE_ADD) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int f = fg + 64 * hh;
         if (p.vec_ok && f + 3 < a.n_out) {
-          pre.y1[hh] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.y) + (size_t)n * a.ldy + f);
+          pre_w.y1[hh] = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.y) + (size_t)n * a.ldy + f);
           if (a.m_a > 0) {
-            pre.y2[hh] =
+            pre_w.y2[hh] =
                 *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.y) + (size_t)(a.m_p + n) * a.ldy + f);
-            pre.c[hh] = ld_bf16x4(a.vec, f);
+            pre_w.c[hh] = ld_bf16x4(a.vec, f);
           }
-          if (norm_out) pre.g[hh] = ld_bf16x4(a.g_next, f);
+          if (norm_out) pre_w.g[hh] = ld_bf16x4(a.g_next, f);
         }
       }
     } else if (EPI == EPI_SWIGLU) {
-      if (a.m_a > 0) pre.c[0] = ld_bf16x4(a.vec, tile * 64 + fa);
+      if (a.m_a > 0) pre_w.c[0] = ld_bf16x4(a.vec, tile * 64 + fa);
     } else if (EPI == EPI_QKV) {
       const int pos = a.seq_len[n];
-      pre.pos = pos;
+      pre_w.pos = pos;
       if (pos >= 0 && pos <= a.max_ctx) {
         const float2* cs = a.rope + (size_t)pos * 64 + fa;
-        pre.y1[0] = *reinterpret_cast<const float4*>(cs);
-        pre.y1[1] = *reinterpret_cast<const float4*>(cs + 2);
+        pre_w.y1[0] = *reinterpret_cast<const float4*>(cs);
+        pre_w.y1[1] = *reinterpret_cast<const float4*>(cs + 2);
       }
       if (tile < a.n_q_heads && a.m_a > 0) {
-        pre.c[0] = ld_bf16x4(a.vec, tile * kHeadDim + fa);
-        pre.c[1] = ld_bf16x4(a.vec, tile * kHeadDim + fa + 64);
+        pre_w.c[0] = ld_bf16x4(a.vec, tile * kHeadDim + fa);
+        pre_w.c[1] = ld_bf16x4(a.vec, tile * kHeadDim + fa + 64);
       }
     }
   }
@@ -613,6 +620,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   }
   for (int base = 0; base < units; base += kThreads) {
     const int it = base + threadIdx.x;
+    // this iteration's preloaded operands (with two units, a select, so that both stay in registers)
+    EpiPre pu_sel;
+    if constexpr (pre_units > 1) pu_sel = base != 0 ? pre[1] : pre[0];
+    const EpiPre& pu = pre_units > 1 ? pu_sel : pre[0];
     const bool live = it < units;
     const int n = live ? (listed ? sel_list[it / nq] : cb + it / nq) : 0, qd = it % nq;
     const int fa = lo0 + 4 * qd;        // tile feature of the low quad
@@ -636,9 +647,9 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
         for (int hh = 0; hh < 2; ++hh) {
           const int f = fg + 64 * hh;
           if (f >= a.n_out) continue;
-          const float4 hv = f4_add(pre_ok ? pre.y1[hh] : *reinterpret_cast<const float4*>(y + f), hh ? hi : lo);
+          const float4 hv = f4_add(pre_ok ? pu.y1[hh] : *reinterpret_cast<const float4*>(y + f), hh ? hi : lo);
           *reinterpret_cast<float4*>(y + f) = hv;
-          st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(hv, pre_ok ? pre.g[hh] : ld_bf16x4(a.g_next, f)));
+          st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(hv, pre_ok ? pu.g[hh] : ld_bf16x4(a.g_next, f)));
           ss0 = f4_sumsq_acc(ss0, hv);
         }
       } else if (EPI == EPI_COUPLE_ADD) {
@@ -658,17 +669,17 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
           const float4 z2 = hh ? z2hi : z2lo;
           if (p.vec_ok && f + 3 < a.n_out) {
             float* y1 = reinterpret_cast<float*>(a.y) + (size_t)n * a.ldy + f;
-            const float4 h1 = f4_add(pre_ok ? pre.y1[hh] : *reinterpret_cast<const float4*>(y1), z1);
+            const float4 h1 = f4_add(pre_ok ? pu.y1[hh] : *reinterpret_cast<const float4*>(y1), z1);
             *reinterpret_cast<float4*>(y1) = h1;
             float4 h2 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (a.m_a > 0) {
               float* y2 = reinterpret_cast<float*>(a.y) + (size_t)(a.m_p + n) * a.ldy + f;
-              h2 = f4_add(pre_ok ? pre.y2[hh] : *reinterpret_cast<const float4*>(y2),
-                          f4_fma(pre_ok ? pre.c[hh] : ld_bf16x4(a.vec, f), z1, z2));
+              h2 = f4_add(pre_ok ? pu.y2[hh] : *reinterpret_cast<const float4*>(y2),
+                          f4_fma(pre_ok ? pu.c[hh] : ld_bf16x4(a.vec, f), z1, z2));
               *reinterpret_cast<float4*>(y2) = h2;
             }
             if (norm_out) {
-              const float4 g = pre_ok ? pre.g[hh] : ld_bf16x4(a.g_next, f);
+              const float4 g = pre_ok ? pu.g[hh] : ld_bf16x4(a.g_next, f);
               st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(h1, g));
               ss0 = f4_sumsq_acc(ss0, h1);
               if (a.m_a > 0) {
@@ -728,17 +739,17 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
             p2 = f4_scale(p2, r);
           }
           st_bf16x4(a.y, (size_t)(a.m_p + n) * a.ldy + j,
-                    f4_fma(pre_ok && base == 0 ? pre.c[0] : ld_bf16x4(a.vec, j), u1, f4_silu_mul(g2, p2)));
+                    f4_fma(pre_ok ? pu.c[0] : ld_bf16x4(a.vec, j), u1, f4_silu_mul(g2, p2)));
         }
       } else if (EPI == EPI_QKV) {
         const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, B = a.m_p, b = n;
-        const int pos = pre_ok ? pre.pos : a.seq_len[b];
+        const int pos = pre_ok ? pu.pos : a.seq_len[b];
         if (pos < 0 || pos > a.max_ctx) {
           set_status(p.status, DF_ERR_DEVICE_BOUNDS);
         } else {
           const float2* cs = a.rope + (size_t)pos * 64 + fa;
-          const float4 cs0 = pre_ok ? pre.y1[0] : *reinterpret_cast<const float4*>(cs);
-          const float4 cs1 = pre_ok ? pre.y1[1] : *reinterpret_cast<const float4*>(cs + 2);
+          const float4 cs0 = pre_ok ? pu.y1[0] : *reinterpret_cast<const float4*>(cs);
+          const float4 cs1 = pre_ok ? pu.y1[1] : *reinterpret_cast<const float4*>(cs + 2);
           float4 r_lo, r_hi;
           if (tile < Hq) {
             const int h = tile;
@@ -754,8 +765,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
                 x2 = f4_scale(x2, r);
                 x2p = f4_scale(x2p, r);
               }
-              x2 = f4_fma(pre_ok ? pre.c[0] : ld_bf16x4(a.vec, h * kHeadDim + fa), lo, x2);
-              x2p = f4_fma(pre_ok ? pre.c[1] : ld_bf16x4(a.vec, h * kHeadDim + fa + 64), hi, x2p);
+              x2 = f4_fma(pre_ok ? pu.c[0] : ld_bf16x4(a.vec, h * kHeadDim + fa), lo, x2);
+              x2p = f4_fma(pre_ok ? pu.c[1] : ld_bf16x4(a.vec, h * kHeadDim + fa + 64), hi, x2p);
               rope4_pre(cs0, cs1, x2, x2p, r_lo, r_hi);
               const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
               st_bf16x4(a.q_out, o2 + fa, r_lo);
@@ -857,10 +868,10 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   }
 }
 
-template <int EPI, bool RB = false>
+template <int EPI, bool RB = false, bool PRE2 = false>
 int launch_epi(const CUtensorMap& mw, const CUtensorMap& mx, const CUtensorMap& mpf, const GemmParams& p, size_t smem,
                cudaStream_t s) {
-  auto kern = gemm_tc_kernel<EPI, RB>;
+  auto kern = gemm_tc_kernel<EPI, RB, PRE2>;
   if (set_smem_attrs_once(reinterpret_cast<const void*>(kern)) != DF_OK) return DF_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_tiles, p.row_blocks > 1 ? p.row_blocks : p.splits,
@@ -1022,12 +1033,19 @@ int launch_gemm_tc(dualflow_ctx* ctx, const GemmArgs& a, cudaStream_t s) {
       default: return DF_ERR_UNSUPPORTED;
     }
   }
+  // the O and QKV projections with two epilogue units per thread (PRE2)
+  const int rows_epi = a.epi == EPI_QKV ? a.m_p : m, units_epi = rows_epi * ((64 / p.splits) / 4);
+  const bool pre2 = (a.epi == EPI_ADD_F32 || a.epi == EPI_QKV) && units_epi > kThreads && units_epi <= 2 * kThreads;
   switch (a.epi) {
     case EPI_STORE_F32: return launch_epi<EPI_STORE_F32>(mw, mx, mpf, p, smem, s);
     case EPI_STORE_BF16: return launch_epi<EPI_STORE_BF16>(mw, mx, mpf, p, smem, s);
-    case EPI_ADD_F32: return launch_epi<EPI_ADD_F32>(mw, mx, mpf, p, smem, s);
+    case EPI_ADD_F32:
+      return pre2 ? launch_epi<EPI_ADD_F32, false, true>(mw, mx, mpf, p, smem, s)
+                  : launch_epi<EPI_ADD_F32>(mw, mx, mpf, p, smem, s);
     case EPI_COUPLE_ADD: return launch_epi<EPI_COUPLE_ADD>(mw, mx, mpf, p, smem, s);
-    case EPI_QKV: return launch_epi<EPI_QKV>(mw, mx, mpf, p, smem, s);
+    case EPI_QKV:
+      return pre2 ? launch_epi<EPI_QKV, false, true>(mw, mx, mpf, p, smem, s)
+                  : launch_epi<EPI_QKV>(mw, mx, mpf, p, smem, s);
     case EPI_Q2: return launch_epi<EPI_Q2>(mw, mx, mpf, p, smem, s);
     case EPI_SWIGLU: return launch_epi<EPI_SWIGLU>(mw, mx, mpf, p, smem, s);
     case EPI_MOE_GATEUP: return launch_epi<EPI_MOE_GATEUP>(mw, mx, mpf, p, smem, s);
