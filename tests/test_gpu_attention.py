@@ -2,8 +2,9 @@
 
 bf16 storage, fp32 accumulation: per-tensor max relative error <= 2e-2 against the oracle in
 mirror mode (it rounds to bf16 where the GPU stores bf16). Sizes span several 64-key tiles with
-ragged tails, empty sequences, paged caches with shuffled tables, and the two full-size
-attention workloads (the long ragged one on sampled sequences, shortest and longest included).
+ragged tails, empty sequences, equal lengths on both sides of the per-pair cut's limits, paged
+caches with shuffled tables, and the two full-size attention workloads (the long ragged one on
+sampled sequences, shortest and longest included).
 """
 import numpy as np
 import pytest
@@ -27,6 +28,10 @@ CASES = {
     "paged64_ragged": W.PAGED_RAGGED_B64.replace(**dict(SMALL, ctx_hi=700, page_size=64, n_q_heads=4)),
     "full_b8_l2048": W.ATTN_B8_L2048,
 }
+# every sequence of the same length: the per-pair cut (CTAs per pair = min(grid / pairs, tiles,
+# tiles / 8), the grid capped by the longest cache length), across the boundaries of that rule
+for _L in (1, 64, 65, 500, 576, 1024, 1088):
+    CASES[f"uniform_l{_L}"] = W.ATTN_B8_L2048.replace(**dict(SMALL, ctx_len=_L))
 
 
 def _check(run, w, rows):
