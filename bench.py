@@ -1027,7 +1027,9 @@ def sweep_topk_aux(w, ks, local_rank: int, steps: int = 20) -> list:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 600; 36 000 calls for the 18 us attention-only workload, so that the "
+                         "timed region spans the 200 ms clock samples)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layers", type=int, default=0,
@@ -1038,6 +1040,8 @@ def main():
     ap.add_argument("--sweep-topk-aux", default="",
                     help="MoE only: comma-separated auxiliary fan-outs to time as well (cost side of the decode budget)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 36000 if args.workload == "attn" and args.impl == "ours" else 600
     args.warmup = max(args.warmup, 3)
     w = workload(args.workload)
     if args.layers:
