@@ -115,13 +115,27 @@ __global__ void norm_prep_kernel(float* h, const __nv_bfloat16* E1, const __nv_b
   float* hr = h + (size_t)n * d;
   __nv_bfloat16* xr = x + (size_t)n * d;
   float s = 0.f;
-#pragma unroll 4
-  for (int q = lane * 4; q < d; q += 128) {
-    const float4 v = src ? ld4(src + q) : ld4(hr + q);
-    const float4 gg = ld4(g + q);
-    if (src) st4(hr + q, v);
-    st4(xr + q, make_float4(v.x * gg.x, v.y * gg.y, v.z * gg.z, v.w * gg.w));
-    s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  // the row in chunks of 16 vectors per lane (2048 features per warp): every load of a chunk is
+  // issued before its stores, so a chunk costs one round trip
+  for (int q0 = lane * 4; q0 < d; q0 += 16 * 128) {
+    float4 v[16], gg[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int q = q0 + 128 * j;
+      if (q < d) {
+        v[j] = src ? ld4(src + q) : ld4(hr + q);
+        gg[j] = ld4(g + q);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int q = q0 + 128 * j;
+      if (q < d) {
+        if (src) st4(hr + q, v[j]);
+        st4(xr + q, make_float4(v[j].x * gg[j].x, v[j].y * gg[j].y, v[j].z * gg[j].z, v[j].w * gg[j].w));
+        s += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+      }
+    }
   }
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (lane == 0) ss[(size_t)n * ss_ld] = s;
