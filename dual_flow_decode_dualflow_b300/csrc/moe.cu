@@ -51,6 +51,8 @@ __global__ void moe_route_kernel(const float* rlog, int B, int E, int k1, int k2
   if (b >= B) return;
   const bool live = e < E;
   const float r1 = live ? rlog[(size_t)b * E + e] : -INFINITY;
+  // the auxiliary row's logits are requested with the primary's (one round trip)
+  const float r2 = (live && aux_on) ? rlog[(size_t)(B + b) * E + e] : -INFINITY;
   const int rank = rank_of(r1, e, E);
   const bool in1 = live && rank < k1;
   const float w1 = masked_softmax(r1, in1);
@@ -67,7 +69,6 @@ __global__ void moe_route_kernel(const float* rlog, int B, int E, int k1, int k2
     return;
   }
   // auxiliary flow: the primary logits choose the set (replay), its own logits weight it
-  const float r2 = live ? rlog[(size_t)(B + b) * E + e] : -INFINITY;
   const bool in2 = live && rank < k2;
   const float w2 = masked_softmax(r2, in2);
   if (live) {
@@ -115,15 +116,27 @@ __global__ void moe_combine_kernel(const float* Y, int mrows, int d, int B, int 
   const int i = chunk * 512 + 4 * t;
   const bool live = i < d;  // d is a multiple of 4
   float4 y[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  // the residual rows, then the expert rows in chunks of kCombineLoads, each chunk's loads issued
+  // before its sums (which keep the set order)
+  constexpr int kCombineLoads = 8;
+  float4 hres[2];
+  if (live)
+    for (int f = 0; f < nf; ++f) hres[f] = *reinterpret_cast<const float4*>(h + (size_t)(f * B + b) * d + i);
   if (live) {
     for (int f = 0; f < nf; ++f) {
       const int row = f * B + b;
-      for (int j = 0; j < nsel[f]; ++j) {
-        const int e = order[f][j];
-        const float w = wts[f][j];
-        const float4 v = *reinterpret_cast<const float4*>(Y + ((size_t)e * mrows + row) * d + i);
-        y[f] = make_float4(__fmaf_rn(w, v.x, y[f].x), __fmaf_rn(w, v.y, y[f].y), __fmaf_rn(w, v.z, y[f].z),
-                           __fmaf_rn(w, v.w, y[f].w));
+      for (int j0 = 0; j0 < nsel[f]; j0 += kCombineLoads) {
+        float4 v[kCombineLoads];
+#pragma unroll
+        for (int j = 0; j < kCombineLoads; ++j)
+          if (j0 + j < nsel[f]) v[j] = *reinterpret_cast<const float4*>(Y + ((size_t)order[f][j0 + j] * mrows + row) * d + i);
+#pragma unroll
+        for (int j = 0; j < kCombineLoads; ++j)
+          if (j0 + j < nsel[f]) {
+            const float w = wts[f][j0 + j];
+            y[f] = make_float4(__fmaf_rn(w, v[j].x, y[f].x), __fmaf_rn(w, v[j].y, y[f].y),
+                               __fmaf_rn(w, v[j].z, y[f].z), __fmaf_rn(w, v[j].w, y[f].w));
+          }
       }
     }
   }
@@ -145,7 +158,7 @@ __global__ void moe_combine_kernel(const float* Y, int mrows, int d, int B, int 
     for (int f = 0; f < nf; ++f) {
       const int row = f * B + b;
       float4* hp = reinterpret_cast<float4*>(h + (size_t)row * d + i);
-      float4 hv = *hp;
+      float4 hv = hres[f];
       hv = make_float4(__fadd_rn(hv.x, y[f].x), __fadd_rn(hv.y, y[f].y), __fadd_rn(hv.z, y[f].z),
                        __fadd_rn(hv.w, y[f].w));
       *hp = hv;
