@@ -104,9 +104,22 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
 
   // ---- pass 1: online softmax triples of both flows over the slice ----
   Soft s1 = {-INFINITY, 0.f, 0.f}, s2 = {-INFINITY, 0.f, 0.f};
-  for (int i = t; i < n; i += kMixThreads) {
-    s1 = soft_add(s1, __ldg(l1 + i));
-    if (!primary_only) s2 = soft_add(s2, __ldg(l2 + i));
+  // sixteen of the thread's logits per flow requested at a time, then added in index order
+  constexpr int kMixLoads = 16;
+  for (int i0 = t; i0 < n; i0 += kMixLoads * kMixThreads) {
+    float a1[kMixLoads], a2[kMixLoads];
+#pragma unroll
+    for (int j = 0; j < kMixLoads; ++j) {
+      const int i = i0 + j * kMixThreads;
+      a1[j] = i < n ? __ldg(l1 + i) : 0.f;
+      a2[j] = (i < n && !primary_only) ? __ldg(l2 + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kMixLoads; ++j)
+      if (i0 + j * kMixThreads < n) {
+        s1 = soft_add(s1, a1[j]);
+        if (!primary_only) s2 = soft_add(s2, a2[j]);
+      }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -145,17 +158,29 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
   const int i0 = min(n, t * per), i1 = min(n, i0 + per);
   float run = 0.f, bv = -INFINITY;
   int bi = 0x7fffffff, lastpos = -1;
-  for (int i = i0; i < i1; ++i) {
-    const float p1 = expf(__ldg(l1 + i) - g1.m) * iz1;
-    const float p2 = primary_only ? 0.f : expf(__ldg(l2 + i) - g2.m) * iz2;
-    const float pm = __fmaf_rn(alpha, p1, beta * p2);
-    if (p_mix) p_mix[(size_t)b * V + lo + i] = pm;
-    if (pm > bv) {
-      bv = pm;
-      bi = lo + i;
+  for (int c0 = i0; c0 < i1; c0 += kMixLoads) {
+    float x1[kMixLoads], x2[kMixLoads];
+#pragma unroll
+    for (int j = 0; j < kMixLoads; ++j) {
+      const int i = c0 + j;
+      x1[j] = i < i1 ? __ldg(l1 + i) : 0.f;
+      x2[j] = (i < i1 && !primary_only) ? __ldg(l2 + i) : 0.f;
     }
-    if (pm > 0.f) lastpos = lo + i;
-    run = __fadd_rn(run, pm);
+#pragma unroll
+    for (int j = 0; j < kMixLoads; ++j) {
+      const int i = c0 + j;
+      if (i >= i1) continue;
+      const float p1 = expf(x1[j] - g1.m) * iz1;
+      const float p2 = primary_only ? 0.f : expf(x2[j] - g2.m) * iz2;
+      const float pm = __fmaf_rn(alpha, p1, beta * p2);
+      if (p_mix) p_mix[(size_t)b * V + lo + i] = pm;
+      if (pm > bv) {
+        bv = pm;
+        bi = lo + i;
+      }
+      if (pm > 0.f) lastpos = lo + i;
+      run = __fadd_rn(run, pm);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
