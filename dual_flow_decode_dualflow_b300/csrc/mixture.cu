@@ -288,20 +288,35 @@ __global__ void __launch_bounds__(kMixThreads) mixture_head_kernel(const float* 
 
 // After a decode step of the generation loop: every sequence's length grows by one (its new entry
 // is in the cache), and a paged sequence whose next slot opens a page gets one from the free list,
-// taken from the top in sequence order. One thread: the page assignment does not depend on
-// scheduling. A length that would reach max_ctx, a page slot beyond the table, or an empty free
+// taken from the top in sequence order. The page assignment is one thread's, so it does not depend
+// on scheduling. A length that would reach max_ctx, a page slot beyond the table, or an empty free
 // list latches DF_ERR_DEVICE_BOUNDS and leaves that sequence as it is.
 __global__ void gen_advance_kernel(int32_t* seq_len, int B, int max_ctx, int paged, int page_size, int32_t* table,
                                    int pages_per_seq, int max_pages, int32_t* free_pages, int32_t* n_free,
                                    int32_t* status) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  // every length is read at once (one round trip), then advanced; page allocation, when a next slot
+  // opens a page, stays with one thread in sequence order (the free list is taken from the top)
+  extern __shared__ int32_t next_len[];  // [B]
+  for (int b = threadIdx.x; b < B; b += blockDim.x) next_len[b] = seq_len[b] + 1;  // the next step writes slot L
+  __syncthreads();
+  if (!paged) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      const int L = next_len[b];
+      if (L < 1 || L >= max_ctx)
+        atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
+      else
+        seq_len[b] = L;
+    }
+    return;
+  }
+  if (threadIdx.x != 0) return;
   for (int b = 0; b < B; ++b) {
-    const int L = seq_len[b] + 1;  // the next step writes slot L
+    const int L = next_len[b];
     if (L < 1 || L >= max_ctx) {
       atomicCAS(status, 0, DF_ERR_DEVICE_BOUNDS);
       continue;
     }
-    if (paged && L % page_size == 0) {
+    if (L % page_size == 0) {
       const int j = L / page_size;
       int32_t* slot = table + (size_t)b * pages_per_seq + j;
       if (j >= pages_per_seq) {
@@ -431,8 +446,9 @@ int launch_release_slots(const dualflow_config& c, int32_t* seq_len, const int32
 int launch_gen_advance(const dualflow_config& c, int32_t* seq_len, int batch, int32_t* table, int32_t* free_pages,
                        int32_t* n_free, int32_t* status, cudaStream_t s) {
   const int pps = c.paged ? (c.max_ctx + c.page_size - 1) / c.page_size : 0;
-  gen_advance_kernel<<<1, 32, 0, s>>>(seq_len, batch, c.max_ctx, c.paged, c.page_size, table, pps, c.max_pages,
-                                      free_pages, n_free, status);
+  gen_advance_kernel<<<1, 256, (size_t)batch * sizeof(int32_t), s>>>(seq_len, batch, c.max_ctx, c.paged, c.page_size,
+                                                                      table, pps, c.max_pages, free_pages, n_free,
+                                                                      status);
   return cudaGetLastError() == cudaSuccess ? DF_OK : DF_ERR_CUDA;
 }
 
