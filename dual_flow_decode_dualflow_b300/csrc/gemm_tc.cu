@@ -475,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   EpiPre pre[2];
   constexpr int pre_units = (PRE2 && (EPI == EPI_ADD_F32 || EPI == EPI_QKV)) ? 2 : 1;
   const bool pre_ok = !RB && rows * nq <= pre_units * kThreads &&
-                      (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV);
+                      (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD || EPI == EPI_SWIGLU || EPI == EPI_QKV ||
+                       EPI == EPI_Q2);
   if (pre_ok && (int)threadIdx.x < rows * nq) griddep_wait();  // the operands were written by preceding kernels
 #pragma unroll
   for (int u = 0; u < pre_units; ++u) {
@@ -520,6 +521,20 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
         pre_w.c[0] = ld_bf16x4(a.vec, tile * kHeadDim + fa);
         pre_w.c[1] = ld_bf16x4(a.vec, tile * kHeadDim + fa + 64);
       }
+    } else if (EPI == EPI_Q2) {
+      // the attention-only call: row n is sequence n's auxiliary query, tile = query head
+      const int pos = a.seq_len[n];
+      pre_w.pos = pos;
+      if (pos >= 0 && pos <= a.max_ctx) {
+        const float2* cs = a.rope + (size_t)pos * 64 + fa;
+        pre_w.y1[0] = *reinterpret_cast<const float4*>(cs);
+        pre_w.y1[1] = *reinterpret_cast<const float4*>(cs + 2);
+      }
+      const size_t qi = ((size_t)n * a.n_q_heads + tile) * kHeadDim;
+      pre_w.y2[0] = ld_bf16x4(a.q1_in, qi + fa);
+      pre_w.y2[1] = ld_bf16x4(a.q1_in, qi + fa + 64);
+      pre_w.c[0] = ld_bf16x4(a.vec, tile * kHeadDim + fa);
+      pre_w.c[1] = ld_bf16x4(a.vec, tile * kHeadDim + fa + 64);
     }
   }
 
@@ -826,21 +841,24 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
         }
       } else if (EPI == EPI_Q2) {
         const int Hq = a.n_q_heads, B = a.m_a, h = tile, b = n;
-        const int pos = a.seq_len[b];
+        const int pos = pre_ok ? pu.pos : a.seq_len[b];
         if (pos < 0 || pos > a.max_ctx) {
           set_status(p.status, DF_ERR_DEVICE_BOUNDS);
         } else {
           const float2* cs = a.rope + (size_t)pos * 64 + fa;
+          const float4 cs0 = pre_ok ? pu.y1[0] : *reinterpret_cast<const float4*>(cs);
+          const float4 cs1 = pre_ok ? pu.y1[1] : *reinterpret_cast<const float4*>(cs + 2);
           const size_t qi = ((size_t)b * Hq + h) * kHeadDim;
-          const float4 x1 = ld_bf16x4(a.q1_in, qi + fa), x1p = ld_bf16x4(a.q1_in, qi + fa + 64);
+          const float4 x1 = pre_ok ? pu.y2[0] : ld_bf16x4(a.q1_in, qi + fa);
+          const float4 x1p = pre_ok ? pu.y2[1] : ld_bf16x4(a.q1_in, qi + fa + 64);
           float4 r_lo, r_hi;
-          rope4(cs, x1, x1p, r_lo, r_hi);
+          rope4_pre(cs0, cs1, x1, x1p, r_lo, r_hi);
           const size_t o1 = (((size_t)0 * B + b) * Hq + h) * kHeadDim;
           st_bf16x4(a.q_out, o1 + fa, r_lo);
           st_bf16x4(a.q_out, o1 + fa + 64, r_hi);
-          const float4 x2 = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa), x1, lo);
-          const float4 x2p = f4_fma(ld_bf16x4(a.vec, h * kHeadDim + fa + 64), x1p, hi);
-          rope4(cs, x2, x2p, r_lo, r_hi);
+          const float4 x2 = f4_fma(pre_ok ? pu.c[0] : ld_bf16x4(a.vec, h * kHeadDim + fa), x1, lo);
+          const float4 x2p = f4_fma(pre_ok ? pu.c[1] : ld_bf16x4(a.vec, h * kHeadDim + fa + 64), x1p, hi);
+          rope4_pre(cs0, cs1, x2, x2p, r_lo, r_hi);
           const size_t o2 = (((size_t)1 * B + b) * Hq + h) * kHeadDim;
           st_bf16x4(a.q_out, o2 + fa, r_lo);
           st_bf16x4(a.q_out, o2 + fa + 64, r_hi);
