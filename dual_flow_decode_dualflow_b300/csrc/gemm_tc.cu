@@ -633,8 +633,22 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     }
     units = 0;  // done: the loop below has nothing left
   }
+  // row-blocked residual epilogues (prefill): every thread walks many units whose residual rows
+  // come from HBM; L2 is asked for them kRbAhead iterations ahead, so that a unit's loads hit L2
+  constexpr int kRbAhead = 4;
+  constexpr bool kRbResidual = RB && (EPI == EPI_ADD_F32 || EPI == EPI_COUPLE_ADD);
+  auto rb_prefetch = [&](int itp) {
+    if (itp >= units) return;
+    const int np = cb + itp / nq, fp = tile * kGemmTileN + lo0 + 4 * (itp % nq);
+    const float* yp = reinterpret_cast<const float*>(a.y) + (size_t)np * a.ldy + fp;
+    if (fp < a.n_out) prefetch_l2(yp);
+    if (fp + 64 < a.n_out) prefetch_l2(yp + 64);
+  };
+  if constexpr (kRbResidual)
+    for (int j = 0; j < kRbAhead; ++j) rb_prefetch(j * kThreads + threadIdx.x);
   for (int base = 0; base < units; base += kThreads) {
     const int it = base + threadIdx.x;
+    if constexpr (kRbResidual) rb_prefetch(it + kRbAhead * kThreads);
     // this iteration's preloaded operands (with two units, a select, so that both stay in registers)
     EpiPre pu_sel;
     if constexpr (pre_units > 1) pu_sel = base != 0 ? pre[1] : pre[0];

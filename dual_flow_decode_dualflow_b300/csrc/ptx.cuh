@@ -73,6 +73,9 @@ __device__ __forceinline__ bool mbar_drain(uint64_t* full, int stages, int issue
   return ok;
 }
 
+// Asks L2 for the line holding p (no register result, nothing waits for it).
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
