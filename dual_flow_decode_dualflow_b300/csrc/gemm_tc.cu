@@ -68,7 +68,9 @@ struct GemmParams {
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) { atomicCAS(st, 0, code); }
 
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// silu with the fast exponential and division intrinsics (a few ulp in fp32, far below the bf16
+// rounding of the result; the accurate forms made the prefill gate/up epilogue ALU-latency-bound)
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ float4 ld_bf16x4(const void* p, size_t i) {
   const uint2 u = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p) + i);
