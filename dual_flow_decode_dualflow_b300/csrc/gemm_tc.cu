@@ -646,11 +646,27 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
     if (fp < a.n_out) prefetch_l2(yp);
     if (fp + 64 < a.n_out) prefetch_l2(yp + 64);
   };
-  if constexpr (kRbResidual)
+  // and each unit's residual rows are in registers one iteration before they are used
+  float4 ynx[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  auto rb_load = [&](int itn) {
+    if (itn >= units) return;
+    const int nn = cb + itn / nq, fn = tile * kGemmTileN + lo0 + 4 * (itn % nq);
+    const float* yp = reinterpret_cast<const float*>(a.y) + (size_t)nn * a.ldy + fn;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh)
+      if (fn + 64 * hh < a.n_out) ynx[hh] = *reinterpret_cast<const float4*>(yp + 64 * hh);
+  };
+  if constexpr (kRbResidual) {
     for (int j = 0; j < kRbAhead; ++j) rb_prefetch(j * kThreads + threadIdx.x);
+    rb_load(threadIdx.x);
+  }
   for (int base = 0; base < units; base += kThreads) {
     const int it = base + threadIdx.x;
-    if constexpr (kRbResidual) rb_prefetch(it + kRbAhead * kThreads);
+    float4 ycur[2] = {ynx[0], ynx[1]};
+    if constexpr (kRbResidual) {
+      rb_prefetch(it + kRbAhead * kThreads);
+      rb_load(it + kThreads);
+    }
     // this iteration's preloaded operands (with two units, a select, so that both stay in registers)
     EpiPre pu_sel;
     if constexpr (pre_units > 1) pu_sel = base != 0 ? pre[1] : pre[0];
@@ -678,7 +694,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
         for (int hh = 0; hh < 2; ++hh) {
           const int f = fg + 64 * hh;
           if (f >= a.n_out) continue;
-          const float4 hv = f4_add(pre_ok ? pu.y1[hh] : *reinterpret_cast<const float4*>(y + f), hh ? hi : lo);
+          const float4 hv = f4_add(kRbResidual ? ycur[hh] : pre_ok ? pu.y1[hh] : *reinterpret_cast<const float4*>(y + f),
+                                   hh ? hi : lo);
           *reinterpret_cast<float4*>(y + f) = hv;
           st_bf16x4(a.x_next, (size_t)n * a.n_out + f, f4_mul(hv, pre_ok ? pu.g[hh] : ld_bf16x4(a.g_next, f)));
           ss0 = f4_sumsq_acc(ss0, hv);
@@ -700,7 +717,8 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
           const float4 z2 = hh ? z2hi : z2lo;
           if (p.vec_ok && f + 3 < a.n_out) {
             float* y1 = reinterpret_cast<float*>(a.y) + (size_t)n * a.ldy + f;
-            const float4 h1 = f4_add(pre_ok ? pu.y1[hh] : *reinterpret_cast<const float4*>(y1), z1);
+            const float4 h1 =
+                f4_add(kRbResidual ? ycur[hh] : pre_ok ? pu.y1[hh] : *reinterpret_cast<const float4*>(y1), z1);
             *reinterpret_cast<float4*>(y1) = h1;
             float4 h2 = make_float4(0.f, 0.f, 0.f, 0.f);
             if (a.m_a > 0) {
