@@ -410,10 +410,21 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
       }
     }
     umma_commit(done);
-  } else if (warp >= 2 && (a.ss_in != nullptr || a.sel_pos != nullptr)) {
+  } else if (warp >= 2 && (a.ss_in != nullptr || a.sel_pos != nullptr || EPI == EPI_PREFILL_QKV)) {
     // idle during the main loop: which rows selected this launch's expert (grouped launches) and
     // 1 / rms of every activation row, from the producer's partials
     griddep_wait();
+    if (EPI == EPI_PREFILL_QKV) {
+      // every row's cache slot and position (prompt token t of prompt sequence i is activation row
+      // i * seq_rows + t, held by cache slot b = slots[i], at position seq_len[b] + t): the
+      // epilogue's units then start from shared memory instead of two dependent global loads
+      for (int n = threadIdx.x - 64; n < m; n += 64) {
+        const int grow = a.row_base + n, si = grow / a.seq_rows, b = a.slots ? a.slots[si] : si;
+        const bool slot_ok = b >= 0 && b < a.max_batch;
+        sel_list[n] = b;
+        sel_s[n] = slot_ok ? a.seq_len[b] + grow % a.seq_rows : -1;
+      }
+    }
     if (a.sel_pos != nullptr) {
       for (int n = threadIdx.x - 64; n < m; n += 64) sel_s[n] = a.sel_pos[(size_t)n * a.n_groups + grp] >= 0;
       if (warp == 2) {
@@ -843,9 +854,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
         // prompt token t of prompt sequence i (activation row i * seq_rows + t), held by cache slot
         // b = slots[i], at position seq_len[b] + t
         const int Hq = a.n_q_heads, Hkv = a.n_kv_heads, grow = a.row_base + n;
-        const int si = grow / a.seq_rows, b = a.slots ? a.slots[si] : si;
-        const bool slot_ok = b >= 0 && b < a.max_batch;
-        const int pos = slot_ok ? a.seq_len[b] + grow % a.seq_rows : -1;
+        const int b = sel_list[n], pos = sel_s[n];  // staged by the idle warps (see above)
         if (pos < 0 || pos >= a.max_ctx) {
           set_status(p.status, DF_ERR_DEVICE_BOUNDS);
         } else {
