@@ -941,6 +941,10 @@ int dualflow_mixture_head(dualflow_ctx* ctx, const float* logits, int32_t batch,
   return launch_mixture_head(logits, batch, ctx->cfg.vocab, u, alpha, p_mix, token, nullptr, 1, S(stream));
 }
 
+static int generate_loop(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, int32_t batch,
+                         int32_t n_steps, const float* u, int32_t* tokens_out, float* logits, float* logits_all,
+                         int32_t* free_pages, int32_t* n_free, int32_t aux_on, dualflow_stream stream);
+
 int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, const int32_t* tokens,
                       int32_t batch, int32_t n_steps, const float* u, int32_t* tokens_out, float* logits,
                       float* logits_all, int32_t* free_pages, int32_t* n_free, int32_t aux_on,
@@ -949,11 +953,21 @@ int dualflow_generate(dualflow_ctx* ctx, const dualflow_weights* w, const dualfl
   if (aux_on != 0 && aux_on != 1) return DF_ERR_ARG;
   if (batch <= 0 || batch > ctx->cfg.max_batch || n_steps < 0) return DF_ERR_SHAPE;
   if (n_steps == 0) return DF_OK;
+  // the loop's own token buffer (the host variant copies the first tokens there directly)
+  if (tokens != ctx->gen_tokens &&
+      cudaMemcpyAsync(ctx->gen_tokens, tokens, (size_t)batch * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                      S(stream)) != cudaSuccess)
+    return DF_ERR_CUDA;
+  return generate_loop(ctx, w, kv, batch, n_steps, u, tokens_out, logits, logits_all, free_pages, n_free, aux_on,
+                       stream);
+}
+
+// The decode loop on the tokens already in ctx->gen_tokens.
+static int generate_loop(dualflow_ctx* ctx, const dualflow_weights* w, const dualflow_kv* kv, int32_t batch,
+                         int32_t n_steps, const float* u, int32_t* tokens_out, float* logits, float* logits_all,
+                         int32_t* free_pages, int32_t* n_free, int32_t aux_on, dualflow_stream stream) {
   const dualflow_config& c = ctx->cfg;
   cudaStream_t s = S(stream);
-  if (cudaMemcpyAsync(ctx->gen_tokens, tokens, (size_t)batch * sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
-      cudaSuccess)
-    return DF_ERR_CUDA;
   const size_t per_step = (size_t)2 * batch * c.vocab;
   // the step reads the loop's own token buffer, so every step replays the same captured graph
   for (int t = 0; t < n_steps; ++t) {
@@ -1228,11 +1242,13 @@ int dualflow_generate_host(dualflow_ctx* ctx, const dualflow_weights* w, const d
   if (n_steps == 0) return DF_OK;
   cudaStream_t s = S(stream);
   const size_t nb = (size_t)batch * sizeof(int32_t), total = (size_t)n_steps * batch;
-  if (cudaMemcpyAsync(ctx->tokens_dev, tokens_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess) return DF_ERR_CUDA;
+  if (!kv || !kv->seq_len || (aux_on != 0 && aux_on != 1)) return DF_ERR_ARG;
+  // the first tokens go straight into the loop's own token buffer
+  if (cudaMemcpyAsync(ctx->gen_tokens, tokens_host, nb, cudaMemcpyHostToDevice, s) != cudaSuccess) return DF_ERR_CUDA;
   if (u_host && cudaMemcpyAsync(ctx->gen_u_dev, u_host, total * sizeof(float), cudaMemcpyHostToDevice, s) != cudaSuccess)
     return DF_ERR_CUDA;
-  DF_TRY(dualflow_generate(ctx, w, kv, ctx->tokens_dev, batch, n_steps, u_host ? ctx->gen_u_dev : nullptr,
-                           ctx->gen_out_dev, ctx->logits_dev, nullptr, nullptr, nullptr, aux_on, stream));
+  DF_TRY(generate_loop(ctx, w, kv, batch, n_steps, u_host ? ctx->gen_u_dev : nullptr, ctx->gen_out_dev,
+                       ctx->logits_dev, nullptr, nullptr, nullptr, aux_on, stream));
   if (cudaMemcpyAsync(tokens_out_host, ctx->gen_out_dev, total * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
       cudaSuccess)
     return DF_ERR_CUDA;
