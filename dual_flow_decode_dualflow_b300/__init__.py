@@ -25,8 +25,8 @@ C_FUNCTIONS = ("dualflow_init", "dualflow_free", "dualflow_status_string", "dual
                "dualflow_set_graphs", "dualflow_set_profiling", "dualflow_profile_read", "dualflow_sync_status",
                "dualflow_decode_attention_noalloc", "dualflow_expert_ids", "dualflow_mixture_head",
                "dualflow_generate", "dualflow_generate_host", "dualflow_prefill_reserve", "dualflow_prefill",
-               "dualflow_prefill_slots", "dualflow_release_slots", "dualflow_set_nvtx", "dualflow_set_wait_limit",
-               "dualflow_router_logits", "dualflow_cuda_error_string")
+               "dualflow_prefill_slots", "dualflow_release_slots", "dualflow_set_nvtx", "dualflow_set_call_chaining",
+               "dualflow_set_wait_limit", "dualflow_router_logits", "dualflow_cuda_error_string")
 DF_PROF_FAMILIES = 8
 DF_NOALLOC_MAX_PAIRS = 512  # the header's limit of batch * n_kv_heads for the context-free attention
 PROF_NAMES = ("norm", "qkv", "attention", "o_proj", "gate_up", "down", "lm_head", "other")
@@ -100,6 +100,7 @@ def load_library(path: str = LIB_PATH):
         "dualflow_generate_host": ([vp, POINTER(dualflow_weights), POINTER(dualflow_kv), vp, i32, i32, vp, vp, i32, vp],
                                    i32),
         "dualflow_set_nvtx": ([vp, i32], i32),
+        "dualflow_set_call_chaining": ([vp, i32], i32),
         "dualflow_set_wait_limit": ([vp, ctypes.c_int64], i32),
         "dualflow_router_logits": ([vp, vp, i32, vp], i32),
         "dualflow_cuda_error_string": ([], ctypes.c_char_p),
@@ -207,6 +208,11 @@ def dualflow_set_profiling(ctx, mode: int) -> None:
     """0: off; 1: CUDA event pair around every launch (serialising); 2: in-graph end stamps, each
     launch's share of the step (no serialisation)."""
     _check("dualflow_set_profiling", load_library().dualflow_set_profiling(ctx, mode))
+
+
+def dualflow_set_call_chaining(ctx, enabled: int) -> None:
+    """Chains dualflow_decode_attention's first kernel to the caller's preceding kernel (see the header)."""
+    _check("dualflow_set_call_chaining", load_library().dualflow_set_call_chaining(ctx, enabled))
 
 
 def dualflow_set_nvtx(ctx, enabled: int) -> None:

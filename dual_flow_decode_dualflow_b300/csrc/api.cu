@@ -829,12 +829,15 @@ int dualflow_decode_attention(dualflow_ctx* ctx, const void* q1, const void* h2,
   const dualflow_config& c = ctx->cfg;
   cudaStream_t s = S(stream);
   if (c.dtype == DF_DTYPE_BF16) {
-    // On a caller's stream the two launches are chained by programmatic dependent launch, as in
-    // the step: the attention requests its first K/V stages while the query projection runs.
+    // On a caller's stream the attention is chained to the call's first launch by programmatic
+    // dependent launch, as in the step: it requests its first K/V stages while the query
+    // projection runs. The first launch itself waits for the caller's preceding work in the usual
+    // way (unless the caller enabled chaining), so nothing this call reads early (weights, cached
+    // K/V) can be older than that work.
     const int pdl = s != nullptr ? 1 : 0;
     if (aux_on) {
       GemmArgs g = gemm_args(ctx);
-      g.pdl = pdl;
+      g.pdl = ctx->chain_calls ? pdl : 0;
       g.x = h2;
       g.W = Wq;
       g.n_out = c.n_q_heads * c.head_dim;
@@ -1311,6 +1314,12 @@ int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches, int32
       }
     }
   }
+  return DF_OK;
+}
+
+int dualflow_set_call_chaining(dualflow_ctx* ctx, int32_t enabled) {
+  if (!ctx || (enabled != 0 && enabled != 1)) return DF_ERR_ARG;
+  ctx->chain_calls = enabled;
   return DF_OK;
 }
 

@@ -196,6 +196,7 @@ struct dualflow_ctx {
   // limit of the bounded pipeline waits (ns); 0 = the library default. Failure-path tests only.
   unsigned long long wait_ns = 0;
   int nvtx = 0;  // NVTX ranges around the step's layers and launches
+  int chain_calls = 0;  // dualflow_set_call_chaining
 };
 
 namespace df {

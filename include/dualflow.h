@@ -165,7 +165,9 @@ DF_API const char* dualflow_cuda_error_string(void);
  * Nothing is appended. q1 [batch, Hq, D] (raw primary query projection), h2 [batch, d]
  * (auxiliary flow's normed input), Wq [Hq D, d], a [Hq D]: device, storage dtype.
  * o: device [2, batch, Hq, D], storage dtype (aux rows written only when aux_on).
- * seq_len[b] == 0 yields o = 0 for that row. Every K1/V1 tile is read once for both flows. */
+ * seq_len[b] == 0 yields o = 0 for that row. Every K1/V1 tile is read once for both flows.
+ * The call's first kernel waits for the caller's preceding work on the stream in the usual way
+ * (unless dualflow_set_call_chaining enabled chaining); its second is chained to its first. */
 DF_API int dualflow_decode_attention(dualflow_ctx* ctx, const void* q1, const void* h2, const void* Wq, const void* a,
                               const dualflow_kv* kv, int32_t layer, int32_t batch, void* o, int32_t aux_on,
                               dualflow_stream stream);
@@ -362,6 +364,13 @@ DF_API int dualflow_set_profiling(dualflow_ctx* ctx, int32_t mode);
  * (all 0 in mode 0). Either array may be NULL; n_families entries are written (at most
  * DF_PROF_FAMILIES). With graphs on, the last step is the last replay of the last captured graph. */
 DF_API int dualflow_profile_read(dualflow_ctx* ctx, float* ms, int32_t* launches, int32_t n_families);
+
+/* Enables (1) or disables (0, default) chaining of dualflow_decode_attention's first kernel to the
+ * kernel that precedes the call on a non-NULL stream, by programmatic dependent launch: the call
+ * then starts while that kernel finishes, and may read Wq and the cached K/V of positions below
+ * seq_len[b] before that kernel's writes are visible. Only for callers whose preceding kernel
+ * writes none of them (back-to-back calls of this library qualify: they write o only). */
+DF_API int dualflow_set_call_chaining(dualflow_ctx* ctx, int32_t enabled);
 
 /* Enables (1) or disables (0, default) NVTX ranges: one per layer of dualflow_step and one per
  * kernel launch, named after the families above. They are host-side ranges around the launches,

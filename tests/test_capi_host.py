@@ -82,6 +82,7 @@ def test_null_arguments_rejected():
     assert lib.dualflow_prefill_slots(None, None, None, None, None, 1, 1, None, None, None) == dfl.DF_ERR_ARG
     assert lib.dualflow_release_slots(None, None, None, 1, None, None, None) == dfl.DF_ERR_ARG
     assert lib.dualflow_set_nvtx(None, 1) == dfl.DF_ERR_ARG
+    assert lib.dualflow_set_call_chaining(None, 1) == dfl.DF_ERR_ARG
     assert lib.dualflow_set_wait_limit(None, 0) == dfl.DF_ERR_ARG
     assert lib.dualflow_router_logits(None, None, 1, None) == dfl.DF_ERR_ARG
 

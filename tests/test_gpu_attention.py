@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import dual_flow_decode_dualflow_b300 as dfl
 from dfsynth import workloads as W
 from tests import gpu_harness as H
 
@@ -58,8 +59,17 @@ def test_attention_parity(cuda_device, name):
         assert run.status() == 0
         assert torch.equal(run.o[0], o_dual[0])
         assert torch.isnan(run.o[1].float()).all()
-        # repeated calls are deterministic
+        # repeated calls are deterministic, also chained to the preceding call on a stream
         run.attention(aux_on=1)
+        assert torch.equal(run.o, o_dual)
+        s = torch.cuda.Stream()
+        dfl.dualflow_set_call_chaining(run.ctx, 1)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                run.attention(aux_on=1, stream=s)
+        s.synchronize()
+        dfl.dualflow_set_call_chaining(run.ctx, 0)
+        assert run.status() == 0
         assert torch.equal(run.o, o_dual)
     finally:
         run.close()
