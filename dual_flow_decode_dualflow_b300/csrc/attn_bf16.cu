@@ -13,9 +13,10 @@
 //
 // Work split (flash-decoding): all (b, g, tile) triples are laid end to end and cut into equal
 // contiguous ranges, one per CTA, so ragged lengths balance across the GPU. When every pair has the
-// same length and the grid holds k >= 1 CTAs per pair, each pair goes to k CTAs instead, CTA j
-// taking the pair's tiles j, j + k, j + 2k, ...: no CTA changes pair, and the pair's CTAs stream
-// through its cache rows side by side. A pair cut across
+// same length T tiles and the grid holds at least one CTA per pair, each pair goes to
+// k = min(grid / pairs, T, max(1, T / 8)) CTAs instead, CTA j taking the pair's tiles j, j + k,
+// j + 2k, ...: no CTA changes pair, and the pair's CTAs stream through its cache rows side by side.
+// A pair cut across
 // several CTAs writes per-CTA partials (O, max, sum); the last CTA to arrive (atomic counter, no
 // waiting) merges them in CTA order, with all four consumer warps, so the result does not depend
 // on arrival order. The query rows of a pair reach shared memory by bulk copy with the pair's

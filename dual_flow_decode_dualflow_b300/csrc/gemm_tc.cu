@@ -28,6 +28,9 @@
 //   EPI_ADD_F32 / EPI_STORE_F32 / EPI_STORE_BF16  residual update, logits, plain stores
 //   EPI_MOE_GATEUP / EPI_MOE_DOWN  one expert per grid.z: SWIGLU (with b where both flows chose the
 //                expert) or a plain fp32 store, for the rows whose routing selected that expert
+//                (the epilogue walks a compact list of those rows)
+// The epilogue operands that do not depend on the accumulator (residual rows, the next norm's gain,
+// coupling vectors, rotary angles) are loaded while the MMAs run, one or two units per thread.
 //
 // RMSNorm across kernels (decode step). RMSNorm(h) . W^T = (1/rms(h)) ((h (*) g) . W^T): a residual
 // epilogue that has just produced h also writes x_next = bf16(h (*) g_next) and, per row, the sum
