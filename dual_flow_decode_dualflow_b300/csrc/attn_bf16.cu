@@ -536,9 +536,16 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
           const float* part0 = P.part + (size_t)(p + first) * kAttnPartFloats;
           const int n = last - first + 1;
           float M = NEG_INF;
+#pragma unroll 4
+          for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(part0 + (size_t)k * kAttnPartFloats + 8 * kHeadDim + r));
           float den = 0.f;
           float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          auto add = [&](float mv, float lv, float4 v0, float4 v1) {
+#pragma unroll 4
+          for (int k = 0; k < n; ++k) {
+            const float* sl = part0 + (size_t)k * kAttnPartFloats;
+            const float mv = __ldcg(sl + 8 * kHeadDim + r), lv = __ldcg(sl + 8 * kHeadDim + 8 + r);
+            const float4 v0 = __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0));
+            const float4 v1 = __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0 + 4));
             const float wt = (M == NEG_INF) ? 0.f : exp2f(mv - M);
             den += lv * wt;
             acc[0] += v0.x * wt;
@@ -549,37 +556,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attn_bf16_kernel(const __grid
             acc[5] += v1.y * wt;
             acc[6] += v1.z * wt;
             acc[7] += v1.w * wt;
-          };
-          if (n <= 4) {
-            // up to four partials (the per-pair cut): every load issued before the first use,
-            // one round trip to L2; the same maximum and the same order of sums as below
-            float mv[4], lv[4];
-            float4 va[4], vb[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (k < n) {
-                const float* sl = part0 + (size_t)k * kAttnPartFloats;
-                mv[k] = __ldcg(sl + 8 * kHeadDim + r);
-                lv[k] = __ldcg(sl + 8 * kHeadDim + 8 + r);
-                va[k] = __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0));
-                vb[k] = __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0 + 4));
-              }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (k < n) M = fmaxf(M, mv[k]);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              if (k < n) add(mv[k], lv[k], va[k], vb[k]);
-          } else {
-#pragma unroll 4
-            for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(part0 + (size_t)k * kAttnPartFloats + 8 * kHeadDim + r));
-#pragma unroll 4
-            for (int k = 0; k < n; ++k) {
-              const float* sl = part0 + (size_t)k * kAttnPartFloats;
-              add(__ldcg(sl + 8 * kHeadDim + r), __ldcg(sl + 8 * kHeadDim + 8 + r),
-                  __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0)),
-                  __ldcg(reinterpret_cast<const float4*>(sl + r * kHeadDim + d0 + 4)));
-            }
           }
           const int f = r / G, hh = r % G;
           if (r < 2 * G && (f == 0 || a.aux_on)) {
