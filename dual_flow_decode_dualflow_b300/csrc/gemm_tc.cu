@@ -617,15 +617,19 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
   const bool listed = kListed && !RB && S == 1 && a.sel_pos != nullptr;
   if (listed) units = (int)tmem_slot[3] * nq;
   if (EPI == EPI_SWIGLU && !RB && S > 1 && units <= 2 * kThreads) {
-    // gate/up of a split launch with up to two units per thread: every partial load of both units
-    // is issued before any of their arithmetic, so the exchange costs one round trip to L2
-    float4 lo[2], hi[2], g2[2], p2[2];
+    // gate/up of a split launch with up to two units per thread: every partial load of both units,
+    // and the coupling vector b, is issued before any of their arithmetic, so the exchange costs
+    // one round trip to L2
+    float4 lo[2], hi[2], g2[2], p2[2], bv[2];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       const int it = u * kThreads + threadIdx.x, n = it / nq, qd = it % nq;
       if (it < units) {
         reduce_pair(red, lo0, n, qd, lo[u], hi[u]);
-        if (a.m_a > 0) reduce_pair(red, lo0, a.m_p + n, qd, g2[u], p2[u]);
+        if (a.m_a > 0) {
+          reduce_pair(red, lo0, a.m_p + n, qd, g2[u], p2[u]);
+          bv[u] = ld_bf16x4(a.vec, tile * 64 + lo0 + 4 * qd);
+        }
       }
     }
 #pragma unroll
@@ -644,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, min_ctas_per_sm<EPI>())
           g2[u] = f4_scale(g2[u], rstd_s[a.m_p + n]);
           p2[u] = f4_scale(p2[u], rstd_s[a.m_p + n]);
         }
-        st_bf16x4(a.y, (size_t)(a.m_p + n) * a.ldy + j, f4_fma(ld_bf16x4(a.vec, j), u1, f4_silu_mul(g2[u], p2[u])));
+        st_bf16x4(a.y, (size_t)(a.m_p + n) * a.ldy + j, f4_fma(bv[u], u1, f4_silu_mul(g2[u], p2[u])));
       }
     }
     units = 0;  // done: the loop below has nothing left
